@@ -1,0 +1,313 @@
+"""Pins of the CPU oracle to facts that do not come from the oracle itself.
+
+Each check is chosen so that a plausible slip in the oracle (a dropped term,
+a wrong sign or index, a transposed operand, a wrong rounding) fails at least
+one of them: library routines (numpy matmul / sort / bincount), brute force on
+tiny inputs, closed forms, and cases worked out by hand.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+
+
+# ---- an independent bf16 rounding (numpy frexp + rint, half to even) ---------
+
+def np_round_bf16(v: np.ndarray) -> np.ndarray:
+    """Nearest bf16 value (as float64) of each double, ties to even (normals)."""
+    v = np.asarray(v, dtype=np.float64)
+    m, e = np.frexp(v)
+    return np.ldexp(np.rint(np.ldexp(m, 8)), e - 8)
+
+
+def bits_of(vals: np.ndarray) -> np.ndarray:
+    return (np.asarray(vals, dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def as_bf16_bits(vals):
+    """Exact bf16 bit patterns of values that are representable in bf16."""
+    v = np.asarray(vals, dtype=np.float64)
+    assert np.all(np_round_bf16(v) == v)
+    return bits_of(v)
+
+
+def rand_bf16(rng, shape, scale=1.0):
+    return bits_of(np_round_bf16(rng.standard_normal(shape) * scale))
+
+
+def f64(bits):
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def np_silu(z):
+    return z / (1.0 + np.exp(-z))
+
+
+def np_ffn(x, wg, wu, wd):
+    """One expert on one token with numpy: Wd . bf16(silu(Wg x) * (Wu x))."""
+    g = f64(wg) @ f64(x)
+    u = f64(wu) @ f64(x)
+    h = np_round_bf16(np_silu(g) * u)
+    return h, f64(wd) @ h
+
+
+# ---- bf16 -----------------------------------------------------------------------
+
+def test_bf16_decode_matches_float32_reinterpretation():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    got = oracle.bf16_to_f64(bits)
+    finite = np.isfinite(ref)
+    assert np.array_equal(got[finite], ref[finite])
+
+
+def test_bf16_round_trip_exhaustive():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    vals = oracle.bf16_to_f64(bits)
+    finite = np.isfinite(vals)
+    back = oracle.f64_to_bf16(vals[finite])
+    assert np.array_equal(back, bits[finite])
+
+
+@pytest.mark.parametrize("value,expect", [
+    (1.0 + 2.0 ** -8, 0x3F80),                 # half-way, even neighbour below
+    (1.0 + 3 * 2.0 ** -8, 0x3F82),             # half-way, even neighbour above
+    (-(1.0 + 2.0 ** -8), 0xBF80),
+    (1.0 + 2.0 ** -8 + 2.0 ** -40, 0x3F81),    # just above half-way
+    (1.0 + 2.0 ** -8 - 2.0 ** -40, 0x3F80),    # just below half-way
+    (2.0 ** -133, 0x0001),                     # smallest subnormal
+    (1.5 * 2.0 ** -133, 0x0002),               # subnormal tie -> even
+    (0.5 * 2.0 ** -133, 0x0000),               # tie with zero -> even (zero)
+    ((2 - 2.0 ** -7) * 2.0 ** 127, 0x7F7F),    # largest finite
+    ((2 - 2.0 ** -8) * 2.0 ** 127, 0x7F80),    # tie above largest -> even = inf
+    (-0.0, 0x8000),
+    (3.0, 0x4040),
+])
+def test_bf16_rounding_cases(value, expect):
+    assert int(oracle.f64_to_bf16(np.array([value]))[0]) == expect
+
+
+def test_bf16_rounding_matches_frexp_rint():
+    rng = np.random.default_rng(1)
+    v = rng.standard_normal(200000) * np.exp(rng.uniform(-20, 20, 200000))
+    got = oracle.bf16_to_f64(oracle.f64_to_bf16(v))
+    assert np.array_equal(got, np_round_bf16(v))
+
+
+def test_silu_closed_form():
+    assert oracle.silu(0.0) == 0.0
+    assert abs(oracle.silu(40.0) - 40.0) < 1e-12
+    assert abs(oracle.silu(-40.0)) < 1e-15
+    assert abs(oracle.silu(1.0) - 1.0 / (1.0 + math.e ** -1)) < 1e-15
+    # silu(z) - silu(-z) = z
+    for z in (0.3, 1.7, 5.0):
+        assert abs(oracle.silu(z) - oracle.silu(-z) - z) < 1e-14
+
+
+# ---- router and top-k -----------------------------------------------------------
+
+def test_router_logits_match_numpy_matmul():
+    rng = np.random.default_rng(2)
+    T, d, E = 7, 40, 5
+    x = rand_bf16(rng, (T, d))
+    wr = rand_bf16(rng, (E, d), 0.2)
+    b = rng.standard_normal(E).astype(np.float32)
+    L = oracle.router_logits(x, wr, b)
+    ref = f64(x) @ f64(wr).T + b.astype(np.float64)
+    assert np.allclose(L, ref, rtol=1e-13, atol=1e-13)
+    L0 = oracle.router_logits(x, wr, None)
+    assert np.allclose(L0, f64(x) @ f64(wr).T, rtol=1e-13, atol=1e-13)
+
+
+@pytest.mark.parametrize("E,k", [(8, 2), (16, 5), (6, 6), (1, 1), (32, 8)])
+def test_topk_brute_force_sort(E, k):
+    rng = np.random.default_rng(E * 100 + k)
+    T = 50
+    L = rng.standard_normal((T, E))
+    L[3, :] = 0.25  # all tied: lower expert index first
+    if E > 2:
+        L[4, 1] = L[4, 2] = 3.0  # a tie at the top
+    idx, w, p, gap = oracle.topk(L, k)
+    for t in range(T):
+        order = sorted(range(E), key=lambda e: (-L[t, e], e))
+        assert list(idx[t]) == order[:k]
+        kept = np.exp(L[t, order[:k]] - L[t].max())
+        assert np.allclose(w[t], kept / kept.sum(), rtol=1e-13, atol=0)
+        if k < E:
+            assert gap[t] == pytest.approx(L[t, order[k - 1]] - L[t, order[k]], abs=1e-15)
+    assert np.allclose(w.sum(axis=1), 1.0, atol=1e-12)
+    ex = np.exp(L - L.max(axis=1, keepdims=True))
+    assert np.allclose(p, ex / ex.sum(axis=1, keepdims=True), rtol=1e-13)
+
+
+def test_topk_with_k_equal_E_is_full_softmax():
+    rng = np.random.default_rng(3)
+    L = rng.standard_normal((9, 7)) * 3
+    idx, w, p, _ = oracle.topk(L, 7)
+    full = np.zeros_like(L)
+    for t in range(9):
+        full[t, idx[t]] = w[t]
+    ex = np.exp(L - L.max(axis=1, keepdims=True))
+    assert np.allclose(full, ex / ex.sum(axis=1, keepdims=True), rtol=1e-13)
+
+
+def test_topk_hand_example_renormalisation():
+    # logits 0, ln 2, ln 3: softmax is (1, 2, 3)/6; the top two are experts 2
+    # and 1, renormalised to 3/5 and 2/5.
+    x = as_bf16_bits([[1.0]])
+    wr = as_bf16_bits([[0.0], [0.0], [0.0]])
+    b = np.array([0.0, math.log(2.0), math.log(3.0)], dtype=np.float32)
+    r = oracle.route(x, wr, b, 2)
+    assert list(r["idx"][0]) == [2, 1]
+    assert np.allclose(r["w"][0], [0.6, 0.4], atol=1e-6)
+    assert np.allclose(r["p"][0], [1 / 6, 2 / 6, 3 / 6], atol=1e-6)
+
+
+# ---- permutation ------------------------------------------------------------------
+
+def test_permute_hand_example():
+    idx = np.array([[2, 0], [0, 1], [2, 1]], dtype=np.int32)
+    counts, offsets, perm, pos = oracle.permute(idx, 3)
+    assert list(counts) == [2, 2, 2]
+    assert list(offsets) == [0, 2, 4, 6]
+    assert list(perm) == [0, 1, 1, 2, 0, 2]
+    assert pos.tolist() == [[4, 0], [1, 2], [5, 3]]
+
+
+@pytest.mark.parametrize("T,E,k", [(1, 1, 1), (37, 8, 2), (64, 16, 5), (200, 64, 6), (5, 9, 9)])
+def test_permute_invariants(T, E, k):
+    rng = np.random.default_rng(T + E + k)
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    counts, offsets, perm, pos = oracle.permute(idx, E)
+    assert np.array_equal(counts, np.bincount(idx.ravel(), minlength=E))
+    assert counts.sum() == T * k
+    assert offsets[0] == 0 and offsets[E] == T * k and np.all(np.diff(offsets) == counts)
+    assert np.array_equal(np.sort(pos.ravel()), np.arange(T * k))       # bijection
+    for t in range(T):
+        for j in range(k):
+            r = pos[t, j]
+            assert perm[r] == t
+            e = idx[t, j]
+            assert offsets[e] <= r < offsets[e + 1]
+    for e in range(E):
+        seg = perm[offsets[e]:offsets[e + 1]]
+        assert np.all(np.diff(seg) > 0)  # tokens ascending, each once
+        assert set(seg.tolist()) == {t for t in range(T) if e in idx[t]}
+
+
+def test_permute_rejects_bad_indices():
+    with pytest.raises(ValueError):
+        oracle.permute(np.array([[0, 0]], dtype=np.int32), 4)
+    with pytest.raises(ValueError):
+        oracle.permute(np.array([[5]], dtype=np.int32), 4)
+
+
+# ---- experts and the whole layer ------------------------------------------------------
+
+def test_expert_ffn_matches_numpy():
+    rng = np.random.default_rng(4)
+    d, f = 24, 40
+    x = rand_bf16(rng, (d,))
+    wg = rand_bf16(rng, (f, d), d ** -0.5)
+    wu = rand_bf16(rng, (f, d), d ** -0.5)
+    wd = rand_bf16(rng, (d, f), f ** -0.5)
+    h, y = oracle.expert_ffn(x, wg, wu, wd)
+    h_ref, y_ref = np_ffn(x, wg, wu, wd)
+    # h can differ only where silu(g)*u sits exactly on a bf16 half-way point
+    assert np.array_equal(h, h_ref)
+    assert np.allclose(y, y_ref, rtol=1e-12, atol=1e-13)
+
+
+def test_layer_hand_computed():
+    # T=1, d=2, f=1, E=2, k=1.  x = (1, 2); router = identity -> logits (1, 2),
+    # expert 1 wins with weight 1.  g = 0.5*1 + 0.25*2 = 1, u = 1 + 2 = 3,
+    # h = bf16(silu(1) * 3) = bf16(2.19317...) = 2.1875, y = (2.1875, -1.09375).
+    x = as_bf16_bits([[1.0, 2.0]])
+    wr = as_bf16_bits([[1.0, 0.0], [0.0, 1.0]])
+    wg = as_bf16_bits([[[3.0, -1.0]], [[0.5, 0.25]]])
+    wu = as_bf16_bits([[[1.0, 1.0]], [[1.0, 1.0]]])
+    wd = as_bf16_bits([[[7.0], [7.0]], [[1.0], [-0.5]]])
+    out, acc = oracle.layer(x, wr, None, wg, wu, wd, k=1)
+    assert out[0].tolist() == [0x400C, 0xBF8C]
+    assert acc[0].tolist() == [2.1875, -1.09375]
+
+
+def _tiny_layer(rng, T, d, E, f, S=0, identical=False):
+    x = rand_bf16(rng, (T, d))
+    wr = rand_bf16(rng, (E, d), d ** -0.5)
+    b = (rng.standard_normal(E) * 0.3).astype(np.float32)
+    n = E + S
+    if identical:
+        wg = np.repeat(rand_bf16(rng, (1, f, d), d ** -0.5), n, axis=0)
+        wu = np.repeat(rand_bf16(rng, (1, f, d), d ** -0.5), n, axis=0)
+        wd = np.repeat(rand_bf16(rng, (1, d, f), f ** -0.5), n, axis=0)
+    else:
+        wg = rand_bf16(rng, (n, f, d), d ** -0.5)
+        wu = rand_bf16(rng, (n, f, d), d ** -0.5)
+        wd = rand_bf16(rng, (n, d, f), f ** -0.5)
+    return x, wr, b, wg, wu, wd
+
+
+@pytest.mark.parametrize("T,d,E,f", [(8, 32, 4, 32), (5, 16, 3, 24), (3, 8, 2, 12)])
+def test_layer_k_equal_E_is_dense_mixture(T, d, E, f):
+    rng = np.random.default_rng(T * d + E * f)
+    x, wr, b, wg, wu, wd = _tiny_layer(rng, T, d, E, f)
+    out, acc = oracle.layer(x, wr, b, wg, wu, wd, k=E)
+    L = f64(x) @ f64(wr).T + b.astype(np.float64)
+    p = np.exp(L - L.max(axis=1, keepdims=True))
+    p /= p.sum(axis=1, keepdims=True)
+    for t in range(T):
+        ref = sum(p[t, e] * np_ffn(x[t], wg[e], wu[e], wd[e])[1] for e in range(E))
+        assert np.allclose(acc[t], ref, rtol=1e-11, atol=1e-12)
+        assert np.array_equal(f64(out[t]), np_round_bf16(acc[t]))
+
+
+def test_layer_with_shared_expert_dense_check():
+    rng = np.random.default_rng(11)
+    T, d, E, f, k = 6, 16, 4, 20, 2
+    x, wr, b, wg, wu, wd = _tiny_layer(rng, T, d, E, f, S=1)
+    out, acc = oracle.layer(x, wr, b, wg, wu, wd, k=k, S=1)
+    L = f64(x) @ f64(wr).T + b.astype(np.float64)
+    for t in range(T):
+        top = sorted(range(E), key=lambda e: (-L[t, e], e))[:k]
+        wk = np.exp(L[t, top] - L[t, top].max())
+        wk /= wk.sum()
+        ref = sum(wk[j] * np_ffn(x[t], wg[e], wu[e], wd[e])[1] for j, e in enumerate(top))
+        ref = ref + np_ffn(x[t], wg[E], wu[E], wd[E])[1]
+        assert np.allclose(acc[t], ref, rtol=1e-11, atol=1e-12)
+
+
+@pytest.mark.parametrize("k", [1, 2, 3])
+def test_layer_identical_experts_is_one_ffn(k):
+    rng = np.random.default_rng(20 + k)
+    T, d, E, f = 7, 24, 5, 16
+    x, wr, b, wg, wu, wd = _tiny_layer(rng, T, d, E, f, identical=True)
+    out, acc = oracle.layer(x, wr, b, wg, wu, wd, k=k)
+    for t in range(T):
+        _, y = np_ffn(x[t], wg[0], wu[0], wd[0])
+        assert np.allclose(acc[t], y, rtol=1e-12, atol=1e-13)
+
+
+def test_layer_token_subset_equals_full():
+    rng = np.random.default_rng(30)
+    T, d, E, f, k = 12, 16, 6, 8, 2
+    x, wr, b, wg, wu, wd = _tiny_layer(rng, T, d, E, f)
+    full, _ = oracle.layer(x, wr, b, wg, wu, wd, k=k)
+    sub = np.array([11, 0, 5], dtype=np.int32)
+    part, _ = oracle.layer(x, wr, b, wg, wu, wd, k=k, tokens=sub)
+    assert np.array_equal(part, full[sub])
+
+
+def test_token_out_slot_order_and_weights():
+    # token_out with explicit routing equals the weighted numpy sum
+    rng = np.random.default_rng(31)
+    d, f, E = 16, 12, 4
+    _, _, _, wg, wu, wd = _tiny_layer(rng, 1, d, E, f)
+    x = rand_bf16(rng, (d,))
+    idx = np.array([3, 1], dtype=np.int32)
+    w = np.array([0.7, 0.3])
+    out, acc = oracle.token_out(x, idx, w, wg, wu, wd, E=E, S=0)
+    ref = 0.7 * np_ffn(x, wg[3], wu[3], wd[3])[1] + 0.3 * np_ffn(x, wg[1], wu[1], wd[1])[1]
+    assert np.allclose(acc, ref, rtol=1e-12, atol=1e-13)
