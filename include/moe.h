@@ -1,0 +1,160 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) MoE-layer forward megakernel.
+ *
+ * The operation (what every call below computes) is the forward pass of one
+ * Mixture-of-Experts layer, as described in
+ *   Weave abstract (arXiv 2609.21483): routing, then dispatch of tokens to
+ *     experts, the expert computation, and the combine back to token order,
+ *     run as one persistent megakernel whose CTAs are split by a cost model
+ *     into data-movement and computation workers once routing is known;
+ *   xxqk.cn/news/665650 section 1 (router, top-k expert selection, the
+ *     expert matrix products, weighted merge of the expert outputs) and
+ *     section 2.1-2.3 (an in-kernel atomic task queue; per-task dependency
+ *     counters that release a task when they reach zero; no global barrier);
+ *   m.xxqk.cn/news/657744 section 2.1 (scheduling units: an expert's up
+ *     projection, then its down projection, large GEMMs split along K) and
+ *     section 5.1 (scheduling state lives in device memory passed to the
+ *     kernel, so the launch can be captured in a CUDA graph).
+ *
+ * Per token t (T tokens, model dim d, E routed experts, top-k, expert FFN
+ * dim f, S in {0,1} always-on shared experts):
+ *   L[t,e]  = sum_i x[t,i] * Wr[e,i] + b[e]                (fp32 accumulate)
+ *   p[t,:]  = softmax(L[t,:]) over all E experts
+ *   idx[t,:]= the k experts with the largest p (ties: lower expert index)
+ *   w[t,j]  = p[t,idx[t,j]] / sum_j' p[t,idx[t,j']]         (renormalised)
+ *   h       = bf16( silu(Wg[e] x_t) * (Wu[e] x_t) ),  silu(z) = z / (1 + e^-z)
+ *   y_e     = Wd[e] h
+ *   out[t]  = bf16( sum_j w[t,j] * y_{idx[t,j]}  +  y_shared )
+ * Tokens are permuted into per-expert rows in the canonical order: experts
+ * ascending, tokens ascending inside an expert.
+ *
+ * Conventions for every entry point:
+ *   - bf16 tensors are IEEE bfloat16, row-major, contiguous, 16-byte aligned
+ *     device pointers owned by the caller;
+ *       x        [T, d]         token activations
+ *       router_w [E, d]         router weight (nn.Linear layout)
+ *       w_gate   [E+S, f, d]    gate projections, shared expert stored last
+ *       w_up     [E+S, f, d]    up projections
+ *       w_down   [E+S, d, f]    down projections
+ *       out      [T, d]         overwritten (not accumulated)
+ *   - a stream argument is a cudaStream_t passed as void* (NULL = the legacy
+ *     default stream);
+ *   - every int-returning call returns MOE_OK (0) or one of MOE_E_*; the
+ *     message of the last failure on the calling thread is moe_last_error();
+ *   - a handle serves one stream at a time; calls on one handle are not
+ *     thread-safe.
+ * Limits: d % 64 == 0, f % 128 == 0, 1 <= k <= E <= 256, k <= 16, S <= 1,
+ * 0 <= T <= T_max given to moe_layer_reserve.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct moe_layer moe_layer_t;
+
+/* status codes */
+#define MOE_OK 0
+#define MOE_E_INVAL 1   /* bad argument, alignment, size, or T > T_max    */
+#define MOE_E_CUDA 2    /* a CUDA call or kernel launch failed             */
+#define MOE_E_TIMEOUT 3 /* a device-side wait ran out of its time budget   */
+#define MOE_E_DEVICE 4  /* the kernel found an inconsistent scheduler state */
+#define MOE_E_NOMEM 5   /* device or pinned host allocation failed         */
+#define MOE_E_STATE 6   /* call order: forward before reserve, etc.        */
+
+/* execution modes (option MOE_OPT_MODE) */
+#define MOE_MODE_PERSISTENT 0  /* one persistent megakernel, task queue      */
+#define MOE_MODE_MULTIKERNEL 1 /* ablation: one kernel per stage, no queue   */
+
+/* option keys for moe_layer_set_option */
+#define MOE_OPT_MODE 1         /* MOE_MODE_*                                   */
+#define MOE_OPT_TIMEOUT_NS 2   /* device wait budget in ns (default 2e9)      */
+#define MOE_OPT_MOVER_CTAS 3   /* >0: fixed number of mover CTAs; 0 = model   */
+#define MOE_OPT_GRID_CTAS 4    /* >0: persistent grid size; 0 = one per SM    */
+#define MOE_OPT_SPLIT_K 5      /* down-projection K splits (1,2,4; 0 = auto)  */
+#define MOE_OPT_TOKENS_PER_TILE 6 /* max tokens per GEMM tile (16..256, %16) */
+#define MOE_OPT_FAULT_DROP_TASK 7 /* test only: -1 off; else drop the dependency
+                                     notification of the n-th finished GEMM task,
+                                     which must end in MOE_E_TIMEOUT            */
+#define MOE_OPT_ROUTE_TOKENS 8 /* tokens per router tile (8..64; 0 = auto)    */
+
+/* statistics keys for moe_layer_get_stat (values of the last forward;
+ * moe_layer_status must have been called after it) */
+#define MOE_STAT_MOVER_CTAS 1  /* mover CTAs chosen by the cost model          */
+#define MOE_STAT_TASKS 2       /* tasks executed (all types)                   */
+#define MOE_STAT_GRID 3        /* CTAs launched for the persistent kernel      */
+#define MOE_STAT_GEMM_TASKS 4  /* expert GEMM tasks executed                   */
+#define MOE_STAT_MOVER_TASKS 5 /* gather + combine tasks executed              */
+#define MOE_STAT_STOLEN 6      /* tasks a CTA ran from the other role's queue  */
+
+/* Create a layer description.  Pure host call (no CUDA call, no allocation on
+ * the device).  Returns NULL on invalid dimensions (see moe_last_error). */
+moe_layer_t* moe_layer_create(int d, int f, int E, int k, int shared_experts);
+
+/* Allocate the device workspace for up to T_max tokens on the current device
+ * (routing arrays, permuted activations, expert intermediates, scheduler
+ * state) and cache the device properties.  The only allocating call besides
+ * moe_layer_forward_host's first use; call it before any stream capture.
+ * May be called again to grow or shrink. */
+int moe_layer_reserve(moe_layer_t* h, int T_max, void* stream);
+
+/* Set the per-expert router bias (fp32 [E] device pointer, added to the
+ * logits before softmax and top-k); NULL removes it.  The pointer is read at
+ * every forward and must stay valid. */
+int moe_layer_set_router_bias(moe_layer_t* h, const float* bias);
+
+/* One forward pass of the layer on T tokens (device pointers, see the layout
+ * above).  Asynchronous on `stream`; allocates nothing and never synchronises,
+ * so it can be captured in a CUDA graph.  Device-side failures (timeouts,
+ * inconsistent state) are reported by the next moe_layer_status. T == 0 is a
+ * no-op. */
+int moe_layer_forward(moe_layer_t* h, int T, const void* x, const void* router_w,
+                      const void* w_gate, const void* w_up, const void* w_down, void* out,
+                      void* stream);
+
+/* The same forward pass with x and out in host memory: copies x to the
+ * device, runs moe_layer_forward, copies out back and synchronises the
+ * stream.  Weights are device pointers as above.  Host buffers may be
+ * pageable or pinned; the first call allocates a device staging area for
+ * T_max tokens.  Returns the device status of the pass as well. */
+int moe_layer_forward_host(moe_layer_t* h, int T, const void* x_host, const void* router_w,
+                           const void* w_gate, const void* w_up, const void* w_down,
+                           void* out_host, void* stream);
+
+/* Copy the routing of the last forward into caller device buffers (any may be
+ * NULL): idx int32 [T,k], w fp32 [T,k] (renormalised weights, slot order),
+ * counts int32 [E], offsets int32 [E+1], perm int32 [T*k] (source token of
+ * each permuted row), pos int32 [T,k] (permuted row of each (token, slot)).
+ * Asynchronous on `stream`. */
+int moe_layer_get_routing(moe_layer_t* h, int32_t* idx, float* w, int32_t* counts,
+                          int32_t* offsets, int32_t* perm, int32_t* pos, void* stream);
+
+/* Synchronise `stream`, then return and clear the sticky device status of the
+ * last forward (MOE_OK, MOE_E_TIMEOUT or MOE_E_DEVICE), or MOE_E_CUDA when a
+ * CUDA error is pending. */
+int moe_layer_status(moe_layer_t* h, void* stream);
+
+/* Set an option (MOE_OPT_*).  Takes effect at the next forward. */
+int moe_layer_set_option(moe_layer_t* h, int key, long long value);
+
+/* Read a statistic (MOE_STAT_*) of the last forward whose status was read. */
+long long moe_layer_get_stat(moe_layer_t* h, int key);
+
+/* Bytes of device workspace moe_layer_reserve(T_max) allocates (host-only). */
+long long moe_layer_workspace_bytes(const moe_layer_t* h, int T_max);
+
+/* Free the workspace and the handle.  NULL is ignored. */
+void moe_layer_destroy(moe_layer_t* h);
+
+/* Message of the last failed call on this thread ("" if none). */
+const char* moe_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H_ */

@@ -1,0 +1,159 @@
+"""ctypes binding of include/moe.h: argument marshalling only.
+
+Each C entry point is exposed under its own name on ``lib`` (a ``ctypes.CDLL``
+with argument and return types set from the header).  ``MoELayer`` wraps a
+handle for callers holding torch tensors: it passes ``data_ptr()`` values and
+the current CUDA stream, and turns non-zero status codes into ``MoEError``.
+Every step of the layer runs in the library's kernels.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_build", "libmoe.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "moe.h")
+
+MOE_OK, MOE_E_INVAL, MOE_E_CUDA, MOE_E_TIMEOUT, MOE_E_DEVICE, MOE_E_NOMEM, MOE_E_STATE = range(7)
+MOE_MODE_PERSISTENT, MOE_MODE_MULTIKERNEL = 0, 1
+
+OPTIONS = {
+    "mode": 1, "timeout_ns": 2, "mover_ctas": 3, "grid_ctas": 4, "split_k": 5,
+    "tokens_per_tile": 6, "fault_drop_task": 7, "route_tokens": 8,
+}
+STATS = {"mover_ctas": 1, "tasks": 2, "grid": 3, "gemm_tasks": 4, "mover_tasks": 5, "stolen": 6}
+
+_vp, _i32, _i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong
+
+_SIGNATURES = {
+    "moe_layer_create": ([_i32, _i32, _i32, _i32, _i32], _vp),
+    "moe_layer_reserve": ([_vp, _i32, _vp], _i32),
+    "moe_layer_set_router_bias": ([_vp, _vp], _i32),
+    "moe_layer_forward": ([_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp], _i32),
+    "moe_layer_forward_host": ([_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp], _i32),
+    "moe_layer_get_routing": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp], _i32),
+    "moe_layer_status": ([_vp, _vp], _i32),
+    "moe_layer_set_option": ([_vp, _i32, _i64], _i32),
+    "moe_layer_get_stat": ([_vp, _i32], _i64),
+    "moe_layer_workspace_bytes": ([_vp, _i32], _i64),
+    "moe_layer_destroy": ([_vp], None),
+    "moe_last_error": ([], ctypes.c_char_p),
+}
+
+
+class MoEError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"moe error {code}: {msg}")
+        self.code = code
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libmoe.so (raises OSError if it was not built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise OSError(f"{path} is missing: build it with persistent_megakernel_sm_gb300.build")
+    dll = ctypes.CDLL(path)
+    for name, (args, res) in _SIGNATURES.items():
+        fn = getattr(dll, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = dll
+    return dll
+
+
+class _LazyLib:
+    def __getattr__(self, name):
+        return getattr(load_library(), name)
+
+
+lib = _LazyLib()
+
+
+def header_symbols(header: str = HEADER) -> list[str]:
+    """Names of the functions include/moe.h declares."""
+    text = open(header).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", text)))
+
+
+def _err(code: int):
+    if code != MOE_OK:
+        raise MoEError(code, (lib.moe_last_error() or b"").decode())
+
+
+def _stream_ptr(stream):
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(getattr(stream, "cuda_stream", stream))
+
+
+class MoELayer:
+    """One MoE layer handle (d, f, E, k, shared experts)."""
+
+    def __init__(self, d: int, f: int, E: int, k: int, shared_experts: int = 0):
+        h = lib.moe_layer_create(d, f, E, k, shared_experts)
+        if not h:
+            raise MoEError(MOE_E_INVAL, (lib.moe_last_error() or b"").decode())
+        self.h = ctypes.c_void_p(h)
+        self.d, self.f, self.E, self.k, self.S = d, f, E, k, shared_experts
+        self._bias = None
+
+    def reserve(self, T_max: int, stream=None):
+        _err(lib.moe_layer_reserve(self.h, T_max, _stream_ptr(stream)))
+
+    def set_router_bias(self, bias):
+        self._bias = bias  # keep the tensor alive while the library holds its pointer
+        _err(lib.moe_layer_set_router_bias(self.h, None if bias is None else bias.data_ptr()))
+
+    def set_option(self, key, value: int):
+        _err(lib.moe_layer_set_option(self.h, OPTIONS.get(key, key), int(value)))
+
+    def forward(self, x, router_w, w_gate, w_up, w_down, out, stream=None):
+        T = x.shape[0]
+        _err(lib.moe_layer_forward(self.h, T, x.data_ptr(), router_w.data_ptr(),
+                                   w_gate.data_ptr(), w_up.data_ptr(), w_down.data_ptr(),
+                                   out.data_ptr(), _stream_ptr(stream)))
+        return out
+
+    def forward_host(self, T, x_host_ptr, router_w, w_gate, w_up, w_down, out_host_ptr,
+                     stream=None):
+        _err(lib.moe_layer_forward_host(self.h, T, x_host_ptr, router_w.data_ptr(),
+                                        w_gate.data_ptr(), w_up.data_ptr(), w_down.data_ptr(),
+                                        out_host_ptr, _stream_ptr(stream)))
+
+    def status(self, stream=None) -> int:
+        return lib.moe_layer_status(self.h, _stream_ptr(stream))
+
+    def check(self, stream=None):
+        _err(self.status(stream))
+
+    def get_routing(self, idx=None, w=None, counts=None, offsets=None, perm=None, pos=None,
+                    stream=None):
+        ptr = (lambda t: None if t is None else t.data_ptr())
+        _err(lib.moe_layer_get_routing(self.h, ptr(idx), ptr(w), ptr(counts), ptr(offsets),
+                                       ptr(perm), ptr(pos), _stream_ptr(stream)))
+
+    def stat(self, key) -> int:
+        return lib.moe_layer_get_stat(self.h, STATS.get(key, key))
+
+    def workspace_bytes(self, T_max: int) -> int:
+        return lib.moe_layer_workspace_bytes(self.h, T_max)
+
+    def close(self):
+        if self.h:
+            lib.moe_layer_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

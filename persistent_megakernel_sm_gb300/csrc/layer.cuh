@@ -1,0 +1,134 @@
+// Launch parameters, workspace layout and task encoding of the MoE-layer
+// forward megakernel.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+constexpr int kThreads = 256;       // 8 warps per CTA
+constexpr int kBM = 128;            // MMA M: weight rows per accumulator
+constexpr int kBK = 64;             // K elements per pipeline stage (128 B rows)
+constexpr int kABoxBytes = kBM * kBK * 2;   // 16 KB weight box
+constexpr int kBBoxRows = 32;       // token rows per activation box
+constexpr int kBBoxBytes = kBBoxRows * kBK * 2;  // 4 KB
+constexpr int kGatherRows = 32;     // permuted rows per gather task
+constexpr int kMaxE = 256;
+constexpr int kMaxK = 16;
+constexpr int kTmemCols = 512;
+constexpr int kAcc1Col = 256;       // second accumulator's first TMEM column
+
+// task types (bits 28-31 of a task id)
+enum TaskType : int {
+  kTaskRoute = 1,    // router tile: logits, softmax, top-k, per-tile counts
+  kTaskGather = 2,   // mover: copy token rows of x into permuted rows of Xp
+  kTaskGateUp = 3,   // GEMM: H = bf16(silu(Xp Wg^T) * (Xp Wu^T)), one f tile
+  kTaskDown = 4,     // GEMM: Y = H Wd^T, two d tiles, one K split
+  kTaskCombine = 5,  // mover: out = bf16(sum_j w_j Y[pos] + Y_shared)
+};
+
+__host__ __device__ constexpr int task_id(int type, int payload) { return (type << 28) | payload; }
+__host__ __device__ constexpr int task_type(int id) { return (id >> 28) & 0xF; }
+__host__ __device__ constexpr int task_payload(int id) { return id & 0x0FFFFFFF; }
+
+// One GEMM row group: up to bn_max permuted rows of one expert (or, for the
+// shared expert, up to bn_max consecutive tokens).
+struct Group {
+  int e;         // expert index (E for the shared expert)
+  int row0;      // first row in H / Y
+  int nrows;     // rows in this group
+  int src_row0;  // first row of the B operand source (Xp for routed, x for shared)
+};
+
+// Scheduler state.  Zeroed before every launch.
+struct Sched {
+  int status;
+  int route_done;
+  int plan_done;
+  int n_movers;
+  int mover_head;
+  int mover_tail;       // dynamic pushes (slots after the router tiles)
+  int mover_total_dyn;
+  int gemm_head;
+  int gemm_tail;        // dynamic pushes (slots after the static shared-expert tasks)
+  int gemm_total_dyn;
+  int n_groups;         // shared + routed groups
+  int tasks_done;
+  int stat_gemm;
+  int stat_mover;
+  int stat_stolen;
+  int fault_seen;
+  int err_info;
+  int pad[15];
+};
+
+struct Params {
+  // problem
+  int T, d, f, E, k, S;
+  // tiling
+  int bn_max;        // max tokens per GEMM tile (multiple of 16, <= 256)
+  int stages;        // pipeline stages
+  int stage_bytes;   // 2 * kABoxBytes + ceil(bn_max / 32) * kBBoxBytes
+  int n_ftiles;      // f / 128
+  int n_dtiles;      // ceil(d / 256): each down task covers 256 d rows
+  int ks;            // split of the down projection's K (= f)
+  int kb_down;       // k blocks (of 64) per down split
+  int rt;            // tokens per router tile
+  int n_route;       // router tiles
+  int ct;            // tokens per combine tile
+  int n_comb;        // combine tiles
+  int n_shared_groups;
+  int n_static_gemm; // shared-expert gate/up tasks, ready at launch
+  int y_f32;         // Y holds fp32 partial sums [ks][rows][d]; else bf16 [rows][d]
+  int rows_y;        // rows of one Y partial (T*k + T*S)
+  int max_groups;    // capacity of the group arrays
+  int mover_cap, gemm_cap;  // ring capacities
+  int fault_drop;    // -1, or the index of the GEMM completion to drop
+  int mover_override;
+  unsigned long long timeout_ns;
+  // cost model constants
+  float beta_move;   // bytes/s one mover CTA sustains
+  float phi_gemm;    // FLOP/s one GEMM CTA sustains
+  float hbm_bw;      // bytes/s of the whole device
+  // inputs and output
+  const __nv_bfloat16* x;
+  const __nv_bfloat16* wr;
+  const float* bias;
+  __nv_bfloat16* out;
+  // routing workspace
+  int* idx;          // [T, k]
+  float* wgt;        // [T, k]
+  int* rank;         // [T, k] rank of (t, j) among the tile's tokens of its expert
+  int* tile_cnt;     // [n_route, E] per-tile counts, then exclusive prefix over tiles
+  int* counts;       // [E]
+  int* offsets;      // [E + 1]
+  int* perm;         // [T * k]
+  int* pos;          // [T, k]
+  // activations
+  __nv_bfloat16* Xp; // [T * k, d]
+  __nv_bfloat16* H;  // [T * k + T * S, f]
+  void* Y;           // bf16 [rows_y, d] or fp32 [ks, rows_y, d]
+  // scheduler
+  Group* groups;     // [max_groups]
+  int* gather_done;  // [max_groups]
+  int* gu_done;      // [max_groups]
+  int* comb_done;    // [n_comb]
+  int* ring_mover;   // [mover_cap]
+  int* ring_gemm;    // [gemm_cap]
+  Sched* sched;
+};
+
+struct Maps {
+  CUtensorMap wg;  // [(E+S) f, d], box 64 x 128
+  CUtensorMap wu;  // [(E+S) f, d], box 64 x 128
+  CUtensorMap wd;  // [(E+S) d, f], box 64 x 128
+  CUtensorMap xp;  // [T k, d],      box 64 x 32
+  CUtensorMap x;   // [T, d],        box 64 x 32
+  CUtensorMap h;   // [T k + T S, f], box 64 x 32
+};
+
+}  // namespace moe

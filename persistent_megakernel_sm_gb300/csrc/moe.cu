@@ -1,0 +1,759 @@
+// MoE-layer forward for GB300 (sm_103a): the persistent megakernel, the
+// one-kernel-per-stage ablation, and the C ABI declared in include/moe.h.
+//
+// Persistent mode (Weave abstract, arXiv 2609.21483; xxqk.cn/news/665650
+// sections 2.1-2.3; m.xxqk.cn/news/657744 sections 2.2-2.3): one CTA per SM
+// stays resident and loops { claim a task; run it; publish its writes; bump
+// the dependency counters it feeds; push the tasks that reached zero } until
+// both task queues are drained.  Termination is by task count, never by
+// seeing an empty queue (m.xxqk.cn/news/657744 section 3.3 describes the
+// early-exit race the other rule invites).  Router tiles and shared-expert
+// tiles are ready at launch; the CTA that finishes the last router tile runs
+// the plan (scan, permutation, row groups, cost model) and pushes the gathers.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "layer.cuh"
+#include "tasks.cuh"
+
+namespace moe {
+
+__device__ __forceinline__ char* align1024(char* p) {
+  return reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// CTA set-up shared by every kernel: barriers, TMEM, per-thread state.
+__device__ __forceinline__ void cta_setup(const Params& p, const Maps& maps, char*& smem,
+                                          Ctrl*& c, CtaState& st, bool with_tmem) {
+  extern __shared__ __align__(1024) char smem_raw[];
+  smem = align1024(smem_raw);
+  c = reinterpret_cast<Ctrl*>(smem + (size_t)p.stages * p.stage_bytes);
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&c->full_bar[s], 1);
+      mbar_init(&c->empty_bar[s], 1);
+    }
+    mbar_init(&c->acc_bar, 1);
+    fence_mbar_init();
+    c->deadline = globaltimer() + p.timeout_ns;
+  }
+  if (with_tmem && warp == 1) {
+    tmem_alloc(&c->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 32 * 2) {
+    prefetch_tmap(&maps.wg);
+    prefetch_tmap(&maps.wu);
+    prefetch_tmap(&maps.wd);
+    prefetch_tmap(&maps.xp);
+    prefetch_tmap(&maps.x);
+    prefetch_tmap(&maps.h);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  st.pipe_it = 0;
+  st.gemm_count = 0;
+  st.deadline = c->deadline;
+  st.role_mover = 0;
+}
+
+__device__ __forceinline__ void cta_teardown(Ctrl* c, bool with_tmem) {
+  tc_fence_before();
+  __syncthreads();
+  if (with_tmem && (threadIdx.x >> 5) == 1) {
+    tc_fence_after();
+    tmem_dealloc(c->tmem_base, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ persistent megakernel
+
+__global__ void __launch_bounds__(kThreads, 1)
+    moe_persistent_kernel(const __grid_constant__ Params p, const __grid_constant__ Maps maps) {
+  char* smem;
+  Ctrl* c;
+  CtaState st;
+  cta_setup(p, maps, smem, c, st, true);
+  int executed = 0, gemm_tasks = 0, mover_tasks = 0;
+  while (true) {
+    if (threadIdx.x == 0) c->task = claim_next(p, st);
+    __syncthreads();
+    const int task = c->task;
+    if (task < 0) break;
+    ++executed;
+    const int type = task_type(task), pl = task_payload(task);
+    if (type == kTaskRoute) {
+      route_task(p, pl, smem, c);
+      release_writes();
+      if (threadIdx.x == 0) {
+        const int old = atom_add_acq_rel(&p.sched->route_done, 1);
+        c->flag = (old + 1 == p.n_route);
+      }
+      __syncthreads();
+      if (c->flag) {
+        fence_acq_rel_gpu();
+        plan_task(p, c, true);
+      }
+    } else if (type == kTaskGather) {
+      ++mover_tasks;
+      const int g = pl >> 3, ch = pl & 7;
+      gather_task(p, g, ch, c);
+      notify_gather_done(p, g);
+    } else if (type == kTaskGateUp) {
+      ++gemm_tasks;
+      const int g = pl / p.n_ftiles, ft = pl - g * p.n_ftiles;
+      gateup_task(p, maps, g, ft, smem, c, st);
+      notify_gateup_done(p, g);
+    } else if (type == kTaskDown) {
+      ++gemm_tasks;
+      const int n_down = p.n_dtiles * p.ks;
+      const int g = pl / n_down, r = pl - g * n_down;
+      const int dt = r / p.ks, ks = r - dt * p.ks;
+      down_task(p, maps, g, dt, ks, smem, c, st);
+      notify_down_done(p, g, c);
+    } else if (type == kTaskCombine) {
+      ++mover_tasks;
+      combine_task(p, pl, c);
+      __syncthreads();
+    } else {
+      if (threadIdx.x == 0) set_status(p, MOE_E_DEVICE, 6);
+      break;
+    }
+  }
+  if (threadIdx.x == 0) {
+    atomicAdd(&p.sched->tasks_done, executed);
+    atomicAdd(&p.sched->stat_gemm, gemm_tasks);
+    atomicAdd(&p.sched->stat_mover, mover_tasks);
+  }
+  cta_teardown(c, true);
+}
+
+// ------------------------------------------------------------------ ablation: one kernel per stage
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_route(const __grid_constant__ Params p, const __grid_constant__ Maps maps) {
+  char* smem;
+  Ctrl* c;
+  CtaState st;
+  cta_setup(p, maps, smem, c, st, false);
+  route_task(p, blockIdx.x, smem, c);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_plan(const __grid_constant__ Params p, const __grid_constant__ Maps maps) {
+  char* smem;
+  Ctrl* c;
+  CtaState st;
+  cta_setup(p, maps, smem, c, st, false);
+  plan_task(p, c, false);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_gather(const __grid_constant__ Params p, const __grid_constant__ Maps maps) {
+  const int g = p.n_shared_groups + (int)(blockIdx.x >> 3), ch = blockIdx.x & 7;
+  if (g >= p.sched->n_groups) return;
+  const Group G = load_group(p, g);
+  if (ch * kGatherRows >= G.nrows) return;
+  char* smem;
+  Ctrl* c;
+  CtaState st;
+  cta_setup(p, maps, smem, c, st, false);
+  gather_task(p, g, ch, c);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_gateup(const __grid_constant__ Params p, const __grid_constant__ Maps maps) {
+  const int g = blockIdx.x / p.n_ftiles, ft = blockIdx.x - g * p.n_ftiles;
+  if (g >= p.sched->n_groups) return;
+  char* smem;
+  Ctrl* c;
+  CtaState st;
+  cta_setup(p, maps, smem, c, st, true);
+  gateup_task(p, maps, g, ft, smem, c, st);
+  cta_teardown(c, true);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_down(const __grid_constant__ Params p, const __grid_constant__ Maps maps) {
+  const int n_down = p.n_dtiles * p.ks;
+  const int g = blockIdx.x / n_down, r = blockIdx.x - g * n_down;
+  if (g >= p.sched->n_groups) return;
+  char* smem;
+  Ctrl* c;
+  CtaState st;
+  cta_setup(p, maps, smem, c, st, true);
+  down_task(p, maps, g, r / p.ks, r % p.ks, smem, c, st);
+  cta_teardown(c, true);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_combine(const __grid_constant__ Params p, const __grid_constant__ Maps maps) {
+  char* smem;
+  Ctrl* c;
+  CtaState st;
+  cta_setup(p, maps, smem, c, st, false);
+  combine_task(p, blockIdx.x, c);
+}
+
+}  // namespace moe
+
+// ====================================================================== host side
+
+using namespace moe;
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const std::string& msg) {
+  g_err = msg;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  g_err = std::string(what) + ": " + cudaGetErrorString(e);
+  return MOE_E_CUDA;
+}
+
+#define CK(call)                                   \
+  do {                                             \
+    cudaError_t e_ = (call);                       \
+    if (e_ != cudaSuccess) return cuda_fail(e_, #call); \
+  } while (0)
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor [rows, cols] (row-major), box 64 columns x box_rows rows,
+// 128-byte swizzle, out-of-range elements read as zero.
+bool encode_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int cdiv(long long a, long long b) { return (int)((a + b - 1) / b); }
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+constexpr int kSmemBudget = 227 * 1024;
+constexpr int kRtMin = 8;
+
+// Sizes that bound the workspace for T_max tokens.
+struct Bounds {
+  int T;
+  int n_route;      // router tiles at the smallest tile
+  int max_groups;   // shared + routed groups at the smallest token tile (32)
+  int n_comb;       // combine tiles at one token per tile
+  int mover_cap, gemm_cap;
+  size_t y_elems;   // elements of Y storage (fp32 words or 2x bf16)
+};
+
+}  // namespace
+
+struct moe_layer {
+  int d, f, E, k, S;
+  int T_max = 0;
+  int device = -1;
+  int num_sms = 0;
+  // options
+  int mode = MOE_MODE_PERSISTENT;
+  unsigned long long timeout_ns = 2000000000ull;
+  int mover_override = 0;
+  int grid_override = 0;
+  int split_k = 0;
+  int bn_opt = 0;
+  int fault_drop = -1;
+  int rt_opt = 0;
+  const float* bias = nullptr;
+  // workspace
+  char* ws = nullptr;
+  size_t ws_bytes = 0;
+  Bounds B{};
+  // offsets into ws
+  size_t o_idx, o_wgt, o_rank, o_tile, o_counts, o_offsets, o_perm, o_pos, o_xp, o_h, o_y,
+      o_groups, o_zero, o_gd, o_gu, o_cd, o_sched, o_zero_end, o_ring, o_ring_m, o_ring_g,
+      o_ring_end;
+  // host staging for moe_layer_forward_host
+  void* x_dev_stage = nullptr;
+  void* out_dev_stage = nullptr;
+  // last forward
+  Sched last{};
+  bool last_valid = false;
+  int last_grid = 0;
+  int last_T = 0;
+};
+
+namespace {
+
+Bounds make_bounds(const moe_layer* h, int T) {
+  Bounds b{};
+  b.T = T;
+  const long long Tk = (long long)T * h->k;
+  b.n_route = std::max(1, cdiv(T, kRtMin));
+  const int shared_groups = h->S ? cdiv(T, 32) : 0;
+  b.max_groups = shared_groups + cdiv(Tk, 32) + std::min<long long>(h->E, Tk) + 1;
+  b.n_comb = std::max(T, 1);
+  b.mover_cap = cdiv(Tk, 32) + b.max_groups + b.n_comb + 16;
+  const int n_ft = h->f / 128, n_dt = cdiv(h->d, 256);
+  b.gemm_cap = b.max_groups * (n_ft + n_dt * 4) + 16;
+  const long long rows = Tk + (long long)T * h->S;
+  // fp32 partials for up to 4 K splits when small, else bf16 (half a word each)
+  const long long small = rows * h->d * 4;
+  b.y_elems = (size_t)(small <= (1ll << 27) ? small : (rows * h->d + 1) / 2);
+  return b;
+}
+
+void layout(moe_layer* h, const Bounds& b) {
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    size_t r = o;
+    o = align_up(o + bytes, 256);
+    return r;
+  };
+  const size_t Tk = (size_t)b.T * h->k;
+  const size_t rows = Tk + (size_t)b.T * h->S;
+  h->o_idx = take(Tk * 4);
+  h->o_wgt = take(Tk * 4);
+  h->o_rank = take(Tk * 4);
+  h->o_tile = take((size_t)b.n_route * h->E * 4);
+  h->o_counts = take(h->E * 4);
+  h->o_offsets = take((h->E + 1) * 4);
+  h->o_perm = take(Tk * 4);
+  h->o_pos = take(Tk * 4);
+  h->o_xp = take((Tk + 64) * h->d * 2);
+  h->o_h = take((rows + 64) * h->f * 2);
+  h->o_y = take(b.y_elems * 4 + 4096);
+  h->o_groups = take((size_t)b.max_groups * sizeof(Group));
+  h->o_zero = o;
+  h->o_sched = take(sizeof(Sched));
+  h->o_gd = take((size_t)b.max_groups * 4);
+  h->o_gu = take((size_t)b.max_groups * 4);
+  h->o_cd = take((size_t)b.n_comb * 4);
+  h->o_zero_end = o;
+  h->o_ring = o;
+  h->o_ring_m = take((size_t)b.mover_cap * 4);
+  h->o_ring_g = take((size_t)b.gemm_cap * 4);
+  h->o_ring_end = o;
+  h->ws_bytes = o;
+}
+
+// Tiling of one forward pass.
+struct Tiling {
+  int bn, stages, stage_bytes, smem, ks, rt, ct, y_f32;
+};
+
+int choose_tiling(const moe_layer* h, int T, Tiling* t) {
+  const long long Tk = (long long)T * h->k;
+  int bn = h->bn_opt;
+  if (bn <= 0) {
+    const long long avg = Tk / h->E;
+    long long want = std::max<long long>(32, 2 * avg);
+    want = std::min<long long>(want, std::max(T, 1));
+    bn = (int)std::min<long long>(256, ((want + 31) / 32) * 32);
+  }
+  bn = std::max(32, std::min(256, ((bn + 31) / 32) * 32));
+  t->bn = bn;
+  t->stage_bytes = 2 * kABoxBytes + cdiv(bn, kBBoxRows) * kBBoxBytes;
+  const int ctrl = (int)align_up(sizeof(Ctrl), 1024);
+  t->stages = std::min(8, (kSmemBudget - 1024 - ctrl) / t->stage_bytes);
+  if (t->stages < 2) return fail(MOE_E_INVAL, "tile too large for shared memory");
+  t->smem = 1024 + t->stages * t->stage_bytes + ctrl;
+  // down-projection K split: fp32 partials when the batch is small
+  const int kblocks = h->f / kBK;
+  const long long rows = Tk + (long long)T * h->S;
+  int ks = h->split_k;
+  if (ks <= 0) ks = (Tk <= 2048) ? 4 : 1;
+  while (ks > 1 && (kblocks % ks != 0 || (size_t)rows * h->d * ks > h->B.y_elems)) ks >>= 1;
+  if (ks < 1) ks = 1;
+  t->ks = ks;
+  t->y_f32 = ks > 1 ? 1 : ((size_t)rows * h->d <= h->B.y_elems ? 1 : 0);
+  // router tile: ~one tile per SM, 8..64 tokens (logits must fit the stages)
+  int rt = h->rt_opt;
+  if (rt <= 0) rt = ((cdiv(T, std::max(h->num_sms, 1)) + 7) / 8) * 8;
+  rt = std::max(kRtMin, std::min(64, rt));
+  while (rt > kRtMin && (size_t)rt * (h->E + h->k) * 4 > (size_t)t->stages * t->stage_bytes) rt -= 8;
+  t->rt = rt;
+  // combine tile: ~one per SM, (k+S) rows per token, <= 256 (token, slot) pairs
+  int ct = cdiv(T, std::max(h->num_sms, 1));
+  ct = std::max(1, std::min(ct, kThreads / h->k));
+  t->ct = ct;
+  return MOE_OK;
+}
+
+int set_error_from_sched(const Sched& s) {
+  if (s.status == MOE_E_TIMEOUT) {
+    g_err = "device wait timed out (site " + std::to_string(s.err_info) + ")";
+    return MOE_E_TIMEOUT;
+  }
+  if (s.status != 0) {
+    g_err = "device scheduler inconsistency (site " + std::to_string(s.err_info) + ")";
+    return MOE_E_DEVICE;
+  }
+  return MOE_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_last_error(void) { return g_err.c_str(); }
+
+moe_layer_t* moe_layer_create(int d, int f, int E, int k, int shared_experts) {
+  if (d <= 0 || d % 128 != 0) {
+    g_err = "d must be a positive multiple of 128";
+    return nullptr;
+  }
+  if (f <= 0 || f % 128 != 0) {
+    g_err = "f must be a positive multiple of 128";
+    return nullptr;
+  }
+  if (E < 1 || E > kMaxE || k < 1 || k > E || k > kMaxK) {
+    g_err = "need 1 <= k <= E <= 256 and k <= 16";
+    return nullptr;
+  }
+  if (shared_experts < 0 || shared_experts > 1) {
+    g_err = "shared_experts must be 0 or 1";
+    return nullptr;
+  }
+  moe_layer_t* h = new (std::nothrow) moe_layer();
+  if (!h) {
+    g_err = "out of host memory";
+    return nullptr;
+  }
+  h->d = d;
+  h->f = f;
+  h->E = E;
+  h->k = k;
+  h->S = shared_experts;
+  g_err.clear();
+  return h;
+}
+
+long long moe_layer_workspace_bytes(const moe_layer_t* h, int T_max) {
+  if (!h || T_max < 0) return -1;
+  moe_layer tmp = *h;
+  tmp.ws = nullptr;
+  Bounds b = make_bounds(&tmp, std::max(T_max, 1));
+  layout(&tmp, b);
+  return (long long)tmp.ws_bytes;
+}
+
+int moe_layer_reserve(moe_layer_t* h, int T_max, void* stream) {
+  if (!h) return fail(MOE_E_INVAL, "null handle");
+  if (T_max < 1 || (long long)T_max * h->k >= (1ll << 26)) return fail(MOE_E_INVAL, "T_max out of range");
+  CK(cudaGetDevice(&h->device));
+  CK(cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device));
+  int cc_major = 0, cc_minor = 0;
+  CK(cudaDeviceGetAttribute(&cc_major, cudaDevAttrComputeCapabilityMajor, h->device));
+  CK(cudaDeviceGetAttribute(&cc_minor, cudaDevAttrComputeCapabilityMinor, h->device));
+  if (cc_major != 10 || cc_minor != 3)
+    return fail(MOE_E_INVAL, "this library is built for sm_103a (GB300) only");
+  if (!encode_fn()) return fail(MOE_E_CUDA, "cuTensorMapEncodeTiled is not available");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (h->ws) {
+    CK(cudaStreamSynchronize(s));
+    CK(cudaFree(h->ws));
+    h->ws = nullptr;
+  }
+  Bounds b = make_bounds(h, T_max);
+  layout(h, b);
+  h->B = b;
+  if (cudaMalloc(&h->ws, h->ws_bytes) != cudaSuccess) {
+    h->ws = nullptr;
+    cudaGetLastError();
+    return fail(MOE_E_NOMEM, "workspace allocation failed");
+  }
+  CK(cudaMemsetAsync(h->ws, 0, h->ws_bytes, s));
+  if (h->x_dev_stage) {
+    cudaFree(h->x_dev_stage);
+    cudaFree(h->out_dev_stage);
+    h->x_dev_stage = h->out_dev_stage = nullptr;
+  }
+  h->T_max = T_max;
+  const int kernels_smem = kSmemBudget;
+  CK(cudaFuncSetAttribute(moe_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                          kernels_smem));
+  CK(cudaFuncSetAttribute(k_route, cudaFuncAttributeMaxDynamicSharedMemorySize, kernels_smem));
+  CK(cudaFuncSetAttribute(k_plan, cudaFuncAttributeMaxDynamicSharedMemorySize, kernels_smem));
+  CK(cudaFuncSetAttribute(k_gather, cudaFuncAttributeMaxDynamicSharedMemorySize, kernels_smem));
+  CK(cudaFuncSetAttribute(k_gateup, cudaFuncAttributeMaxDynamicSharedMemorySize, kernels_smem));
+  CK(cudaFuncSetAttribute(k_down, cudaFuncAttributeMaxDynamicSharedMemorySize, kernels_smem));
+  CK(cudaFuncSetAttribute(k_combine, cudaFuncAttributeMaxDynamicSharedMemorySize, kernels_smem));
+  g_err.clear();
+  return MOE_OK;
+}
+
+int moe_layer_set_router_bias(moe_layer_t* h, const float* bias) {
+  if (!h) return fail(MOE_E_INVAL, "null handle");
+  if (bias && !aligned16(bias)) return fail(MOE_E_INVAL, "bias must be 16-byte aligned");
+  h->bias = bias;
+  return MOE_OK;
+}
+
+int moe_layer_set_option(moe_layer_t* h, int key, long long v) {
+  if (!h) return fail(MOE_E_INVAL, "null handle");
+  switch (key) {
+    case MOE_OPT_MODE:
+      if (v != MOE_MODE_PERSISTENT && v != MOE_MODE_MULTIKERNEL) return fail(MOE_E_INVAL, "bad mode");
+      h->mode = (int)v;
+      break;
+    case MOE_OPT_TIMEOUT_NS:
+      if (v < 1000) return fail(MOE_E_INVAL, "timeout below 1 us");
+      h->timeout_ns = (unsigned long long)v;
+      break;
+    case MOE_OPT_MOVER_CTAS:
+      if (v < 0) return fail(MOE_E_INVAL, "negative mover count");
+      h->mover_override = (int)v;
+      break;
+    case MOE_OPT_GRID_CTAS:
+      if (v < 0 || v > 4096) return fail(MOE_E_INVAL, "grid out of range");
+      h->grid_override = (int)v;
+      break;
+    case MOE_OPT_SPLIT_K:
+      if (v != 0 && v != 1 && v != 2 && v != 4) return fail(MOE_E_INVAL, "split_k must be 0,1,2,4");
+      h->split_k = (int)v;
+      break;
+    case MOE_OPT_TOKENS_PER_TILE:
+      if (v != 0 && (v < 16 || v > 256 || v % 16)) return fail(MOE_E_INVAL, "tokens per tile must be 16..256, multiple of 16");
+      h->bn_opt = (int)v;
+      break;
+    case MOE_OPT_FAULT_DROP_TASK:
+      h->fault_drop = v < 0 ? -1 : (int)v;
+      break;
+    case MOE_OPT_ROUTE_TOKENS:
+      if (v != 0 && (v < 8 || v > 64 || v % 8)) return fail(MOE_E_INVAL, "router tile must be 8..64, multiple of 8");
+      h->rt_opt = (int)v;
+      break;
+    default:
+      return fail(MOE_E_INVAL, "unknown option");
+  }
+  return MOE_OK;
+}
+
+int moe_layer_forward(moe_layer_t* h, int T, const void* x, const void* router_w,
+                      const void* w_gate, const void* w_up, const void* w_down, void* out,
+                      void* stream) {
+  if (!h) return fail(MOE_E_INVAL, "null handle");
+  if (!h->ws) return fail(MOE_E_STATE, "moe_layer_reserve was not called");
+  if (T < 0 || T > h->T_max) return fail(MOE_E_INVAL, "T out of range (0..T_max)");
+  if (T == 0) return MOE_OK;
+  if (!x || !router_w || !w_gate || !w_up || !w_down || !out)
+    return fail(MOE_E_INVAL, "null tensor pointer");
+  if (!aligned16(x) || !aligned16(router_w) || !aligned16(w_gate) || !aligned16(w_up) ||
+      !aligned16(w_down) || !aligned16(out))
+    return fail(MOE_E_INVAL, "tensors must be 16-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Tiling tl;
+  int rc = choose_tiling(h, T, &tl);
+  if (rc) return rc;
+
+  Params p;
+  memset(&p, 0, sizeof(p));
+  p.T = T;
+  p.d = h->d;
+  p.f = h->f;
+  p.E = h->E;
+  p.k = h->k;
+  p.S = h->S;
+  p.bn_max = tl.bn;
+  p.stages = tl.stages;
+  p.stage_bytes = tl.stage_bytes;
+  p.n_ftiles = h->f / kBM;
+  p.n_dtiles = cdiv(h->d, 2 * kBM);
+  p.ks = tl.ks;
+  p.kb_down = (h->f / kBK) / tl.ks;
+  p.rt = tl.rt;
+  p.n_route = cdiv(T, tl.rt);
+  p.ct = tl.ct;
+  p.n_comb = cdiv(T, tl.ct);
+  p.n_shared_groups = h->S ? cdiv(T, tl.bn) : 0;
+  p.n_static_gemm = p.n_shared_groups * p.n_ftiles;
+  p.y_f32 = tl.y_f32;
+  p.rows_y = T * h->k + T * h->S;
+  const long long Tk = (long long)T * h->k;
+  p.max_groups = p.n_shared_groups + cdiv(Tk, tl.bn) + (int)std::min<long long>(h->E, Tk);
+  if (p.max_groups > h->B.max_groups) return fail(MOE_E_INVAL, "group capacity exceeded");
+  p.mover_cap = h->B.mover_cap;
+  p.gemm_cap = h->B.gemm_cap;
+  p.fault_drop = h->fault_drop;
+  p.mover_override = h->mover_override;
+  p.timeout_ns = h->timeout_ns;
+  p.beta_move = 40e9f;
+  p.phi_gemm = 1925e12f / 152.f;
+  p.hbm_bw = 6.79e12f;
+  p.x = static_cast<const __nv_bfloat16*>(x);
+  p.wr = static_cast<const __nv_bfloat16*>(router_w);
+  p.bias = h->bias;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  char* w = h->ws;
+  p.idx = reinterpret_cast<int*>(w + h->o_idx);
+  p.wgt = reinterpret_cast<float*>(w + h->o_wgt);
+  p.rank = reinterpret_cast<int*>(w + h->o_rank);
+  p.tile_cnt = reinterpret_cast<int*>(w + h->o_tile);
+  p.counts = reinterpret_cast<int*>(w + h->o_counts);
+  p.offsets = reinterpret_cast<int*>(w + h->o_offsets);
+  p.perm = reinterpret_cast<int*>(w + h->o_perm);
+  p.pos = reinterpret_cast<int*>(w + h->o_pos);
+  p.Xp = reinterpret_cast<__nv_bfloat16*>(w + h->o_xp);
+  p.H = reinterpret_cast<__nv_bfloat16*>(w + h->o_h);
+  p.Y = w + h->o_y;
+  p.groups = reinterpret_cast<Group*>(w + h->o_groups);
+  p.gather_done = reinterpret_cast<int*>(w + h->o_gd);
+  p.gu_done = reinterpret_cast<int*>(w + h->o_gu);
+  p.comb_done = reinterpret_cast<int*>(w + h->o_cd);
+  p.ring_mover = reinterpret_cast<int*>(w + h->o_ring_m);
+  p.ring_gemm = reinterpret_cast<int*>(w + h->o_ring_g);
+  p.sched = reinterpret_cast<Sched*>(w + h->o_sched);
+
+  Maps m;
+  const int nt = h->E + h->S;
+  bool ok = encode_2d(&m.wg, w_gate, (uint64_t)nt * h->f, h->d, kBM) &&
+            encode_2d(&m.wu, w_up, (uint64_t)nt * h->f, h->d, kBM) &&
+            encode_2d(&m.wd, w_down, (uint64_t)nt * h->d, h->f, kBM) &&
+            encode_2d(&m.xp, p.Xp, (uint64_t)Tk, h->d, kBBoxRows) &&
+            encode_2d(&m.x, x, (uint64_t)T, h->d, kBBoxRows) &&
+            encode_2d(&m.h, p.H, (uint64_t)p.rows_y, h->f, kBBoxRows);
+  if (!ok) return fail(MOE_E_INVAL, "tensor map encoding failed");
+
+  CK(cudaMemsetAsync(w + h->o_zero, 0, h->o_zero_end - h->o_zero, s));
+  CK(cudaMemsetAsync(w + h->o_ring, 0xFF, h->o_ring_end - h->o_ring, s));
+  if (h->mode == MOE_MODE_PERSISTENT) {
+    int grid = h->grid_override > 0 ? h->grid_override : h->num_sms;
+    h->last_grid = grid;
+    moe_persistent_kernel<<<grid, kThreads, tl.smem, s>>>(p, m);
+    CK(cudaGetLastError());
+  } else {
+    h->last_grid = 0;
+    k_route<<<p.n_route, kThreads, tl.smem, s>>>(p, m);
+    CK(cudaGetLastError());
+    k_plan<<<1, kThreads, tl.smem, s>>>(p, m);
+    CK(cudaGetLastError());
+    const int routed_max = p.max_groups - p.n_shared_groups;
+    k_gather<<<routed_max * 8, kThreads, tl.smem, s>>>(p, m);
+    CK(cudaGetLastError());
+    k_gateup<<<p.max_groups * p.n_ftiles, kThreads, tl.smem, s>>>(p, m);
+    CK(cudaGetLastError());
+    k_down<<<p.max_groups * p.n_dtiles * p.ks, kThreads, tl.smem, s>>>(p, m);
+    CK(cudaGetLastError());
+    k_combine<<<p.n_comb, kThreads, tl.smem, s>>>(p, m);
+    CK(cudaGetLastError());
+  }
+  h->last_valid = false;
+  h->last_T = T;
+  return MOE_OK;
+}
+
+int moe_layer_forward_host(moe_layer_t* h, int T, const void* x_host, const void* router_w,
+                           const void* w_gate, const void* w_up, const void* w_down,
+                           void* out_host, void* stream) {
+  if (!h) return fail(MOE_E_INVAL, "null handle");
+  if (!h->ws) return fail(MOE_E_STATE, "moe_layer_reserve was not called");
+  if (T < 0 || T > h->T_max) return fail(MOE_E_INVAL, "T out of range (0..T_max)");
+  if (T == 0) return MOE_OK;
+  if (!x_host || !out_host) return fail(MOE_E_INVAL, "null host pointer");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t bytes = (size_t)h->T_max * h->d * 2;
+  if (!h->x_dev_stage) {
+    if (cudaMalloc(&h->x_dev_stage, bytes) != cudaSuccess ||
+        cudaMalloc(&h->out_dev_stage, bytes) != cudaSuccess) {
+      cudaGetLastError();
+      return fail(MOE_E_NOMEM, "staging allocation failed");
+    }
+  }
+  const size_t n = (size_t)T * h->d * 2;
+  CK(cudaMemcpyAsync(h->x_dev_stage, x_host, n, cudaMemcpyHostToDevice, s));
+  int rc = moe_layer_forward(h, T, h->x_dev_stage, router_w, w_gate, w_up, w_down,
+                             h->out_dev_stage, stream);
+  if (rc) return rc;
+  CK(cudaMemcpyAsync(out_host, h->out_dev_stage, n, cudaMemcpyDeviceToHost, s));
+  return moe_layer_status(h, stream);
+}
+
+int moe_layer_get_routing(moe_layer_t* h, int32_t* idx, float* w, int32_t* counts,
+                          int32_t* offsets, int32_t* perm, int32_t* pos, void* stream) {
+  if (!h || !h->ws) return fail(MOE_E_STATE, "no workspace");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // sizes of the last forward are not kept on the host; copy T_max-sized
+  // regions would overrun small caller buffers, so the caller passes buffers
+  // sized for the T of the last forward and we copy exactly that much.
+  const int T = h->last_T;
+  const size_t Tk = (size_t)T * h->k;
+  char* ws = h->ws;
+  if (idx) CK(cudaMemcpyAsync(idx, ws + h->o_idx, Tk * 4, cudaMemcpyDeviceToDevice, s));
+  if (w) CK(cudaMemcpyAsync(w, ws + h->o_wgt, Tk * 4, cudaMemcpyDeviceToDevice, s));
+  if (counts) CK(cudaMemcpyAsync(counts, ws + h->o_counts, h->E * 4, cudaMemcpyDeviceToDevice, s));
+  if (offsets)
+    CK(cudaMemcpyAsync(offsets, ws + h->o_offsets, (h->E + 1) * 4, cudaMemcpyDeviceToDevice, s));
+  if (perm) CK(cudaMemcpyAsync(perm, ws + h->o_perm, Tk * 4, cudaMemcpyDeviceToDevice, s));
+  if (pos) CK(cudaMemcpyAsync(pos, ws + h->o_pos, Tk * 4, cudaMemcpyDeviceToDevice, s));
+  return MOE_OK;
+}
+
+int moe_layer_status(moe_layer_t* h, void* stream) {
+  if (!h) return fail(MOE_E_INVAL, "null handle");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  if (!h->ws) return MOE_OK;
+  CK(cudaMemcpy(&h->last, h->ws + h->o_sched, sizeof(Sched), cudaMemcpyDeviceToHost));
+  h->last_valid = true;
+  const int rc = set_error_from_sched(h->last);
+  if (rc) {
+    int zero = 0;
+    CK(cudaMemcpy(h->ws + h->o_sched, &zero, sizeof(int), cudaMemcpyHostToDevice));
+  }
+  return rc;
+}
+
+long long moe_layer_get_stat(moe_layer_t* h, int key) {
+  if (!h || !h->last_valid) return -1;
+  switch (key) {
+    case MOE_STAT_MOVER_CTAS: return h->last.n_movers;
+    case MOE_STAT_TASKS: return h->last.tasks_done;
+    case MOE_STAT_GRID: return h->last_grid;
+    case MOE_STAT_GEMM_TASKS: return h->last.stat_gemm;
+    case MOE_STAT_MOVER_TASKS: return h->last.stat_mover;
+    case MOE_STAT_STOLEN: return h->last.stat_stolen;
+    default: return -1;
+  }
+}
+
+void moe_layer_destroy(moe_layer_t* h) {
+  if (!h) return;
+  if (h->ws) cudaFree(h->ws);
+  if (h->x_dev_stage) cudaFree(h->x_dev_stage);
+  if (h->out_dev_stage) cudaFree(h->out_dev_stage);
+  delete h;
+}
+
+}  // extern "C"

@@ -1,0 +1,69 @@
+"""The C-ABI library loads, exports every symbol include/moe.h declares, and
+its host-only calls (create, options, workspace sizing) behave; no GPU."""
+import ctypes
+
+import pytest
+
+import persistent_megakernel_sm_gb300 as pkg
+from persistent_megakernel_sm_gb300 import build as cuda_build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    cuda_build.build()
+    return pkg.load_library()
+
+
+def test_header_declares_the_boundary():
+    names = pkg.header_symbols()
+    for must in ("moe_layer_create", "moe_layer_reserve", "moe_layer_forward",
+                 "moe_layer_destroy", "moe_layer_status", "moe_last_error"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in pkg.header_symbols():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+@pytest.mark.parametrize("args,ok", [
+    ((4096, 14336, 8, 2, 0), True),
+    ((7168, 2048, 256, 8, 1), True),
+    ((100, 512, 8, 2, 0), False),     # d not a multiple of 128
+    ((256, 200, 8, 2, 0), False),     # f not a multiple of 128
+    ((256, 512, 8, 9, 0), False),     # k > E
+    ((256, 512, 300, 2, 0), False),   # E > 256
+    ((256, 512, 64, 17, 0), False),   # k > 16
+    ((256, 512, 8, 2, 2), False),     # two shared experts
+])
+def test_create_validates(lib, args, ok):
+    h = lib.moe_layer_create(*args)
+    if ok:
+        assert h
+        lib.moe_layer_destroy(h)
+    else:
+        assert not h
+        assert lib.moe_last_error()
+
+
+def test_options_and_workspace_without_device(lib):
+    h = lib.moe_layer_create(4096, 14336, 8, 2, 0)
+    try:
+        assert lib.moe_layer_set_option(h, pkg.OPTIONS["mode"], 1) == 0
+        assert lib.moe_layer_set_option(h, pkg.OPTIONS["mode"], 7) == pkg.MOE_E_INVAL
+        assert lib.moe_layer_set_option(h, pkg.OPTIONS["split_k"], 3) == pkg.MOE_E_INVAL
+        assert lib.moe_layer_set_option(h, pkg.OPTIONS["tokens_per_tile"], 48) == 0
+        assert lib.moe_layer_set_option(h, pkg.OPTIONS["tokens_per_tile"], 50) == pkg.MOE_E_INVAL
+        assert lib.moe_layer_set_option(h, 999, 1) == pkg.MOE_E_INVAL
+        # forward before reserve is a state error, not a crash
+        rc = lib.moe_layer_forward(h, 1, 16, 16, 16, 16, 16, 16, None)
+        assert rc == pkg.MOE_E_STATE
+        small = lib.moe_layer_workspace_bytes(h, 256)
+        big = lib.moe_layer_workspace_bytes(h, 4096)
+        # the permuted activations alone are T*k*d*2 bytes
+        assert small >= 256 * 2 * 4096 * 2 and big > small
+        assert lib.moe_layer_get_stat(h, pkg.STATS["tasks"]) == -1
+    finally:
+        lib.moe_layer_destroy(h)
+    lib.moe_layer_destroy(None)

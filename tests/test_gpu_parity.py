@@ -1,0 +1,93 @@
+"""CUDA path against the CPU oracle on small layers that span several tiles,
+ragged tails and the layer's degenerate cases, through the C ABI."""
+import numpy as np
+import pytest
+
+import _harness as hz
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+# (T, d, E, k, f, S, bias std)
+CASES = {
+    "tiny": (64, 256, 8, 2, 512, 0, 0.0),
+    "ragged_bias": (37, 256, 8, 2, 512, 0, 0.5),
+    "one_token": (1, 256, 4, 1, 256, 0, 0.0),
+    "shared_partial_dtile": (100, 384, 16, 4, 384, 1, 0.3),
+    "k_equals_E": (48, 256, 6, 6, 256, 0, 0.0),
+    "multi_mtile_skew": (300, 256, 4, 2, 256, 0, 2.0),
+    "wide_E": (96, 256, 64, 8, 256, 0, 1.0),
+    "top16": (40, 128, 32, 16, 128, 1, 0.0),
+}
+
+
+def _full_check(w, inp, mode="persistent", **opts):
+    dev = hz.upload(inp)
+    layer = hz.make_layer(w, mode=0 if mode == "persistent" else 1, **opts)
+    got, routing = hz.run_layer(layer, w, dev)
+    hz.check_routing(w, inp, routing)
+    ref, _ = oracle.layer(inp["x"], inp["router_w"], inp["bias"], inp["w_gate"], inp["w_up"],
+                          inp["w_down"], k=w.k, S=w.S)
+    hz.check_out(got, ref)
+    layer.close()
+    return got
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_small_layer_parity(name):
+    T, d, E, k, f, S, b = CASES[name]
+    w, inp = hz.custom_case(T, d, E, k, f, S, b)
+    _full_check(w, inp)
+
+
+@pytest.mark.parametrize("name", ["tiny", "shared_partial_dtile", "multi_mtile_skew"])
+def test_multikernel_ablation_bit_identical(name):
+    T, d, E, k, f, S, b = CASES[name]
+    w, inp = hz.custom_case(T, d, E, k, f, S, b)
+    a = _full_check(w, inp, "persistent")
+    m = _full_check(w, inp, "multikernel")
+    assert np.array_equal(a, m), "ablation and megakernel outputs differ"
+
+
+@pytest.mark.parametrize("split_k", [1, 2, 4])
+@pytest.mark.parametrize("tokens_per_tile", [32, 64, 256])
+def test_tiling_options_same_result(split_k, tokens_per_tile):
+    w, inp = hz.custom_case(200, 256, 8, 2, 512, 0, 0.4)
+    _full_check(w, inp, split_k=split_k, tokens_per_tile=tokens_per_tile)
+
+
+def test_all_tokens_one_expert():
+    w, inp = hz.custom_case(130, 256, 8, 1, 256, 0, 0.0)
+    inp["bias"] = np.array([12.0] + [0.0] * 7, dtype=np.float32)
+    _full_check(w, inp)
+
+
+def test_identical_experts_give_one_ffn():
+    w, inp = hz.custom_case(50, 256, 8, 2, 256, 0, 0.0, identical_experts=True)
+    got = _full_check(w, inp)
+    for t in (0, 17, 49):
+        _, y = oracle.expert_ffn(inp["x"][t], inp["w_gate"][0], inp["w_up"][0], inp["w_down"][0])
+        hz.check_out(got[t], oracle.f64_to_bf16(y), "identical experts")
+
+
+def test_grid_and_mover_overrides():
+    w, inp = hz.custom_case(160, 256, 16, 4, 256, 1, 0.5)
+    _full_check(w, inp, grid_ctas=7, mover_ctas=3)
+    _full_check(w, inp, grid_ctas=1)
+
+
+def test_smaller_T_than_reserved_and_repeat():
+    import torch
+    w, inp = hz.custom_case(120, 256, 8, 2, 256, 0, 0.3)
+    dev = hz.upload(inp)
+    layer = hz.make_layer(w, T_max=512)
+    ref, _ = oracle.layer(inp["x"], inp["router_w"], inp["bias"], inp["w_gate"], inp["w_up"],
+                          inp["w_down"], k=w.k)
+    for T in (120, 57, 120):
+        got, routing = hz.run_layer(layer, w, dev, T=T)
+        hz.check_out(got, ref[:T])
+    # T = 0 is a no-op
+    out = torch.zeros((1, w.d), dtype=torch.bfloat16, device="cuda")
+    layer.forward(dev["x"][:0], dev["router_w"], dev["w_gate"], dev["w_up"], dev["w_down"], out)
+    layer.check()
+    layer.close()
