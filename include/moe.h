@@ -43,7 +43,7 @@
  *     message of the last failure on the calling thread is moe_last_error();
  *   - a handle serves one stream at a time; calls on one handle are not
  *     thread-safe.
- * Limits: d % 64 == 0, f % 128 == 0, 1 <= k <= E <= 256, k <= 16, S <= 1,
+ * Limits: d % 128 == 0, f % 128 == 0, 1 <= k <= E <= 256, k <= 16, S <= 1,
  * 0 <= T <= T_max given to moe_layer_reserve.
  */
 #ifndef MOE_H_
@@ -80,7 +80,11 @@ typedef struct moe_layer moe_layer_t;
 #define MOE_OPT_FAULT_DROP_TASK 7 /* test only: -1 off; else drop the dependency
                                      notification of the n-th finished GEMM task,
                                      which must end in MOE_E_TIMEOUT            */
-#define MOE_OPT_ROUTE_TOKENS 8 /* tokens per router tile (8..64; 0 = auto)    */
+#define MOE_OPT_ROUTE_TOKENS 8 /* tokens per router tile: 0 or 128 (the MMA M) */
+#define MOE_OPT_CLAIM_AHEAD 9  /* claim the next task while running one when at
+                                  least this many tasks wait; -1 auto, 0 off  */
+#define MOE_OPT_TRACE 10       /* >0: record up to this many task records per
+                                  forward (allocates; see moe_layer_get_trace) */
 
 /* statistics keys for moe_layer_get_stat (values of the last forward;
  * moe_layer_status must have been called after it) */
@@ -90,6 +94,8 @@ typedef struct moe_layer moe_layer_t;
 #define MOE_STAT_GEMM_TASKS 4  /* expert GEMM tasks executed                   */
 #define MOE_STAT_MOVER_TASKS 5 /* gather + combine tasks executed              */
 #define MOE_STAT_STOLEN 6      /* tasks a CTA ran from the other role's queue  */
+#define MOE_STAT_AHEAD 7       /* tasks claimed ahead while another one ran    */
+#define MOE_STAT_TRACE_RECORDS 8 /* task records the last forward produced     */
 
 /* Create a layer description.  Pure host call (no CUDA call, no allocation on
  * the device).  Returns NULL on invalid dimensions (see moe_last_error). */
@@ -143,6 +149,15 @@ int moe_layer_set_option(moe_layer_t* h, int key, long long value);
 
 /* Read a statistic (MOE_STAT_*) of the last forward whose status was read. */
 long long moe_layer_get_stat(moe_layer_t* h, int key);
+
+/* Copy the task trace of the last forward (option MOE_OPT_TRACE) into a host
+ * buffer of `cap` records; synchronises `stream`.  Each record is four
+ * uint64: (CTA index << 32) | task id, then three %globaltimer readings in ns:
+ * when the CTA began claiming the task, when it began running it, and when
+ * it had published its results.  Task id bits 28-31 hold the type (1 router
+ * tile, 2 gather, 3 gate/up GEMM, 4 down GEMM, 5 combine).  Returns the
+ * number of records copied, or -1 on error. */
+int moe_layer_get_trace(moe_layer_t* h, uint64_t* records, int cap, void* stream);
 
 /* Bytes of device workspace moe_layer_reserve(T_max) allocates (host-only). */
 long long moe_layer_workspace_bytes(const moe_layer_t* h, int T_max);

@@ -21,9 +21,12 @@ MOE_MODE_PERSISTENT, MOE_MODE_MULTIKERNEL = 0, 1
 
 OPTIONS = {
     "mode": 1, "timeout_ns": 2, "mover_ctas": 3, "grid_ctas": 4, "split_k": 5,
-    "tokens_per_tile": 6, "fault_drop_task": 7, "route_tokens": 8,
+    "tokens_per_tile": 6, "fault_drop_task": 7, "route_tokens": 8, "claim_ahead": 9,
+    "trace": 10,
 }
-STATS = {"mover_ctas": 1, "tasks": 2, "grid": 3, "gemm_tasks": 4, "mover_tasks": 5, "stolen": 6}
+STATS = {"mover_ctas": 1, "tasks": 2, "grid": 3, "gemm_tasks": 4, "mover_tasks": 5, "stolen": 6,
+         "ahead": 7, "trace_records": 8}
+TASK_TYPES = {1: "route", 2: "gather", 3: "gateup", 4: "down", 5: "combine"}
 
 _vp, _i32, _i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong
 
@@ -38,6 +41,7 @@ _SIGNATURES = {
     "moe_layer_set_option": ([_vp, _i32, _i64], _i32),
     "moe_layer_get_stat": ([_vp, _i32], _i64),
     "moe_layer_workspace_bytes": ([_vp, _i32], _i64),
+    "moe_layer_get_trace": ([_vp, _vp, _i32, _vp], _i32),
     "moe_layer_destroy": ([_vp], None),
     "moe_last_error": ([], ctypes.c_char_p),
 }
@@ -143,6 +147,20 @@ class MoELayer:
 
     def stat(self, key) -> int:
         return lib.moe_layer_get_stat(self.h, STATS.get(key, key))
+
+    def trace(self, cap: int = 1 << 16, stream=None):
+        """Task records of the last forward as a numpy array of dicts-of-arrays:
+        cta, task id, type, t_claim, t_start, t_end (ns, %globaltimer)."""
+        import numpy as np
+        buf = np.zeros((cap, 4), dtype=np.uint64)
+        n = lib.moe_layer_get_trace(self.h, buf.ctypes.data, cap, _stream_ptr(stream))
+        if n < 0:
+            raise MoEError(MOE_E_CUDA, (lib.moe_last_error() or b"").decode())
+        buf = buf[:n]
+        task = (buf[:, 0] & 0xffffffff).astype(np.int64)
+        return {"cta": (buf[:, 0] >> 32).astype(np.int64), "task": task,
+                "type": task >> 28, "t_claim": buf[:, 1].astype(np.int64),
+                "t_start": buf[:, 2].astype(np.int64), "t_end": buf[:, 3].astype(np.int64)}
 
     def workspace_bytes(self, T_max: int) -> int:
         return lib.moe_layer_workspace_bytes(self.h, T_max)

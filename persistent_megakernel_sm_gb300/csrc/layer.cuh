@@ -17,6 +17,7 @@ constexpr int kABoxBytes = kBM * kBK * 2;   // 16 KB weight box
 constexpr int kBBoxRows = 32;       // token rows per activation box
 constexpr int kBBoxBytes = kBBoxRows * kBK * 2;  // 4 KB
 constexpr int kGatherRows = 32;     // permuted rows per gather task
+constexpr int kRouteTokens = 128;   // tokens per router tile (the MMA M)
 constexpr int kMaxE = 256;
 constexpr int kMaxK = 16;
 constexpr int kTmemCols = 512;
@@ -36,25 +37,32 @@ __host__ __device__ constexpr int task_type(int id) { return (id >> 28) & 0xF; }
 __host__ __device__ constexpr int task_payload(int id) { return id & 0x0FFFFFFF; }
 
 // One GEMM row group: up to bn_max permuted rows of one expert (or, for the
-// shared expert, up to bn_max consecutive tokens).
+// shared expert, up to bn_max consecutive tokens).  An expert with more rows
+// has several sibling groups [sib0, sib0 + nsib); its gate/up and down tasks
+// are released together and interleaved, so the siblings read each weight
+// tile at nearly the same time and the second read is served by L2.
 struct Group {
   int e;         // expert index (E for the shared expert)
   int row0;      // first row in H / Y
   int nrows;     // rows in this group
   int src_row0;  // first row of the B operand source (Xp for routed, x for shared)
+  int sib0;      // first sibling group of the same expert
+  int nsib;      // sibling groups of the expert
+  int gchunks;   // gather tasks of all siblings
+  int pad;
 };
 
 // Scheduler state.  Zeroed before every launch.
+// A queue word packs the queue's head (claims, low 32 bits) and tail
+// (dynamic pushes, high 32 bits) so one load sees both and one CAS claims.
 struct Sched {
+  unsigned long long mover_q;
+  unsigned long long gemm_q;
   int status;
   int route_done;
   int plan_done;
   int n_movers;
-  int mover_head;
-  int mover_tail;       // dynamic pushes (slots after the router tiles)
   int mover_total_dyn;
-  int gemm_head;
-  int gemm_tail;        // dynamic pushes (slots after the static shared-expert tasks)
   int gemm_total_dyn;
   int n_groups;         // shared + routed groups
   int tasks_done;
@@ -63,7 +71,10 @@ struct Sched {
   int stat_stolen;
   int fault_seen;
   int err_info;
-  int pad[15];
+  int trace_n;
+  int stat_ahead;
+  int n_gather;         // gather tasks pushed by the plan (mover slots after the router tiles)
+  int pad[12];
 };
 
 struct Params {
@@ -77,7 +88,7 @@ struct Params {
   int n_dtiles;      // ceil(d / 256): each down task covers 256 d rows
   int ks;            // split of the down projection's K (= f)
   int kb_down;       // k blocks (of 64) per down split
-  int rt;            // tokens per router tile
+  int rt;            // tokens per router tile (kRouteTokens)
   int n_route;       // router tiles
   int ct;            // tokens per combine tile
   int n_comb;        // combine tiles
@@ -89,6 +100,8 @@ struct Params {
   int mover_cap, gemm_cap;  // ring capacities
   int fault_drop;    // -1, or the index of the GEMM completion to drop
   int mover_override;
+  int ahead_depth;   // claim the next task early when this many wait (0 = never)
+  int fa_depth;      // claims are fetch-and-adds when this many tasks wait
   unsigned long long timeout_ns;
   // cost model constants
   float beta_move;   // bytes/s one mover CTA sustains
@@ -117,9 +130,11 @@ struct Params {
   int* gather_done;  // [max_groups]
   int* gu_done;      // [max_groups]
   int* comb_done;    // [n_comb]
-  int* ring_mover;   // [mover_cap]
-  int* ring_gemm;    // [gemm_cap]
+  int* ring_mover;   // [mover_cap] task id + 1, 0 = not yet pushed
+  int* ring_gemm;    // [gemm_cap]  task id + 1, 0 = not yet pushed
   Sched* sched;
+  unsigned long long* trace;  // [trace_cap][4] task trace records (or null)
+  int trace_cap;
 };
 
 struct Maps {
@@ -129,6 +144,8 @@ struct Maps {
   CUtensorMap xp;  // [T k, d],      box 64 x 32
   CUtensorMap x;   // [T, d],        box 64 x 32
   CUtensorMap h;   // [T k + T S, f], box 64 x 32
+  CUtensorMap xr;  // [T, d],        box 64 x 128 (router A operand)
+  CUtensorMap wr;  // [E, d],        box 64 x 32  (router B operand)
 };
 
 }  // namespace moe

@@ -15,6 +15,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdio>
+#include <cstddef>
 #include <cstring>
 #include <string>
 
@@ -40,6 +41,9 @@ __device__ __forceinline__ void cta_setup(const Params& p, const Maps& maps, cha
       mbar_init(&c->empty_bar[s], 1);
     }
     mbar_init(&c->acc_bar, 1);
+    mbar_init(&c->gbar, 1);
+    mbar_init(&c->cbar[0], 1);
+    mbar_init(&c->cbar[1], 1);
     fence_mbar_init();
     c->deadline = globaltimer() + p.timeout_ns;
   }
@@ -54,6 +58,8 @@ __device__ __forceinline__ void cta_setup(const Params& p, const Maps& maps, cha
     prefetch_tmap(&maps.xp);
     prefetch_tmap(&maps.x);
     prefetch_tmap(&maps.h);
+    prefetch_tmap(&maps.xr);
+    prefetch_tmap(&maps.wr);
   }
   tc_fence_before();
   __syncthreads();
@@ -62,6 +68,8 @@ __device__ __forceinline__ void cta_setup(const Params& p, const Maps& maps, cha
   st.gemm_count = 0;
   st.deadline = c->deadline;
   st.role_mover = 0;
+  st.gather_phase = 0;
+  st.comb_phase = 0;
 }
 
 __device__ __forceinline__ void cta_teardown(Ctrl* c, bool with_tmem) {
@@ -81,16 +89,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   Ctrl* c;
   CtaState st;
   cta_setup(p, maps, smem, c, st, true);
-  int executed = 0, gemm_tasks = 0, mover_tasks = 0;
+  int executed = 0, gemm_tasks = 0, mover_tasks = 0, ahead = 0;
+  if (threadIdx.x == 0) c->next_task = -1;
   while (true) {
-    if (threadIdx.x == 0) c->task = claim_next(p, st);
+    if (threadIdx.x == 0) {
+      c->t_claim = globaltimer();
+      const int held = c->next_task;
+      c->next_task = -1;
+      c->task = held >= 0 ? held : claim_next(p, st);
+      c->t_start = globaltimer();
+    }
     __syncthreads();
     const int task = c->task;
     if (task < 0) break;
     ++executed;
+    // claim ahead: an otherwise idle lane takes the next task now, so the
+    // claim's round trips overlap this task; only when the queue is deep, so
+    // that holding a task cannot starve another CTA near the end
+    if (threadIdx.x == 64 && p.ahead_depth > 0) {
+      const int r = claim_once(p, st, p.ahead_depth);
+      if (r >= 0) {
+        c->next_task = r;
+        ++ahead;
+      }
+    }
     const int type = task_type(task), pl = task_payload(task);
     if (type == kTaskRoute) {
-      route_task(p, pl, smem, c);
+      route_task(p, maps, pl, smem, c, st);
       release_writes();
       if (threadIdx.x == 0) {
         const int old = atom_add_acq_rel(&p.sched->route_done, 1);
@@ -99,12 +124,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncthreads();
       if (c->flag) {
         fence_acq_rel_gpu();
-        plan_task(p, c, true);
+        plan_task(p, smem, c, true);
       }
     } else if (type == kTaskGather) {
       ++mover_tasks;
       const int g = pl >> 3, ch = pl & 7;
-      gather_task(p, g, ch, c);
+      gather_task(p, g, ch, smem, c, st);
       notify_gather_done(p, g);
     } else if (type == kTaskGateUp) {
       ++gemm_tasks;
@@ -120,11 +145,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       notify_down_done(p, g, c);
     } else if (type == kTaskCombine) {
       ++mover_tasks;
-      combine_task(p, pl, c);
+      combine_task(p, pl, smem, c, st);
       __syncthreads();
     } else {
       if (threadIdx.x == 0) set_status(p, MOE_E_DEVICE, 6);
       break;
+    }
+    if (threadIdx.x == 0 && p.trace) {
+      const int i = atomicAdd(&p.sched->trace_n, 1);
+      if (i < p.trace_cap) {
+        unsigned long long* r = p.trace + (size_t)i * 4;
+        r[0] = ((unsigned long long)blockIdx.x << 32) | (unsigned)task;
+        r[1] = c->t_claim;
+        r[2] = c->t_start;
+        r[3] = globaltimer();
+      }
     }
   }
   if (threadIdx.x == 0) {
@@ -132,6 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     atomicAdd(&p.sched->stat_gemm, gemm_tasks);
     atomicAdd(&p.sched->stat_mover, mover_tasks);
   }
+  if (threadIdx.x == 64) atomicAdd(&p.sched->stat_ahead, ahead);
   cta_teardown(c, true);
 }
 
@@ -142,8 +178,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   char* smem;
   Ctrl* c;
   CtaState st;
-  cta_setup(p, maps, smem, c, st, false);
-  route_task(p, blockIdx.x, smem, c);
+  cta_setup(p, maps, smem, c, st, true);
+  route_task(p, maps, blockIdx.x, smem, c, st);
+  cta_teardown(c, true);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -152,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   Ctrl* c;
   CtaState st;
   cta_setup(p, maps, smem, c, st, false);
-  plan_task(p, c, false);
+  plan_task(p, smem, c, false);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -165,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   Ctrl* c;
   CtaState st;
   cta_setup(p, maps, smem, c, st, false);
-  gather_task(p, g, ch, c);
+  gather_task(p, g, ch, smem, c, st);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -199,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   Ctrl* c;
   CtaState st;
   cta_setup(p, maps, smem, c, st, false);
-  combine_task(p, blockIdx.x, c);
+  combine_task(p, blockIdx.x, smem, c, st);
 }
 
 }  // namespace moe
@@ -264,7 +301,6 @@ int cdiv(long long a, long long b) { return (int)((a + b - 1) / b); }
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 constexpr int kSmemBudget = 227 * 1024;
-constexpr int kRtMin = 8;
 
 // Sizes that bound the workspace for T_max tokens.
 struct Bounds {
@@ -292,6 +328,9 @@ struct moe_layer {
   int bn_opt = 0;
   int fault_drop = -1;
   int rt_opt = 0;
+  int ahead_opt = -1;
+  int trace_cap = 0;
+  unsigned long long* trace = nullptr;
   const float* bias = nullptr;
   // workspace
   char* ws = nullptr;
@@ -317,7 +356,7 @@ Bounds make_bounds(const moe_layer* h, int T) {
   Bounds b{};
   b.T = T;
   const long long Tk = (long long)T * h->k;
-  b.n_route = std::max(1, cdiv(T, kRtMin));
+  b.n_route = std::max(1, cdiv(T, kRouteTokens));
   const int shared_groups = h->S ? cdiv(T, 32) : 0;
   b.max_groups = shared_groups + cdiv(Tk, 32) + std::min<long long>(h->E, Tk) + 1;
   b.n_comb = std::max(T, 1);
@@ -382,6 +421,8 @@ int choose_tiling(const moe_layer* h, int T, Tiling* t) {
   bn = std::max(32, std::min(256, ((bn + 31) / 32) * 32));
   t->bn = bn;
   t->stage_bytes = 2 * kABoxBytes + cdiv(bn, kBBoxRows) * kBBoxBytes;
+  // the router's tile keeps x (16 KB) then Wr (E rows) in one stage
+  t->stage_bytes = std::max(t->stage_bytes, kABoxBytes + cdiv(h->E, kBBoxRows) * kBBoxBytes);
   const int ctrl = (int)align_up(sizeof(Ctrl), 1024);
   t->stages = std::min(8, (kSmemBudget - 1024 - ctrl) / t->stage_bytes);
   if (t->stages < 2) return fail(MOE_E_INVAL, "tile too large for shared memory");
@@ -395,12 +436,7 @@ int choose_tiling(const moe_layer* h, int T, Tiling* t) {
   if (ks < 1) ks = 1;
   t->ks = ks;
   t->y_f32 = ks > 1 ? 1 : ((size_t)rows * h->d <= h->B.y_elems ? 1 : 0);
-  // router tile: ~one tile per SM, 8..64 tokens (logits must fit the stages)
-  int rt = h->rt_opt;
-  if (rt <= 0) rt = ((cdiv(T, std::max(h->num_sms, 1)) + 7) / 8) * 8;
-  rt = std::max(kRtMin, std::min(64, rt));
-  while (rt > kRtMin && (size_t)rt * (h->E + h->k) * 4 > (size_t)t->stages * t->stage_bytes) rt -= 8;
-  t->rt = rt;
+  t->rt = kRouteTokens;
   // combine tile: ~one per SM, (k+S) rows per token, <= 256 (token, slot) pairs
   int ct = cdiv(T, std::max(h->num_sms, 1));
   ct = std::max(1, std::min(ct, kThreads / h->k));
@@ -550,8 +586,30 @@ int moe_layer_set_option(moe_layer_t* h, int key, long long v) {
     case MOE_OPT_FAULT_DROP_TASK:
       h->fault_drop = v < 0 ? -1 : (int)v;
       break;
+    case MOE_OPT_CLAIM_AHEAD:
+      if (v < -1) return fail(MOE_E_INVAL, "claim-ahead depth must be -1, 0 or positive");
+      h->ahead_opt = (int)v;
+      break;
+    case MOE_OPT_TRACE: {
+      if (v < 0 || v > (1 << 24)) return fail(MOE_E_INVAL, "trace capacity out of range");
+      if (h->trace) {
+        cudaDeviceSynchronize();
+        cudaFree(h->trace);
+        h->trace = nullptr;
+      }
+      h->trace_cap = 0;
+      if (v > 0) {
+        if (cudaMalloc(&h->trace, (size_t)v * 32) != cudaSuccess) {
+          cudaGetLastError();
+          h->trace = nullptr;
+          return fail(MOE_E_NOMEM, "trace allocation failed");
+        }
+        h->trace_cap = (int)v;
+      }
+      break;
+    }
     case MOE_OPT_ROUTE_TOKENS:
-      if (v != 0 && (v < 8 || v > 64 || v % 8)) return fail(MOE_E_INVAL, "router tile must be 8..64, multiple of 8");
+      if (v != 0 && v != kRouteTokens) return fail(MOE_E_INVAL, "router tiles are 128 tokens");
       h->rt_opt = (int)v;
       break;
     default:
@@ -607,6 +665,8 @@ int moe_layer_forward(moe_layer_t* h, int T, const void* x, const void* router_w
   p.gemm_cap = h->B.gemm_cap;
   p.fault_drop = h->fault_drop;
   p.mover_override = h->mover_override;
+  p.trace = h->trace;
+  p.trace_cap = h->trace_cap;
   p.timeout_ns = h->timeout_ns;
   p.beta_move = 40e9f;
   p.phi_gemm = 1925e12f / 152.f;
@@ -642,14 +702,19 @@ int moe_layer_forward(moe_layer_t* h, int T, const void* x, const void* router_w
             encode_2d(&m.wd, w_down, (uint64_t)nt * h->d, h->f, kBM) &&
             encode_2d(&m.xp, p.Xp, (uint64_t)Tk, h->d, kBBoxRows) &&
             encode_2d(&m.x, x, (uint64_t)T, h->d, kBBoxRows) &&
-            encode_2d(&m.h, p.H, (uint64_t)p.rows_y, h->f, kBBoxRows);
+            encode_2d(&m.h, p.H, (uint64_t)p.rows_y, h->f, kBBoxRows) &&
+            encode_2d(&m.xr, x, (uint64_t)T, h->d, kRouteTokens) &&
+            encode_2d(&m.wr, router_w, (uint64_t)h->E, h->d, kBBoxRows);
   if (!ok) return fail(MOE_E_INVAL, "tensor map encoding failed");
 
-  CK(cudaMemsetAsync(w + h->o_zero, 0, h->o_zero_end - h->o_zero, s));
-  CK(cudaMemsetAsync(w + h->o_ring, 0xFF, h->o_ring_end - h->o_ring, s));
+  // scheduler counters and task rings are contiguous: one memset resets them
+  CK(cudaMemsetAsync(w + h->o_zero, 0, h->o_ring_end - h->o_zero, s));
   if (h->mode == MOE_MODE_PERSISTENT) {
     int grid = h->grid_override > 0 ? h->grid_override : h->num_sms;
     h->last_grid = grid;
+    p.ahead_depth = h->ahead_opt < 0 ? 2 * grid : h->ahead_opt;
+    // fetch-and-add claims when more tasks wait than there are claimers
+    p.fa_depth = (p.ahead_depth > 0 ? 2 : 1) * grid + 8;
     moe_persistent_kernel<<<grid, kThreads, tl.smem, s>>>(p, m);
     CK(cudaGetLastError());
   } else {
@@ -744,12 +809,40 @@ long long moe_layer_get_stat(moe_layer_t* h, int key) {
     case MOE_STAT_GEMM_TASKS: return h->last.stat_gemm;
     case MOE_STAT_MOVER_TASKS: return h->last.stat_mover;
     case MOE_STAT_STOLEN: return h->last.stat_stolen;
+    case MOE_STAT_AHEAD: return h->last.stat_ahead;
+    case MOE_STAT_TRACE_RECORDS: return h->last.trace_n;
     default: return -1;
   }
 }
 
+int moe_layer_get_trace(moe_layer_t* h, uint64_t* records, int cap, void* stream) {
+  if (!h || !h->ws || cap < 0 || (cap > 0 && !records)) {
+    g_err = "bad arguments";
+    return -1;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) {
+    g_err = "cudaStreamSynchronize failed";
+    return -1;
+  }
+  if (!h->trace) return 0;
+  int n = 0;
+  if (cudaMemcpy(&n, h->ws + h->o_sched + offsetof(Sched, trace_n), sizeof(int),
+                 cudaMemcpyDeviceToHost) != cudaSuccess) {
+    g_err = "cudaMemcpy failed";
+    return -1;
+  }
+  n = std::min(std::min(n, h->trace_cap), cap);
+  if (n > 0 && cudaMemcpy(records, h->trace, (size_t)n * 32, cudaMemcpyDeviceToHost) != cudaSuccess) {
+    g_err = "cudaMemcpy failed";
+    return -1;
+  }
+  return n;
+}
+
 void moe_layer_destroy(moe_layer_t* h) {
   if (!h) return;
+  if (h->trace) cudaFree(h->trace);
   if (h->ws) cudaFree(h->ws);
   if (h->x_dev_stage) cudaFree(h->x_dev_stage);
   if (h->out_dev_stage) cudaFree(h->out_dev_stage);

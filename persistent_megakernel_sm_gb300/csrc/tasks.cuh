@@ -16,8 +16,10 @@ struct Ctrl {
   uint64_t empty_bar[8];
   uint64_t acc_bar;
   unsigned long long deadline;
+  unsigned long long t_claim, t_start;
   uint32_t tmem_base;
   int task;
+  int next_task;
   int flag;
   int ival[8];
   int tok[kThreads];      // scratch: token ids / combine tiles per row
@@ -25,6 +27,10 @@ struct Ctrl {
   int aux[kMaxE];
   int aux2[kMaxE];
   float wsum[kThreads];
+  uint64_t gbar;                 // bulk-copy barrier of the gather
+  uint64_t cbar[2];              // bulk-copy barriers of the combine (two buffers)
+  uint32_t mask[kMaxE * 4];      // router: 128-bit token mask per expert
+  float bias_s[kMaxE];
 };
 
 // Per-thread state that lives across tasks.
@@ -33,6 +39,8 @@ struct CtaState {
   uint32_t gemm_count;  // GEMM tasks done (all threads)
   uint64_t deadline;    // globaltimer value after which waits give up
   int role_mover;       // 1 if this CTA prefers mover work (after the plan)
+  uint32_t gather_phase;  // parity of the gather barrier (thread 0)
+  uint32_t comb_phase;    // parities of the two combine barriers (bits 0, 1; all threads)
 };
 
 // ------------------------------------------------------------------ helpers
@@ -96,226 +104,159 @@ __device__ __forceinline__ void release_writes() {
 __device__ __forceinline__ Group load_group(const Params& p, int g) {
   if (g < p.n_shared_groups) {
     const int t0 = g * p.bn_max;
-    return Group{p.E, p.T * p.k + t0, min(p.bn_max, p.T - t0), t0};
+    return Group{p.E, p.T * p.k + t0, min(p.bn_max, p.T - t0), t0, 0, p.n_shared_groups, 0, 0};
   }
-  Group G;
-  G.e = __ldcg(&p.groups[g].e);
-  G.row0 = __ldcg(&p.groups[g].row0);
-  G.nrows = __ldcg(&p.groups[g].nrows);
-  G.src_row0 = __ldcg(&p.groups[g].src_row0);
-  return G;
+  const int4 a = __ldcg(reinterpret_cast<const int4*>(p.groups + g));
+  const int4 b = __ldcg(reinterpret_cast<const int4*>(p.groups + g) + 1);
+  return Group{a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 }
 
 __device__ __forceinline__ bool group_ok(const Params& p, const Group& G) {
   return G.nrows >= 1 && G.nrows <= p.bn_max && G.e >= 0 && G.e <= p.E && G.row0 >= 0 &&
-         G.row0 + G.nrows <= p.rows_y;
+         G.row0 + G.nrows <= p.rows_y && G.nsib >= 1 && G.sib0 >= 0 &&
+         G.sib0 + G.nsib <= p.max_groups;
 }
 
 // ------------------------------------------------------------------ queues
 // Two ticket queues.  Slots [0, n_static) of a queue are implicit tasks known
 // at launch (router tiles for the mover queue, shared-expert gate/up tiles
 // for the GEMM queue).  Later slots are reserved by pushers with an atomic add
-// on `tail` and filled with a release store; ring entries start at -1.
+// on `tail` and filled with a release store of (task id + 1); ring entries
+// start at 0 (empty), so one zero memset resets the whole scheduler.
 
 struct QueueRef {
-  int* head;
-  int* tail;
+  unsigned long long* word;  // head (low 32) | tail (high 32)
   int* ring;
   int n_static;
   int cap;
 };
 
 __device__ __forceinline__ QueueRef mover_queue(const Params& p) {
-  return QueueRef{&p.sched->mover_head, &p.sched->mover_tail, p.ring_mover, p.n_route,
-                  p.mover_cap};
+  return QueueRef{&p.sched->mover_q, p.ring_mover, p.n_route, p.mover_cap};
 }
 
 __device__ __forceinline__ QueueRef gemm_queue(const Params& p) {
-  return QueueRef{&p.sched->gemm_head, &p.sched->gemm_tail, p.ring_gemm, p.n_static_gemm,
-                  p.gemm_cap};
+  return QueueRef{&p.sched->gemm_q, p.ring_gemm, p.n_static_gemm, p.gemm_cap};
 }
 
-// Push n consecutive tasks id0, id0 + step, ...  Called by all 32 lanes of one warp.
-__device__ __forceinline__ void push_tasks_warp(const Params& p, const QueueRef& q, int id0,
-                                                int step, int n) {
-  const int lane = threadIdx.x & 31;
-  int base = 0;
-  if (lane == 0) base = atomicAdd(q.tail, n);
-  base = __shfl_sync(0xffffffffu, base, 0);
-  if (base + n > q.cap) {
-    if (lane == 0) set_status(p, MOE_E_DEVICE, 1);
-    return;
-  }
-  for (int i = lane; i < n; i += 32) st_release(q.ring + base + i, id0 + i * step);
-}
-
-// Try to claim one task: >= 0 task id, -1 nothing claimable now, -2 this
-// queue is finished.  Thread 0 only.
-__device__ int try_claim(const Params& p, const QueueRef& q, int total_dyn, bool plan_done,
-                         uint64_t deadline) {
-  const int h = ld_relaxed(q.head);
-  const int avail = q.n_static + ld_acquire(q.tail);
-  if (h >= avail) {
-    if (plan_done && h >= q.n_static + total_dyn) return -2;
-    return -1;
-  }
-  if (atomicCAS(q.head, h, h + 1) != h) return -1;
-  if (h < q.n_static) return -(1000 + h);  // implicit task, decoded by the caller
-  int v;
-  while ((v = ld_acquire(q.ring + (h - q.n_static))) < 0) {
-    if (globaltimer() > deadline) {
-      set_status(p, MOE_E_TIMEOUT, 2);
-      return -3;
-    }
-    if (ld_relaxed(&p.sched->status) != 0) return -3;
-  }
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
 
-// Decide this CTA's next task (thread 0).  Returns a task id or -1 to exit.
-__device__ int claim_next(const Params& p, CtaState& st) {
-  Sched* s = p.sched;
-  uint32_t backoff = 32;
+// Reserve n slots at the tail of a queue; returns the first dynamic index.
+__device__ __forceinline__ int queue_reserve(const QueueRef& q, int n) {
+  const unsigned long long old = atomicAdd(q.word, (unsigned long long)n << 32);
+  return (int)(old >> 32);
+}
+
+// Try to claim one task: >= 0 task id, -1 nothing claimable now, -2 this
+// queue is finished, -3 abort.  `min_depth`: claim only if at least that many
+// tasks are waiting (used to claim ahead without starving other CTAs).
+// When at least `fa_depth` tasks wait, the claim is one fetch-and-add on the
+// head (all claimers are served at the L2's atomic rate); otherwise a CAS
+// that never takes a slot that has not been pushed.  A fetch-and-add can only
+// overshoot the tail if more than fa_depth claims race with it; the overshot
+// ticket then waits for its slot to be pushed, or turns out void when the
+// queue's final size is known and lies below it.
+__device__ int try_claim(const Params& p, const QueueRef& q, const int* total_dyn_ptr,
+                         uint64_t deadline, int min_depth, int fa_depth) {
+  unsigned long long v = ld_acquire_u64(q.word);
   while (true) {
-    if (ld_relaxed(&s->status) != 0) return -1;
-    const bool plan_done = ld_acquire(&s->plan_done) != 0;
-    int mover_total = 0, gemm_total = 0;
-    if (plan_done) {
-      mover_total = ld_relaxed(&s->mover_total_dyn);
-      gemm_total = ld_relaxed(&s->gemm_total_dyn);
-      st.role_mover = (int)blockIdx.x < ld_relaxed(&s->n_movers);
+    const int h = (int)(v & 0xffffffffu);
+    const int avail = q.n_static + (int)(v >> 32);
+    if (h >= avail) {
+      if (ld_acquire(&p.sched->plan_done) && h >= q.n_static + ld_relaxed(total_dyn_ptr))
+        return -2;
+      return -1;
     }
-    // Before the plan every CTA prefers router tiles (they gate everything);
-    // afterwards each CTA prefers its own role's queue and steals otherwise.
-    const bool mover_first = !plan_done || st.role_mover;
-    QueueRef qa = mover_first ? mover_queue(p) : gemm_queue(p);
-    QueueRef qb = mover_first ? gemm_queue(p) : mover_queue(p);
-    const int ta = mover_first ? mover_total : gemm_total;
-    const int tb = mover_first ? gemm_total : mover_total;
-    int finished = 0;
-    for (int pass = 0; pass < 2; ++pass) {
-      const QueueRef& q = pass == 0 ? qa : qb;
-      int r = try_claim(p, q, pass == 0 ? ta : tb, plan_done, st.deadline);
-      if (r == -3) return -1;
-      if (r == -2) {
-        ++finished;
+    if (avail - h < min_depth) return -1;
+    int slot = -1;
+    if (avail - h >= fa_depth) {
+      slot = (int)(atomicAdd(q.word, 1ull) & 0xffffffffu);
+    } else {
+      const unsigned long long seen = atomicCAS(q.word, v, v + 1);
+      if (seen != v) {
+        v = seen;  // lost the race: retry at once with the fresh word
         continue;
       }
-      if (r == -1) continue;
-      const bool is_mover_q = (q.ring == p.ring_mover);
-      if (r <= -1000) {
-        const int slot = -(r + 1000);
-        r = is_mover_q ? task_id(kTaskRoute, slot) : task_id(kTaskGateUp, slot);
-      }
-      if (pass == 1 && plan_done) atomicAdd(&s->stat_stolen, 1);
-      return r;
+      slot = h;
     }
-    if (finished == 2) return -1;
+    if (slot < q.n_static) return -(1000 + slot);  // implicit task, decoded by the caller
+    int e;
+    while ((e = ld_acquire(q.ring + (slot - q.n_static))) == 0) {
+      if (ld_relaxed(&p.sched->status) != 0) return -3;
+      if (ld_acquire(&p.sched->plan_done) && slot >= q.n_static + ld_relaxed(total_dyn_ptr))
+        return -2;  // an overshot ticket beyond the final size: nothing to run
+      if (globaltimer() > deadline) {
+        set_status(p, MOE_E_TIMEOUT, 2);
+        return -3;
+      }
+    }
+    return e - 1;
+  }
+}
+
+// One scheduling decision: the preferred queue first, then the other one.
+// Returns a task id, -1 if nothing is claimable now, -2 if both queues are
+// finished, -3 to abort.
+__device__ int claim_once(const Params& p, CtaState& st, int min_depth) {
+  Sched* s = p.sched;
+  if (ld_relaxed(&s->status) != 0) return -3;
+  const bool plan_done = ld_acquire(&s->plan_done) != 0;
+  bool gathers_left = false;
+  if (plan_done) {
+    st.role_mover = (int)blockIdx.x < ld_relaxed(&s->n_movers);
+    const unsigned long long mw = *reinterpret_cast<volatile unsigned long long*>(&s->mover_q);
+    gathers_left = (int)(mw & 0xffffffffu) < p.n_route + ld_relaxed(&s->n_gather);
+  }
+  // Before the plan every CTA prefers router tiles, and afterwards every CTA
+  // prefers gathers while any is unclaimed: both gate all the GEMM work.
+  // Otherwise each CTA prefers its own role's queue and steals from the other.
+  const bool mover_first = !plan_done || gathers_left || st.role_mover;
+  int finished = 0;
+  for (int pass = 0; pass < 2; ++pass) {
+    const bool use_mover = (pass == 0) == mover_first;
+    const QueueRef q = use_mover ? mover_queue(p) : gemm_queue(p);
+    int r = try_claim(p, q, use_mover ? &s->mover_total_dyn : &s->gemm_total_dyn, st.deadline,
+                      min_depth, p.fa_depth);
+    if (r == -3) return -3;
+    if (r == -2) {
+      ++finished;
+      continue;
+    }
+    if (r == -1) continue;
+    if (r <= -1000) {
+      const int slot = -(r + 1000);
+      if (use_mover) {
+        r = task_id(kTaskRoute, slot);
+      } else {  // shared-expert gate/up tiles, f-tile major across the groups
+        const int nsg = p.n_shared_groups;
+        r = task_id(kTaskGateUp, (slot % nsg) * p.n_ftiles + slot / nsg);
+      }
+    }
+    if (pass == 1 && plan_done) atomicAdd(&s->stat_stolen, 1);
+    return r;
+  }
+  return finished == 2 ? -2 : -1;
+}
+
+// Decide this CTA's next task (thread 0), waiting with back-off until one is
+// claimable.  Returns a task id or -1 to exit.
+__device__ int claim_next(const Params& p, CtaState& st) {
+  uint32_t backoff = 32;
+  while (true) {
+    const int r = claim_once(p, st, 1);
+    if (r >= 0) return r;
+    if (r == -2 || r == -3) return -1;
     if (globaltimer() > st.deadline) {
       set_status(p, MOE_E_TIMEOUT, 3);
       return -1;
     }
     __nanosleep(backoff);
-    if (backoff < 1024) backoff <<= 1;
+    if (backoff < 512) backoff <<= 1;
   }
-}
-
-// ------------------------------------------------------------------ router
-// Router tile: tokens [tau*rt, tau*rt + nt).  Logits on CUDA cores (fp32
-// accumulate of bf16 products), softmax over all E, top-k by (p desc, e asc),
-// renormalised weights, and the tile's per-expert counts and ranks.
-__device__ void route_task(const Params& p, int tau, char* scratch, Ctrl* c) {
-  const int t0 = tau * p.rt;
-  const int nt = min(p.rt, p.T - t0);
-  const int E = p.E, k = p.k;
-  float* logit = reinterpret_cast<float*>(scratch);  // [rt][E]
-  int* sidx = reinterpret_cast<int*>(logit + p.rt * E);  // [rt][k]
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nvec = p.d >> 3;
-
-  for (int pr = warp; pr < nt * E; pr += kThreads / 32) {
-    const int t = pr / E, e = pr - t * E;
-    const uint4* xr = reinterpret_cast<const uint4*>(p.x + (size_t)(t0 + t) * p.d);
-    const uint4* wrr = reinterpret_cast<const uint4*>(p.wr + (size_t)e * p.d);
-    float acc = 0.f;
-#pragma unroll 4
-    for (int v = lane; v < nvec; v += 32) acc += dot8(__ldg(xr + v), __ldg(wrr + v));
-    acc = warp_sum(acc);
-    if (lane == 0) logit[t * E + e] = acc + (p.bias ? __ldg(p.bias + e) : 0.f);
-  }
-  __syncthreads();
-
-  for (int t = warp; t < nt; t += kThreads / 32) {
-    float v[kMaxE / 32];
-    float mx = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < kMaxE / 32; ++i) {
-      const int e = lane + 32 * i;
-      v[i] = e < E ? logit[t * E + e] : -INFINITY;
-      mx = fmaxf(mx, v[i]);
-    }
-    mx = warp_max(mx);
-    float z = 0.f;
-#pragma unroll
-    for (int i = 0; i < kMaxE / 32; ++i) {
-      const int e = lane + 32 * i;
-      v[i] = e < E ? __expf(v[i] - mx) : 0.f;
-      z += v[i];
-    }
-    z = warp_sum(z);
-    const float invz = 1.f / z;
-#pragma unroll
-    for (int i = 0; i < kMaxE / 32; ++i) v[i] = (lane + 32 * i) < E ? v[i] * invz : -1.f;
-    float kept = 0.f, my_p = 0.f;
-    int my_e = 0;
-    for (int j = 0; j < k; ++j) {
-      float bp = -2.f;
-      int be = 0x7fffffff;
-#pragma unroll
-      for (int i = 0; i < kMaxE / 32; ++i)
-        if (v[i] > bp) {
-          bp = v[i];
-          be = lane + 32 * i;
-        }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float op = __shfl_xor_sync(0xffffffffu, bp, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (op > bp || (op == bp && oe < be)) {
-          bp = op;
-          be = oe;
-        }
-      }
-      if ((be & 31) == lane) {
-#pragma unroll
-        for (int i = 0; i < kMaxE / 32; ++i)
-          if (i == (be >> 5)) v[i] = -2.f;
-      }
-      if (lane == j) {
-        my_p = bp;
-        my_e = be;
-      }
-      kept += bp;
-    }
-    if (lane < k) {
-      const size_t o = (size_t)(t0 + t) * k + lane;
-      p.idx[o] = my_e;
-      p.wgt[o] = my_p / kept;
-      sidx[t * k + lane] = my_e;
-    }
-  }
-  for (int e = threadIdx.x; e < E; e += kThreads) c->cnt[e] = 0;
-  __syncthreads();
-  for (int ent = threadIdx.x; ent < nt * k; ent += kThreads) {
-    const int t = ent / k;
-    const int e = sidx[ent];
-    int r = 0;
-    for (int q = 0; q < t * k; ++q) r += (sidx[q] == e);
-    p.rank[(size_t)t0 * k + ent] = r;
-    atomicAdd(&c->cnt[e], 1);
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += kThreads) p.tile_cnt[(size_t)tau * E + e] = c->cnt[e];
 }
 
 // ------------------------------------------------------------------ plan
@@ -354,18 +295,26 @@ __device__ __forceinline__ int gather_chunks(int nrows) { return ceil_div(nrows,
 // groups (experts in order of decreasing count, each split into balanced
 // tiles of at most bn_max rows), the cost-model split of CTAs into movers and
 // GEMM workers, and (persistent mode) the first pushes: every gather task.
-__device__ void plan_task(const Params& p, Ctrl* c, bool push) {
+__device__ void plan_task(const Params& p, char* scratch, Ctrl* c, bool push) {
   const int E = p.E, k = p.k, tid = threadIdx.x;
   int* cnt = c->cnt;     // counts per expert
   int* order = c->aux;   // experts by decreasing count
   int* offs = c->aux2;   // offsets per expert
 
-  // per expert: exclusive prefix over router tiles, in place, and the count
+  // per expert: exclusive prefix of the router tiles' counts (the tile bases)
+  // and the total; in shared memory when the [tiles, E] table fits
+  const int ntile = p.n_route;
+  const bool in_smem = (size_t)ntile * E * 4 <= (size_t)p.stages * p.stage_bytes;
+  int* tb = in_smem ? reinterpret_cast<int*>(scratch) : p.tile_cnt;
+  if (in_smem) {
+    for (int i = tid; i < ntile * E; i += kThreads) tb[i] = __ldcg(p.tile_cnt + i);
+    __syncthreads();
+  }
   if (tid < E) {
     int run = 0;
-    for (int tau = 0; tau < p.n_route; ++tau) {
-      int* q = p.tile_cnt + (size_t)tau * E + tid;
-      const int v = __ldcg(q);
+    for (int tau = 0; tau < ntile; ++tau) {
+      int* q = tb + (size_t)tau * E + tid;
+      const int v = in_smem ? *q : __ldcg(q);
       *q = run;
       run += v;
     }
@@ -411,27 +360,44 @@ __device__ void plan_task(const Params& p, Ctrl* c, bool push) {
   // routed groups follow the shared-expert groups (see load_group)
   {
     int cb = chunk_base;
+    const int sib0 = p.n_shared_groups + gfirst;
     for (int m = 0; m < nmt; ++m) {
-      const int g = p.n_shared_groups + gfirst + m;
+      const int g = sib0 + m;
       const int nrows = min(rows_per, n_r - m * rows_per);
       const int row0 = off_e + m * rows_per;
-      p.groups[g] = Group{e_r, row0, nrows, row0};
+      p.groups[g] = Group{e_r, row0, nrows, row0, sib0, nmt, my_chunks, 0};
       if (push) {
         const int nc = gather_chunks(nrows);
-        for (int q = 0; q < nc; ++q) p.ring_mover[cb + q] = task_id(kTaskGather, g * 8 + q);
+        for (int q = 0; q < nc; ++q) p.ring_mover[cb + q] = task_id(kTaskGather, g * 8 + q) + 1;
         cb += nc;
       }
     }
   }
   __syncthreads();
-  // the canonical permutation
-  for (int ent = tid; ent < p.T * k; ent += kThreads) {
-    const int t = ent / k;
-    const int e = __ldcg(p.idx + ent);
-    const int tau = t / p.rt;
-    const int row = offs[e] + __ldcg(p.tile_cnt + (size_t)tau * E + e) + __ldcg(p.rank + ent);
-    p.perm[row] = t;
-    p.pos[ent] = row;
+  // the canonical permutation: row = offset of e + base of (tile, e) + rank
+  {
+    const int n = p.T * k;
+    constexpr int U = 4;
+    for (int b = tid; b < n; b += kThreads * U) {
+      int e[U], r[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int ent = b + u * kThreads;
+        e[u] = ent < n ? __ldcg(p.idx + ent) : 0;
+        r[u] = ent < n ? __ldcg(p.rank + ent) : 0;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int ent = b + u * kThreads;
+        if (ent < n) {
+          const int t = ent / k;
+          const int* q = tb + (size_t)(t / p.rt) * E + e[u];
+          const int row = offs[e[u]] + (in_smem ? *q : __ldcg(q)) + r[u];
+          p.perm[row] = t;
+          p.pos[ent] = row;
+        }
+      }
+    }
   }
   // cost model (spatial split): CTA-seconds of mover work against GEMM work
   if (tid == 0) {
@@ -441,6 +407,7 @@ __device__ void plan_task(const Params& p, Ctrl* c, bool push) {
     s->n_groups = n_groups;
     s->gemm_total_dyn = n_routed * p.n_ftiles + n_groups * n_down;
     s->mover_total_dyn = n_gather + p.n_comb;
+    s->n_gather = n_gather;
     int movers;
     const int N = gridDim.x;
     if (p.mover_override > 0) {
@@ -465,7 +432,7 @@ __device__ void plan_task(const Params& p, Ctrl* c, bool push) {
   if (push) {
     release_writes();
     if (tid == 0) {
-      atomicAdd(&p.sched->mover_tail, n_gather);
+      queue_reserve(mover_queue(p), n_gather);
       __threadfence();
       st_release(&p.sched->plan_done, 1);
     }
@@ -475,8 +442,12 @@ __device__ void plan_task(const Params& p, Ctrl* c, bool push) {
 }
 
 // ------------------------------------------------------------------ gather (mover)
-// Xp[row, :] = x[perm[row], :] for up to 32 rows of one group.
-__device__ void gather_task(const Params& p, int g, int chunk, Ctrl* c) {
+// Xp[row, :] = x[perm[row], :] for up to 32 rows of one group.  One thread
+// moves whole rows with bulk copies through shared memory (global -> shared
+// on an mbarrier, then shared -> global), as many rows per round as the
+// pipeline stages hold, so hundreds of KB are in flight per SM.
+__device__ void gather_task(const Params& p, int g, int chunk, char* smem, Ctrl* c,
+                            CtaState& st) {
   const Group G = load_group(p, g);
   if (!group_ok(p, G) || chunk * kGatherRows >= G.nrows) {
     if (threadIdx.x == 0) set_status(p, MOE_E_DEVICE, 20);
@@ -486,64 +457,45 @@ __device__ void gather_task(const Params& p, int g, int chunk, Ctrl* c) {
   const int nr = min(kGatherRows, G.nrows - chunk * kGatherRows);
   if (threadIdx.x < nr) c->tok[threadIdx.x] = __ldcg(p.perm + r0 + threadIdx.x);
   __syncthreads();
-  const int nvec = p.d >> 3;
-  const int total = nr * nvec;
-  const uint4* x = reinterpret_cast<const uint4*>(p.x);
-  uint4* xp = reinterpret_cast<uint4*>(p.Xp);
-  constexpr int U = 8;
-  for (int base = threadIdx.x; base < total; base += kThreads * U) {
-    uint4 v[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int i = base + u * kThreads;
-      if (i < total) {
-        const int r = i / nvec, q = i - r * nvec;
-        v[u] = __ldg(x + (size_t)c->tok[r] * nvec + q);
+  if (threadIdx.x == 0) {
+    const uint32_t row_bytes = (uint32_t)p.d * 2;
+    const int cap = max(1, (int)(((size_t)p.stages * p.stage_bytes) / row_bytes));
+    fence_proxy_async_shared();
+    for (int r = 0; r < nr; r += cap) {
+      const int n = min(cap, nr - r);
+      mbar_arrive_expect_tx(&c->gbar, (uint32_t)n * row_bytes);
+      for (int i = 0; i < n; ++i)
+        bulk_load(smem + (size_t)i * row_bytes, p.x + (size_t)c->tok[r + i] * p.d, row_bytes,
+                  &c->gbar);
+      if (!mbar_wait(&c->gbar, st.gather_phase, st.deadline)) {
+        set_status(p, MOE_E_TIMEOUT, 21);
+        break;
       }
+      st.gather_phase ^= 1u;
+      for (int i = 0; i < n; ++i)
+        bulk_store(p.Xp + (size_t)(r0 + r + i) * p.d, smem + (size_t)i * row_bytes, row_bytes);
+      bulk_commit();
+      bulk_wait_read_all();
     }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int i = base + u * kThreads;
-      if (i < total) {
-        const int r = i / nvec, q = i - r * nvec;
-        xp[(size_t)(r0 + r) * nvec + q] = v[u];
-      }
-    }
+    bulk_wait_all();
   }
 }
 
 // ------------------------------------------------------------------ combine (mover)
-// out[t, :] = bf16( sum_j w[t,j] * Y[pos[t,j], :] + Y[T k + t, :] (shared) ),
-// fp32 sum in slot order, then the shared expert; K splits summed first.
-__device__ void combine_task(const Params& p, int ctile, Ctrl* c) {
-  const int t0 = ctile * p.ct;
-  const int nt = min(p.ct, p.T - t0);
-  const int k = p.k;
-  for (int i = threadIdx.x; i < nt * k; i += kThreads) {
-    c->tok[i] = __ldcg(p.pos + (size_t)t0 * k + i);
-    c->wsum[i] = __ldcg(p.wgt + (size_t)t0 * k + i);
-  }
-  __syncthreads();
+// Combine straight from global memory (rows too large for shared memory).
+__device__ void combine_direct(const Params& p, int t0, int nt, Ctrl* c) {
+  const int k = p.k, nsrc = k + p.S;
   const int nvec = p.d >> 3;
-  const int total = nt * nvec;
   uint4* out = reinterpret_cast<uint4*>(p.out);
-  const size_t part = (size_t)p.rows_y * p.d;  // elements per K split
-  for (int i = threadIdx.x; i < total; i += kThreads) {
+  const size_t part = (size_t)p.rows_y * p.d;
+  for (int i = threadIdx.x; i < nt * nvec; i += kThreads) {
     const int t = i / nvec, q = i - t * nvec;
     float acc[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) acc[u] = 0.f;
-    for (int j = 0; j <= k; ++j) {
-      int row;
-      float w;
-      if (j < k) {
-        row = c->tok[t * k + j];
-        w = c->wsum[t * k + j];
-      } else {
-        if (!p.S) break;
-        row = p.T * k + t0 + t;
-        w = 1.f;
-      }
+    for (int j = 0; j < nsrc; ++j) {
+      const int row = j < k ? c->tok[t * k + j] : p.T * k + t0 + t;
+      const float w = j < k ? c->wsum[t * k + j] : 1.f;
       float y[8];
       if (p.y_f32) {
         const float* Y = reinterpret_cast<const float*>(p.Y);
@@ -557,13 +509,106 @@ __device__ void combine_task(const Params& p, int ctile, Ctrl* c) {
           y[4] += b.x; y[5] += b.y; y[6] += b.z; y[7] += b.w;
         }
       } else {
-        const uint4* Y = reinterpret_cast<const uint4*>(p.Y);
-        bf16x8_to_f32(__ldcg(Y + (size_t)row * nvec + q), y);
+        bf16x8_to_f32(__ldcg(reinterpret_cast<const uint4*>(p.Y) + (size_t)row * nvec + q), y);
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) acc[u] = fmaf(w, y[u], acc[u]);
     }
     out[(size_t)(t0 + t) * nvec + q] = f32x8_to_bf16(acc);
+  }
+}
+
+// out[t, :] = bf16( sum_j w[t,j] * Y[pos[t,j], :] + Y[T k + t, :] (shared) ),
+// fp32 sum in slot order, then the shared expert; with fp32 K-split partials
+// each source row is the sum of its splits.  The source rows of a few tokens
+// at a time are bulk-copied into one half of the pipeline's shared memory
+// while the other half is being summed (double buffering).
+__device__ void combine_task(const Params& p, int ctile, char* smem, Ctrl* c, CtaState& st) {
+  const int t0 = ctile * p.ct;
+  const int nt = min(p.ct, p.T - t0);
+  const int k = p.k;
+  for (int i = threadIdx.x; i < nt * k; i += kThreads) {
+    c->tok[i] = __ldcg(p.pos + (size_t)t0 * k + i);
+    c->wsum[i] = __ldcg(p.wgt + (size_t)t0 * k + i);
+  }
+  __syncthreads();
+  const int nsrc = k + p.S;
+  const int nsplit = p.y_f32 ? p.ks : 1;
+  const int ebytes = p.y_f32 ? 4 : 2;
+  const uint32_t row_bytes = (uint32_t)p.d * ebytes;
+  const size_t per_tok = (size_t)nsrc * nsplit * row_bytes;
+  const size_t mem = (size_t)p.stages * p.stage_bytes;
+  if (per_tok > mem) {  // one token's rows do not fit: sum straight from global
+    combine_direct(p, t0, nt, c);
+    return;
+  }
+  const int nbuf = per_tok * 2 <= mem ? 2 : 1;
+  const size_t half = mem / nbuf;          // bytes of one buffer
+  const int tpr = (int)(half / per_tok);   // tokens per round
+  const int rounds = (nt + tpr - 1) / tpr;
+  const size_t part_bytes = (size_t)p.rows_y * p.d * ebytes;
+  const char* Yb = reinterpret_cast<const char*>(p.Y);
+  auto issue = [&](int r) {  // thread 0: bulk loads of round r into buffer r % nbuf
+    const int b = r % nbuf;
+    const int ta = r * tpr, n = min(tpr, nt - ta);
+    char* buf = smem + b * half;
+    mbar_arrive_expect_tx(&c->cbar[b], (uint32_t)(n * per_tok));
+    for (int tt = 0; tt < n; ++tt) {
+      const int t = ta + tt;
+      for (int j = 0; j < nsrc; ++j) {
+        const int row = j < k ? c->tok[t * k + j] : p.T * k + t0 + t;
+        for (int s = 0; s < nsplit; ++s)
+          bulk_load(buf + ((size_t)(tt * nsrc + j) * nsplit + s) * row_bytes,
+                    Yb + s * part_bytes + (size_t)row * row_bytes, row_bytes, &c->cbar[b]);
+      }
+    }
+  };
+  if (threadIdx.x == 0) {
+    fence_proxy_async_shared();
+    issue(0);
+    if (nbuf == 2 && rounds > 1) issue(1);
+  }
+  const int nvec = p.d >> 3;
+  uint4* out = reinterpret_cast<uint4*>(p.out);
+  for (int r = 0; r < rounds; ++r) {
+    const int b = r % nbuf;
+    const bool got = mbar_wait(&c->cbar[b], (st.comb_phase >> b) & 1u, st.deadline);
+    st.comb_phase ^= 1u << b;
+    if (!__syncthreads_and(got ? 1 : 0)) {
+      if (threadIdx.x == 0) set_status(p, MOE_E_TIMEOUT, 24);
+      return;
+    }
+    const int ta = r * tpr, n = min(tpr, nt - ta);
+    const char* buf = smem + b * half;
+    for (int i = threadIdx.x; i < n * nvec; i += kThreads) {
+      const int tt = i / nvec, q = i - tt * nvec;
+      const int t = ta + tt;
+      float acc[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) acc[u] = 0.f;
+      for (int j = 0; j < nsrc; ++j) {
+        const float w = j < k ? c->wsum[t * k + j] : 1.f;
+        const char* src = buf + (size_t)(tt * nsrc + j) * nsplit * row_bytes;
+        float y[8];
+        if (p.y_f32) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) y[u] = 0.f;
+          for (int s = 0; s < nsplit; ++s) {
+            const float4* v = reinterpret_cast<const float4*>(src + s * row_bytes) + 2 * q;
+            const float4 a = v[0], bb = v[1];
+            y[0] += a.x; y[1] += a.y; y[2] += a.z; y[3] += a.w;
+            y[4] += bb.x; y[5] += bb.y; y[6] += bb.z; y[7] += bb.w;
+          }
+        } else {
+          bf16x8_to_f32(reinterpret_cast<const uint4*>(src)[q], y);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) acc[u] = fmaf(w, y[u], acc[u]);
+      }
+      out[(size_t)(t0 + t) * nvec + q] = f32x8_to_bf16(acc);
+    }
+    __syncthreads();  // buffer b is free again
+    if (threadIdx.x == 0 && r + nbuf < rounds) issue(r + nbuf);
   }
 }
 
@@ -579,27 +624,32 @@ __device__ void combine_task(const Params& p, int ctile, Ctrl* c) {
 
 struct GemmJob {
   const CUtensorMap* a0;
-  const CUtensorMap* a1;
+  const CUtensorMap* a1;  // null: one accumulator only
   const CUtensorMap* b;
-  int a_row0, a1_row0;  // weight rows of the two accumulators
-  int b_row0;           // first B row
-  int nrows;            // tokens (columns of the accumulators)
-  int kb0, nkb;         // first k block and number of k blocks
+  int a_row0, a1_row0;    // A rows of the two accumulators
+  int b_row0;             // first B row
+  int b_rows;             // B rows to load (boxes of 32 rows)
+  int n_mma;              // MMA N (multiple of 16, <= 256)
+  int b_off;              // byte offset of the B tile inside a stage (1024-aligned)
+  int kb0, nkb;           // first k block and number of k blocks
+  bool a_stream;          // A is streamed once (evict-first); else B is
 };
 
 // Returns false on a timeout (status already set).
 __device__ bool gemm_mainloop(const Params& p, const GemmJob& job, char* smem, Ctrl* c,
                               CtaState& st) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nbox = ceil_div(job.nrows, kBBoxRows);
-  const uint32_t n_mma = (uint32_t)(((job.nrows + 15) / 16) * 16);
+  const int nbox = ceil_div(job.b_rows, kBBoxRows);
+  const bool two = job.a1 != nullptr;
   bool ok = true;
   if (warp == 0 && lane == 0) {
     fence_proxy_async_global();
     fence_proxy_async_shared();
-    const uint64_t pol_w = policy_evict_first();
-    const uint64_t pol_a = policy_evict_last();
-    const uint32_t bytes = 2u * kABoxBytes + (uint32_t)nbox * kBBoxBytes;
+    const uint64_t pol_first = policy_evict_first();
+    const uint64_t pol_last = policy_evict_last();
+    const uint64_t pol_a = job.a_stream ? pol_first : pol_last;
+    const uint64_t pol_b = job.a_stream ? pol_last : pol_first;
+    const uint32_t bytes = (two ? 2u : 1u) * kABoxBytes + (uint32_t)nbox * kBBoxBytes;
     uint32_t it = st.pipe_it;
     for (int kb = 0; kb < job.nkb; ++kb, ++it) {
       const uint32_t s = it % p.stages, ph = (it / p.stages) & 1u;
@@ -611,14 +661,14 @@ __device__ bool gemm_mainloop(const Params& p, const GemmJob& job, char* smem, C
       char* stage = smem + (size_t)s * p.stage_bytes;
       mbar_arrive_expect_tx(&c->full_bar[s], bytes);
       const int kc = (job.kb0 + kb) * kBK;
-      tma_load_2d(stage, job.a0, &c->full_bar[s], kc, job.a_row0, pol_w);
-      tma_load_2d(stage + kABoxBytes, job.a1, &c->full_bar[s], kc, job.a1_row0, pol_w);
+      tma_load_2d(stage, job.a0, &c->full_bar[s], kc, job.a_row0, pol_a);
+      if (two) tma_load_2d(stage + kABoxBytes, job.a1, &c->full_bar[s], kc, job.a1_row0, pol_a);
       for (int bx = 0; bx < nbox; ++bx)
-        tma_load_2d(stage + 2 * kABoxBytes + bx * kBBoxBytes, job.b, &c->full_bar[s], kc,
-                    job.b_row0 + bx * kBBoxRows, pol_a);
+        tma_load_2d(stage + job.b_off + bx * kBBoxBytes, job.b, &c->full_bar[s], kc,
+                    job.b_row0 + bx * kBBoxRows, pol_b);
     }
   } else if (warp == 1 && lane == 0) {
-    const uint32_t idesc = idesc_bf16(kBM, n_mma);
+    const uint32_t idesc = idesc_bf16(kBM, (uint32_t)job.n_mma);
     const uint32_t t0 = c->tmem_base, t1 = c->tmem_base + kAcc1Col;
     uint32_t it = st.pipe_it;
     for (int kb = 0; kb < job.nkb; ++kb, ++it) {
@@ -631,14 +681,14 @@ __device__ bool gemm_mainloop(const Params& p, const GemmJob& job, char* smem, C
       tc_fence_after();
       const uint32_t base = smem_u32(smem + (size_t)s * p.stage_bytes);
       const uint64_t da0 = sw128_desc(base), da1 = sw128_desc(base + kABoxBytes);
-      const uint64_t db = sw128_desc(base + 2 * kABoxBytes);
+      const uint64_t db = sw128_desc(base + job.b_off);
 #pragma unroll
       for (int kk = 0; kk < kBK / 16; ++kk) {
         const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
         // advancing 16 bf16 (32 B) inside the 128-B swizzle row: +2 in the
         // 16-byte-granular start-address field
         mma_bf16(t0, da0 + 2 * kk, db + 2 * kk, idesc, acc);
-        mma_bf16(t1, da1 + 2 * kk, db + 2 * kk, idesc, acc);
+        if (two) mma_bf16(t1, da1 + 2 * kk, db + 2 * kk, idesc, acc);
       }
       mma_commit(&c->empty_bar[s]);
     }
@@ -672,9 +722,12 @@ __device__ void gateup_task(const Params& p, const Maps& maps, int g, int ft, ch
   job.a_row0 = G.e * p.f + ft * kBM;
   job.a1_row0 = job.a_row0;
   job.b_row0 = G.src_row0;
-  job.nrows = G.nrows;
+  job.b_rows = G.nrows;
+  job.n_mma = ((G.nrows + 15) / 16) * 16;
+  job.b_off = 2 * kABoxBytes;
   job.kb0 = 0;
   job.nkb = p.d / kBK;
+  job.a_stream = true;
   const bool ok = gemm_mainloop(p, job, smem, c, st);
   if (ok) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -710,9 +763,12 @@ __device__ void down_task(const Params& p, const Maps& maps, int g, int dt, int 
   job.a_row0 = G.e * p.d + dt * 2 * kBM;
   job.a1_row0 = job.a_row0 + kBM;
   job.b_row0 = G.row0;
-  job.nrows = G.nrows;
+  job.b_rows = G.nrows;
+  job.n_mma = ((G.nrows + 15) / 16) * 16;
+  job.b_off = 2 * kABoxBytes;
   job.kb0 = ksplit * p.kb_down;
   job.nkb = p.kb_down;
+  job.a_stream = true;
   const bool ok = gemm_mainloop(p, job, smem, c, st);
   if (ok) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -753,6 +809,139 @@ __device__ void down_task(const Params& p, const Maps& maps, int g, int dt, int 
   st.gemm_count++;
 }
 
+
+// ------------------------------------------------------------------ router (tcgen05)
+// Router tile: tokens [tau*128, tau*128 + nt).  Logits on the tensor core:
+// D[token, e] = x[token, :] . Wr[e, :], tokens as the M = 128 operand and the
+// E experts (padded to 16) as N; fp32 accumulation in TMEM.  Epilogue: one
+// thread per token walks its E logits (+ bias) once, keeping the running max
+// and sum of the softmax and the top-k list (logit descending, expert
+// ascending on ties -- the softmax is monotone, so this is the order of p).
+// Then p_j = exp(L_j - max) / sum and w_j = p_j / sum of the kept p.  Ranks
+// inside the tile come from a 128-bit token mask per expert.
+
+template <int KL>
+__device__ __forceinline__ void topk_insert(float (&tv)[KL], int (&te)[KL], float v, int e) {
+  if (!(v > tv[KL - 1])) return;
+  float cv = v;
+  int ce = e;
+#pragma unroll
+  for (int s = 0; s < KL; ++s) {
+    const bool sw = cv > tv[s];
+    const float ov = tv[s];
+    const int oe = te[s];
+    tv[s] = sw ? cv : ov;
+    te[s] = sw ? ce : oe;
+    cv = sw ? ov : cv;
+    ce = sw ? oe : ce;
+  }
+}
+
+template <int KL>
+__device__ __forceinline__ void route_epilogue(const Params& p, Ctrl* c, int t0, int nt) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = p.E, k = p.k;
+  float tv[KL];
+  int te[KL];
+#pragma unroll
+  for (int s = 0; s < KL; ++s) {
+    tv[s] = -INFINITY;
+    te[s] = 0x7fffffff;
+  }
+  const int m = warp * 32 + lane;
+  const bool valid = warp < 4 && m < nt;
+  float mx = -INFINITY, sum = 0.f;
+  if (warp < 4) {
+    const uint32_t lane_addr = c->tmem_base + ((uint32_t)(warp * 32) << 16);
+    for (int ch = 0; ch * 16 < E; ++ch) {
+      float v[16];
+      tmem_ld16(lane_addr + ch * 16, v);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int e = ch * 16 + i;
+        if (e < E) {
+          const float L = v[i] + c->bias_s[e];
+          if (L > mx) {
+            sum = sum * __expf(mx - L) + 1.f;
+            mx = L;
+          } else {
+            sum += __expf(L - mx);
+          }
+          topk_insert<KL>(tv, te, L, e);
+        }
+      }
+    }
+  }
+  float pk[KL];
+  float kept = 0.f;
+#pragma unroll
+  for (int s = 0; s < KL; ++s) {
+    pk[s] = s < k ? __expf(tv[s] - mx) / sum : 0.f;
+    kept += pk[s];
+  }
+  if (valid) {
+    const size_t o = (size_t)(t0 + m) * k;
+#pragma unroll
+    for (int s = 0; s < KL; ++s) {
+      if (s < k) {
+        p.idx[o + s] = te[s];
+        p.wgt[o + s] = pk[s] / kept;
+        atomicOr(&c->mask[te[s] * 4 + (m >> 5)], 1u << (m & 31));
+      }
+    }
+  }
+  __syncthreads();
+  if (valid) {
+    const size_t o = (size_t)(t0 + m) * k;
+    const int wd = m >> 5;
+    const uint32_t below = (1u << (m & 31)) - 1u;
+#pragma unroll
+    for (int s = 0; s < KL; ++s) {
+      if (s < k) {
+        const uint32_t* mk = c->mask + te[s] * 4;
+        int r = __popc(mk[wd] & below);
+        for (int q = 0; q < wd; ++q) r += __popc(mk[q]);
+        p.rank[o + s] = r;
+      }
+    }
+  }
+  for (int e = threadIdx.x; e < E; e += kThreads) {
+    const uint32_t* mk = c->mask + e * 4;
+    p.tile_cnt[(size_t)(t0 / kRouteTokens) * E + e] =
+        __popc(mk[0]) + __popc(mk[1]) + __popc(mk[2]) + __popc(mk[3]);
+  }
+}
+
+__device__ void route_task(const Params& p, const Maps& maps, int tau, char* smem, Ctrl* c,
+                           CtaState& st) {
+  const int t0 = tau * kRouteTokens;
+  const int nt = min(kRouteTokens, p.T - t0);
+  for (int i = threadIdx.x; i < kMaxE * 4; i += kThreads) c->mask[i] = 0u;
+  for (int e = threadIdx.x; e < p.E; e += kThreads) c->bias_s[e] = p.bias ? __ldg(p.bias + e) : 0.f;
+  GemmJob job;
+  job.a0 = &maps.xr;
+  job.a1 = nullptr;
+  job.b = &maps.wr;
+  job.a_row0 = t0;
+  job.a1_row0 = 0;
+  job.b_row0 = 0;
+  job.b_rows = p.E;
+  job.n_mma = ((p.E + 15) / 16) * 16;
+  job.b_off = kABoxBytes;
+  job.kb0 = 0;
+  job.nkb = p.d / kBK;
+  job.a_stream = true;
+  const bool ok = gemm_mainloop(p, job, smem, c, st);
+  if (ok) {
+    if (p.k <= 2) route_epilogue<2>(p, c, t0, nt);
+    else if (p.k <= 4) route_epilogue<4>(p, c, t0, nt);
+    else if (p.k <= 8) route_epilogue<8>(p, c, t0, nt);
+    else route_epilogue<16>(p, c, t0, nt);
+  }
+  tc_fence_before();
+  st.gemm_count++;
+}
+
 // ------------------------------------------------------------------ notifications
 // (persistent mode) Called by all threads after a task; bumps the dependency
 // counters the task feeds and pushes the tasks that became ready.
@@ -762,31 +951,59 @@ __device__ __forceinline__ bool drop_for_fault(const Params& p) {
   return atomicAdd(&p.sched->fault_seen, 1) == p.fault_drop;
 }
 
+// Push the n tasks id_of(i), i = 0..n-1.  Called by all 32 lanes of one warp.
+template <class F>
+__device__ __forceinline__ void push_gen_warp(const Params& p, const QueueRef& q, int n, F id_of) {
+  const int lane = threadIdx.x & 31;
+  int base = 0;
+  if (lane == 0) base = queue_reserve(q, n);
+  base = __shfl_sync(0xffffffffu, base, 0);
+  if (base + n > q.cap) {
+    if (lane == 0) set_status(p, MOE_E_DEVICE, 1);
+    return;
+  }
+  for (int i = lane; i < n; i += 32) st_release(q.ring + base + i, id_of(i) + 1);
+}
+
+// All gathers of an expert done: release its gate/up tiles, f-tile major and
+// sibling minor.
 __device__ void notify_gather_done(const Params& p, int g) {
   release_writes();
   if (threadIdx.x < 32) {
     int ready = 0;
+    const Group G = load_group(p, g);
     if (threadIdx.x == 0) {
-      const Group G = load_group(p, g);
-      const int old = atom_add_acq_rel(p.gather_done + g, 1);
-      ready = (old + 1 == gather_chunks(G.nrows));
+      const int old = atom_add_acq_rel(p.gather_done + G.sib0, 1);
+      ready = (old + 1 == G.gchunks);
     }
     ready = __shfl_sync(0xffffffffu, ready, 0);
-    if (ready) push_tasks_warp(p, gemm_queue(p), task_id(kTaskGateUp, g * p.n_ftiles), 1, p.n_ftiles);
+    if (ready) {
+      const int nf = p.n_ftiles, ns = G.nsib, s0 = G.sib0;
+      push_gen_warp(p, gemm_queue(p), ns * nf, [=](int i) {
+        return task_id(kTaskGateUp, (s0 + i % ns) * nf + i / ns);
+      });
+    }
   }
 }
 
+// All gate/up tiles of an expert done: release its down tiles, interleaved
+// the same way.
 __device__ void notify_gateup_done(const Params& p, int g) {
   release_writes();
   if (threadIdx.x < 32) {
     int ready = 0;
+    const Group G = load_group(p, g);
     if (threadIdx.x == 0 && !drop_for_fault(p)) {
-      const int old = atom_add_acq_rel(p.gu_done + g, 1);
-      ready = (old + 1 == p.n_ftiles);
+      const int old = atom_add_acq_rel(p.gu_done + G.sib0, 1);
+      ready = (old + 1 == G.nsib * p.n_ftiles);
     }
     ready = __shfl_sync(0xffffffffu, ready, 0);
-    const int n_down = p.n_dtiles * p.ks;
-    if (ready) push_tasks_warp(p, gemm_queue(p), task_id(kTaskDown, g * n_down), 1, n_down);
+    if (ready) {
+      const int nd = p.n_dtiles * p.ks, ns = G.nsib, s0 = G.sib0;
+      push_gen_warp(p, gemm_queue(p), ns * nd, [=](int i) {
+        return task_id(kTaskDown, (s0 + i % ns) * nd + i / ns);
+      });
+    }
   }
 }
 
@@ -816,8 +1033,8 @@ __device__ void notify_down_done(const Params& p, int g, Ctrl* c) {
     const int old = atom_add_acq_rel(p.comb_done + ct, len);
     if (old + len == comb_target(p, ct)) {
       const QueueRef q = mover_queue(p);
-      const int slot = atomicAdd(q.tail, 1);
-      if (slot < q.cap) st_release(q.ring + slot, task_id(kTaskCombine, ct));
+      const int slot = queue_reserve(q, 1);
+      if (slot < q.cap) st_release(q.ring + slot, task_id(kTaskCombine, ct) + 1);
       else set_status(p, MOE_E_DEVICE, 5);
     }
   }
