@@ -170,6 +170,22 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(inside)}
 
 
+def reduce_max(x: float, device: str) -> float:
+    """Max of a per-rank scalar over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank: int, ms_slowest: float, world: int) -> float:
+    """Whole-job tokens/s: every rank's batch over the slowest rank's time."""
+    return world * tokens_per_rank / (ms_slowest / 1e3)
+
+
 # ---------------------------------------------------------------- workload facts
 
 def algorithmic(w: gen.Workload, counts: np.ndarray):
@@ -255,12 +271,8 @@ def run_ours(args):
         raise RuntimeError(f"device status {rc} during the timed region")
     times = [a.elapsed_time(b) for a, b in ev]
     ms = float(np.mean(times))
-    ms_max = ms
-    if world > 1:
-        t = torch.tensor([ms], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
-    value = world * w.T / (ms_max / 1e3)
+    ms_max = reduce_max(ms, "cuda")
+    value = job_throughput(w.T, ms_max, world)
 
     # end to end through the host-buffer entry point
     e2e = None
@@ -277,12 +289,8 @@ def run_ours(args):
             t0 = time.perf_counter()
             layer.forward_host(w.T, x_host.data_ptr(), wr, wg, wu, wd, out_host.data_ptr())
             tot += time.perf_counter() - t0
-        e2e_s = tot / ke
-        if world > 1:
-            t = torch.tensor([e2e_s], device="cuda", dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_s = float(t.item())
-        e2e = {"value": world * w.T / e2e_s, "unit": UNIT,
+        e2e_s = reduce_max(tot / ke, "cuda")
+        e2e = {"value": job_throughput(w.T, e2e_s * 1e3, world), "unit": UNIT,
                "h2d_bytes_per_step": w.T * w.d * 2, "d2h_bytes_per_step": w.T * w.d * 2,
                "steps": ke, "ms_per_step": e2e_s * 1e3}
 

@@ -85,6 +85,12 @@ typedef struct moe_layer moe_layer_t;
                                   least this many tasks wait; -1 auto, 0 off  */
 #define MOE_OPT_TRACE 10       /* >0: record up to this many task records per
                                   forward (allocates; see moe_layer_get_trace) */
+#define MOE_OPT_RELEASE 11     /* when gate/up tiles become ready: 0 = all at
+                                  once after the last gather, f-tile major;
+                                  1 = per expert after its gathers (default) */
+#define MOE_OPT_PREFETCH 12    /* 1 (default): while a GEMM tile finishes, the
+                                  TMA producer starts loading the next tile
+                                  claimed ahead; 0: off                        */
 
 /* statistics keys for moe_layer_get_stat (values of the last forward;
  * moe_layer_status must have been called after it) */

@@ -18,10 +18,15 @@ constexpr int kBBoxRows = 32;       // token rows per activation box
 constexpr int kBBoxBytes = kBBoxRows * kBK * 2;  // 4 KB
 constexpr int kGatherRows = 32;     // permuted rows per gather task
 constexpr int kRouteTokens = 128;   // tokens per router tile (the MMA M)
+constexpr int kMaxRouteKs = 8;      // K splits of a router tile, at most
 constexpr int kMaxE = 256;
 constexpr int kMaxK = 16;
 constexpr int kTmemCols = 512;
 constexpr int kAcc1Col = 256;       // second accumulator's first TMEM column
+
+// release policies of the gate/up tiles
+constexpr int kReleaseAll = 0;
+constexpr int kReleaseExpert = 1;
 
 // task types (bits 28-31 of a task id)
 enum TaskType : int {
@@ -73,8 +78,9 @@ struct Sched {
   int err_info;
   int trace_n;
   int stat_ahead;
-  int n_gather;         // gather tasks pushed by the plan (mover slots after the router tiles)
-  int pad[12];
+  int n_gather;         // gather tasks pushed by the plan (mover slots after the router tasks)
+  int gathers_done;
+  int pad[11];
 };
 
 struct Params {
@@ -90,6 +96,10 @@ struct Params {
   int kb_down;       // k blocks (of 64) per down split
   int rt;            // tokens per router tile (kRouteTokens)
   int n_route;       // router tiles
+  int route_ks;      // K splits of a router tile
+  int n_route_tasks; // n_route * route_ks (implicit slots of the mover queue)
+  int release;       // kReleaseAll or kReleaseExpert
+  int prefetch;      // producer starts the next claimed GEMM tile's loads early
   int ct;            // tokens per combine tile
   int n_comb;        // combine tiles
   int n_shared_groups;
@@ -133,6 +143,8 @@ struct Params {
   int* ring_mover;   // [mover_cap] task id + 1, 0 = not yet pushed
   int* ring_gemm;    // [gemm_cap]  task id + 1, 0 = not yet pushed
   Sched* sched;
+  float* rpart;      // [n_route][route_ks][128][E padded to 16] partial router logits
+  int* rsplit_done;  // [n_route] router K splits finished
   unsigned long long* trace;  // [trace_cap][4] task trace records (or null)
   int trace_cap;
 };

@@ -46,6 +46,7 @@ __device__ __forceinline__ void cta_setup(const Params& p, const Maps& maps, cha
     mbar_init(&c->cbar[1], 1);
     fence_mbar_init();
     c->deadline = globaltimer() + p.timeout_ns;
+    c->next_task = -1;
   }
   if (with_tmem && warp == 1) {
     tmem_alloc(&c->tmem_base, kTmemCols);
@@ -70,6 +71,12 @@ __device__ __forceinline__ void cta_setup(const Params& p, const Maps& maps, cha
   st.role_mover = 0;
   st.gather_phase = 0;
   st.comb_phase = 0;
+  st.exit_reason = 0;
+  st.polls = 0;
+  st.plan_seen = false;
+  st.n_gather = st.mover_total = st.gemm_total = 0;
+  st.pf_task = -1;
+  st.pf_count = 0;
 }
 
 __device__ __forceinline__ void cta_teardown(Ctrl* c, bool with_tmem) {
@@ -90,7 +97,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   CtaState st;
   cta_setup(p, maps, smem, c, st, true);
   int executed = 0, gemm_tasks = 0, mover_tasks = 0, ahead = 0;
-  if (threadIdx.x == 0) c->next_task = -1;
   while (true) {
     if (threadIdx.x == 0) {
       c->t_claim = globaltimer();
@@ -104,44 +110,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (task < 0) break;
     ++executed;
     // claim ahead: an otherwise idle lane takes the next task now, so the
-    // claim's round trips overlap this task; only when the queue is deep, so
-    // that holding a task cannot starve another CTA near the end
-    if (threadIdx.x == 64 && p.ahead_depth > 0) {
+    // claim's round trips overlap this task (and the producer can start the
+    // next GEMM tile's loads early); only when the queue is deep, so that
+    // holding a task cannot starve another CTA, and never behind a router
+    // tile, which gates everything else
+    if (threadIdx.x == 64 && p.ahead_depth > 0 && task_type(task) != kTaskRoute) {
       const int r = claim_once(p, st, p.ahead_depth);
       if (r >= 0) {
-        c->next_task = r;
+        st_release_cta_shared(&c->next_task, r);
         ++ahead;
       }
     }
     const int type = task_type(task), pl = task_payload(task);
     if (type == kTaskRoute) {
-      route_task(p, maps, pl, smem, c, st);
-      release_writes();
-      if (threadIdx.x == 0) {
-        const int old = atom_add_acq_rel(&p.sched->route_done, 1);
-        c->flag = (old + 1 == p.n_route);
-      }
-      __syncthreads();
-      if (c->flag) {
-        fence_acq_rel_gpu();
-        plan_task(p, smem, c, true);
+      const int tile = pl / p.route_ks, split = pl - tile * p.route_ks;
+      if (route_task(p, maps, tile, split, smem, c, st)) {
+        release_writes();
+        if (threadIdx.x == 0) {
+          const int old = atom_add_acq_rel(&p.sched->route_done, 1);
+          c->flag = (old + 1 == p.n_route);
+        }
+        __syncthreads();
+        if (c->flag) {
+          fence_acq_rel_gpu();
+          plan_task(p, smem, c, true);
+        }
       }
     } else if (type == kTaskGather) {
       ++mover_tasks;
       const int g = pl >> 3, ch = pl & 7;
       gather_task(p, g, ch, smem, c, st);
-      notify_gather_done(p, g);
+      notify_gather_done(p, g, c);
     } else if (type == kTaskGateUp) {
       ++gemm_tasks;
-      const int g = pl / p.n_ftiles, ft = pl - g * p.n_ftiles;
-      gateup_task(p, maps, g, ft, smem, c, st);
+      const int g = pl / p.n_ftiles;
+      gateup_task(p, maps, task, smem, c, st);
       notify_gateup_done(p, g);
     } else if (type == kTaskDown) {
       ++gemm_tasks;
-      const int n_down = p.n_dtiles * p.ks;
-      const int g = pl / n_down, r = pl - g * n_down;
-      const int dt = r / p.ks, ks = r - dt * p.ks;
-      down_task(p, maps, g, dt, ks, smem, c, st);
+      const int g = pl / (p.n_dtiles * p.ks);
+      down_task(p, maps, task, smem, c, st);
       notify_down_done(p, g, c);
     } else if (type == kTaskCombine) {
       ++mover_tasks;
@@ -162,6 +170,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
+  if (threadIdx.x == 0 && p.trace) {  // exit record: reason and both queue words
+    const int i = atomicAdd(&p.sched->trace_n, 1);
+    if (i < p.trace_cap) {
+      unsigned long long* r = p.trace + (size_t)i * 4;
+      r[0] = ((unsigned long long)blockIdx.x << 32) | 0x7fffffffu;
+      r[1] = ((unsigned long long)st.polls << 8) | (unsigned long long)st.exit_reason;
+      r[2] = *reinterpret_cast<volatile unsigned long long*>(&p.sched->gemm_q);
+      r[3] = globaltimer();
+    }
+  }
   if (threadIdx.x == 0) {
     atomicAdd(&p.sched->tasks_done, executed);
     atomicAdd(&p.sched->stat_gemm, gemm_tasks);
@@ -179,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   Ctrl* c;
   CtaState st;
   cta_setup(p, maps, smem, c, st, true);
-  route_task(p, maps, blockIdx.x, smem, c, st);
+  route_task(p, maps, blockIdx.x / p.route_ks, blockIdx.x % p.route_ks, smem, c, st);
   cta_teardown(c, true);
 }
 
@@ -213,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   Ctrl* c;
   CtaState st;
   cta_setup(p, maps, smem, c, st, true);
-  gateup_task(p, maps, g, ft, smem, c, st);
+  gateup_task(p, maps, task_id(kTaskGateUp, blockIdx.x), smem, c, st);
   cta_teardown(c, true);
 }
 
@@ -226,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   Ctrl* c;
   CtaState st;
   cta_setup(p, maps, smem, c, st, true);
-  down_task(p, maps, g, r / p.ks, r % p.ks, smem, c, st);
+  down_task(p, maps, task_id(kTaskDown, blockIdx.x), smem, c, st);
   cta_teardown(c, true);
 }
 
@@ -329,6 +347,8 @@ struct moe_layer {
   int fault_drop = -1;
   int rt_opt = 0;
   int ahead_opt = -1;
+  int release = kReleaseExpert;
+  int prefetch = 1;
   int trace_cap = 0;
   unsigned long long* trace = nullptr;
   const float* bias = nullptr;
@@ -338,7 +358,7 @@ struct moe_layer {
   Bounds B{};
   // offsets into ws
   size_t o_idx, o_wgt, o_rank, o_tile, o_counts, o_offsets, o_perm, o_pos, o_xp, o_h, o_y,
-      o_groups, o_zero, o_gd, o_gu, o_cd, o_sched, o_zero_end, o_ring, o_ring_m, o_ring_g,
+      o_groups, o_rpart, o_rsd, o_zero, o_gd, o_gu, o_cd, o_sched, o_zero_end, o_ring, o_ring_m, o_ring_g,
       o_ring_end;
   // host staging for moe_layer_forward_host
   void* x_dev_stage = nullptr;
@@ -391,8 +411,10 @@ void layout(moe_layer* h, const Bounds& b) {
   h->o_h = take((rows + 64) * h->f * 2);
   h->o_y = take(b.y_elems * 4 + 4096);
   h->o_groups = take((size_t)b.max_groups * sizeof(Group));
+  h->o_rpart = take((size_t)std::max(h->num_sms, 1) * kRouteTokens * (((h->E + 15) / 16) * 16) * 4);
   h->o_zero = o;
   h->o_sched = take(sizeof(Sched));
+  h->o_rsd = take((size_t)b.n_route * 4);
   h->o_gd = take((size_t)b.max_groups * 4);
   h->o_gu = take((size_t)b.max_groups * 4);
   h->o_cd = take((size_t)b.n_comb * 4);
@@ -608,6 +630,13 @@ int moe_layer_set_option(moe_layer_t* h, int key, long long v) {
       }
       break;
     }
+    case MOE_OPT_RELEASE:
+      if (v != kReleaseAll && v != kReleaseExpert) return fail(MOE_E_INVAL, "release policy must be 0 or 1");
+      h->release = (int)v;
+      break;
+    case MOE_OPT_PREFETCH:
+      h->prefetch = v ? 1 : 0;
+      break;
     case MOE_OPT_ROUTE_TOKENS:
       if (v != 0 && v != kRouteTokens) return fail(MOE_E_INVAL, "router tiles are 128 tokens");
       h->rt_opt = (int)v;
@@ -652,6 +681,17 @@ int moe_layer_forward(moe_layer_t* h, int T, const void* x, const void* router_w
   p.kb_down = (h->f / kBK) / tl.ks;
   p.rt = tl.rt;
   p.n_route = cdiv(T, tl.rt);
+  {
+    // K splits of the router: spread few router tiles over the SMs (at least
+    // two k blocks per split, at most 16 splits)
+    const int nkb = h->d / kBK;
+    int ks = std::min(kMaxRouteKs, std::min(nkb / 2, std::max(h->num_sms, 1) / p.n_route));
+    if (p.n_route > 16) ks = 1;  // enough tiles to spread already
+    p.route_ks = std::max(1, ks);
+    p.n_route_tasks = p.n_route * p.route_ks;
+  }
+  p.release = h->release;
+  p.prefetch = h->prefetch;
   p.ct = tl.ct;
   p.n_comb = cdiv(T, tl.ct);
   p.n_shared_groups = h->S ? cdiv(T, tl.bn) : 0;
@@ -694,6 +734,8 @@ int moe_layer_forward(moe_layer_t* h, int T, const void* x, const void* router_w
   p.ring_mover = reinterpret_cast<int*>(w + h->o_ring_m);
   p.ring_gemm = reinterpret_cast<int*>(w + h->o_ring_g);
   p.sched = reinterpret_cast<Sched*>(w + h->o_sched);
+  p.rpart = reinterpret_cast<float*>(w + h->o_rpart);
+  p.rsplit_done = reinterpret_cast<int*>(w + h->o_rsd);
 
   Maps m;
   const int nt = h->E + h->S;
@@ -712,14 +754,14 @@ int moe_layer_forward(moe_layer_t* h, int T, const void* x, const void* router_w
   if (h->mode == MOE_MODE_PERSISTENT) {
     int grid = h->grid_override > 0 ? h->grid_override : h->num_sms;
     h->last_grid = grid;
-    p.ahead_depth = h->ahead_opt < 0 ? 2 * grid : h->ahead_opt;
+    p.ahead_depth = h->ahead_opt < 0 ? grid : h->ahead_opt;
     // fetch-and-add claims when more tasks wait than there are claimers
     p.fa_depth = (p.ahead_depth > 0 ? 2 : 1) * grid + 8;
     moe_persistent_kernel<<<grid, kThreads, tl.smem, s>>>(p, m);
     CK(cudaGetLastError());
   } else {
     h->last_grid = 0;
-    k_route<<<p.n_route, kThreads, tl.smem, s>>>(p, m);
+    k_route<<<p.n_route_tasks, kThreads, tl.smem, s>>>(p, m);
     CK(cudaGetLastError());
     k_plan<<<1, kThreads, tl.smem, s>>>(p, m);
     CK(cudaGetLastError());

@@ -41,6 +41,11 @@ struct CtaState {
   int role_mover;       // 1 if this CTA prefers mover work (after the plan)
   uint32_t gather_phase;  // parity of the gather barrier (thread 0)
   uint32_t comb_phase;    // parities of the two combine barriers (bits 0, 1; all threads)
+  int exit_reason;        // why claim_next gave up (trace only): 1 done, 2 abort, 3 deadline
+  unsigned polls;         // claim attempts of thread 0 that found nothing (trace only)
+  bool plan_seen;         // the plan's totals below are cached
+  int n_gather, mover_total, gemm_total;
+  int pf_task, pf_count;  // producer: task whose first k blocks are already loading
 };
 
 // ------------------------------------------------------------------ helpers
@@ -132,7 +137,7 @@ struct QueueRef {
 };
 
 __device__ __forceinline__ QueueRef mover_queue(const Params& p) {
-  return QueueRef{&p.sched->mover_q, p.ring_mover, p.n_route, p.mover_cap};
+  return QueueRef{&p.sched->mover_q, p.ring_mover, p.n_route_tasks, p.mover_cap};
 }
 
 __device__ __forceinline__ QueueRef gemm_queue(const Params& p) {
@@ -160,15 +165,13 @@ __device__ __forceinline__ int queue_reserve(const QueueRef& q, int n) {
 // overshoot the tail if more than fa_depth claims race with it; the overshot
 // ticket then waits for its slot to be pushed, or turns out void when the
 // queue's final size is known and lies below it.
-__device__ int try_claim(const Params& p, const QueueRef& q, const int* total_dyn_ptr,
+__device__ int try_claim(const Params& p, const QueueRef& q, unsigned long long v, int total_dyn,
                          uint64_t deadline, int min_depth, int fa_depth) {
-  unsigned long long v = ld_acquire_u64(q.word);
   while (true) {
     const int h = (int)(v & 0xffffffffu);
     const int avail = q.n_static + (int)(v >> 32);
     if (h >= avail) {
-      if (ld_acquire(&p.sched->plan_done) && h >= q.n_static + ld_relaxed(total_dyn_ptr))
-        return -2;
+      if (total_dyn >= 0 && h >= q.n_static + total_dyn) return -2;
       return -1;
     }
     if (avail - h < min_depth) return -1;
@@ -187,7 +190,7 @@ __device__ int try_claim(const Params& p, const QueueRef& q, const int* total_dy
     int e;
     while ((e = ld_acquire(q.ring + (slot - q.n_static))) == 0) {
       if (ld_relaxed(&p.sched->status) != 0) return -3;
-      if (ld_acquire(&p.sched->plan_done) && slot >= q.n_static + ld_relaxed(total_dyn_ptr))
+      if (total_dyn >= 0 && slot >= q.n_static + total_dyn)
         return -2;  // an overshot ticket beyond the final size: nothing to run
       if (globaltimer() > deadline) {
         set_status(p, MOE_E_TIMEOUT, 2);
@@ -200,27 +203,35 @@ __device__ int try_claim(const Params& p, const QueueRef& q, const int* total_dy
 
 // One scheduling decision: the preferred queue first, then the other one.
 // Returns a task id, -1 if nothing is claimable now, -2 if both queues are
-// finished, -3 to abort.
+// finished, -3 to abort.  The plan's totals are cached once seen, so a claim
+// costs one load of both queue words, one atomic and one ring-entry load.
 __device__ int claim_once(const Params& p, CtaState& st, int min_depth) {
   Sched* s = p.sched;
-  if (ld_relaxed(&s->status) != 0) return -3;
-  const bool plan_done = ld_acquire(&s->plan_done) != 0;
-  bool gathers_left = false;
-  if (plan_done) {
+  if (!st.plan_seen && ld_acquire(&s->plan_done) != 0) {
+    st.plan_seen = true;
     st.role_mover = (int)blockIdx.x < ld_relaxed(&s->n_movers);
-    const unsigned long long mw = *reinterpret_cast<volatile unsigned long long*>(&s->mover_q);
-    gathers_left = (int)(mw & 0xffffffffu) < p.n_route + ld_relaxed(&s->n_gather);
+    st.n_gather = ld_relaxed(&s->n_gather);
+    st.mover_total = ld_relaxed(&s->mover_total_dyn);
+    st.gemm_total = ld_relaxed(&s->gemm_total_dyn);
   }
+  const QueueRef mq = mover_queue(p), gq = gemm_queue(p);
+  const unsigned long long mw = ld_acquire_u64(mq.word);
+  const unsigned long long gw = ld_acquire_u64(gq.word);
+  bool gathers_left = false;
+  if (st.plan_seen) gathers_left = (int)(mw & 0xffffffffu) < p.n_route_tasks + st.n_gather;
   // Before the plan every CTA prefers router tiles, and afterwards every CTA
   // prefers gathers while any is unclaimed: both gate all the GEMM work.
   // Otherwise each CTA prefers its own role's queue and steals from the other.
-  const bool mover_first = !plan_done || gathers_left || st.role_mover;
+  const bool mover_first = !st.plan_seen || gathers_left || st.role_mover;
   int finished = 0;
-  for (int pass = 0; pass < 2; ++pass) {
+  // claiming ahead (min_depth > 1) looks at the first-choice queue only, so a
+  // held task can never jump the priority order
+  const int npass = min_depth > 1 ? 1 : 2;
+  for (int pass = 0; pass < npass; ++pass) {
     const bool use_mover = (pass == 0) == mover_first;
-    const QueueRef q = use_mover ? mover_queue(p) : gemm_queue(p);
-    int r = try_claim(p, q, use_mover ? &s->mover_total_dyn : &s->gemm_total_dyn, st.deadline,
-                      min_depth, p.fa_depth);
+    const QueueRef& q = use_mover ? mq : gq;
+    const int total = st.plan_seen ? (use_mover ? st.mover_total : st.gemm_total) : -1;
+    int r = try_claim(p, q, use_mover ? mw : gw, total, st.deadline, min_depth, p.fa_depth);
     if (r == -3) return -3;
     if (r == -2) {
       ++finished;
@@ -236,10 +247,12 @@ __device__ int claim_once(const Params& p, CtaState& st, int min_depth) {
         r = task_id(kTaskGateUp, (slot % nsg) * p.n_ftiles + slot / nsg);
       }
     }
-    if (pass == 1 && plan_done) atomicAdd(&s->stat_stolen, 1);
+    if (pass == 1 && st.plan_seen) atomicAdd(&s->stat_stolen, 1);
     return r;
   }
-  return finished == 2 ? -2 : -1;
+  if (finished == npass && npass == 2) return -2;
+  if (ld_relaxed(&s->status) != 0) return -3;
+  return -1;
 }
 
 // Decide this CTA's next task (thread 0), waiting with back-off until one is
@@ -249,9 +262,14 @@ __device__ int claim_next(const Params& p, CtaState& st) {
   while (true) {
     const int r = claim_once(p, st, 1);
     if (r >= 0) return r;
-    if (r == -2 || r == -3) return -1;
+    ++st.polls;
+    if (r == -2 || r == -3) {
+      st.exit_reason = r == -2 ? 1 : 2;
+      return -1;
+    }
     if (globaltimer() > st.deadline) {
       set_status(p, MOE_E_TIMEOUT, 3);
+      st.exit_reason = 3;
       return -1;
     }
     __nanosleep(backoff);
@@ -633,13 +651,41 @@ struct GemmJob {
   int b_off;              // byte offset of the B tile inside a stage (1024-aligned)
   int kb0, nkb;           // first k block and number of k blocks
   bool a_stream;          // A is streamed once (evict-first); else B is
+  int task;               // task id (-1: not a queue task)
 };
 
 // Returns false on a timeout (status already set).
-__device__ bool gemm_mainloop(const Params& p, const GemmJob& job, char* smem, Ctrl* c,
-                              CtaState& st) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+__device__ bool make_gemm_job(const Params& p, const Maps& maps, int task, GemmJob& job);
+
+// Producer: TMA loads of k blocks [kb_from, kb_to) of `job` into the stages
+// starting at pipeline index it0.  Returns the number of k blocks issued
+// (fewer on a timeout).
+__device__ int issue_loads(const Params& p, const GemmJob& job, char* smem, Ctrl* c,
+                           const CtaState& st, uint32_t it0, int kb_from, int kb_to,
+                           uint64_t pol_a, uint64_t pol_b) {
   const int nbox = ceil_div(job.b_rows, kBBoxRows);
+  const bool two = job.a1 != nullptr;
+  const uint32_t bytes = (two ? 2u : 1u) * kABoxBytes + (uint32_t)nbox * kBBoxBytes;
+  uint32_t it = it0;
+  int kb = kb_from;
+  for (; kb < kb_to; ++kb, ++it) {
+    const uint32_t s = it % p.stages, ph = (it / p.stages) & 1u;
+    if (!mbar_wait(&c->empty_bar[s], ph ^ 1u, st.deadline)) break;
+    char* stage = smem + (size_t)s * p.stage_bytes;
+    mbar_arrive_expect_tx(&c->full_bar[s], bytes);
+    const int kc = (job.kb0 + kb) * kBK;
+    tma_load_2d(stage, job.a0, &c->full_bar[s], kc, job.a_row0, pol_a);
+    if (two) tma_load_2d(stage + kABoxBytes, job.a1, &c->full_bar[s], kc, job.a1_row0, pol_a);
+    for (int bx = 0; bx < nbox; ++bx)
+      tma_load_2d(stage + job.b_off + bx * kBBoxBytes, job.b, &c->full_bar[s], kc,
+                  job.b_row0 + bx * kBBoxRows, pol_b);
+  }
+  return kb - kb_from;
+}
+
+__device__ bool gemm_mainloop(const Params& p, const Maps& maps, const GemmJob& job, char* smem,
+                              Ctrl* c, CtaState& st) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool two = job.a1 != nullptr;
   bool ok = true;
   if (warp == 0 && lane == 0) {
@@ -649,23 +695,32 @@ __device__ bool gemm_mainloop(const Params& p, const GemmJob& job, char* smem, C
     const uint64_t pol_last = policy_evict_last();
     const uint64_t pol_a = job.a_stream ? pol_first : pol_last;
     const uint64_t pol_b = job.a_stream ? pol_last : pol_first;
-    const uint32_t bytes = (two ? 2u : 1u) * kABoxBytes + (uint32_t)nbox * kBBoxBytes;
-    uint32_t it = st.pipe_it;
-    for (int kb = 0; kb < job.nkb; ++kb, ++it) {
-      const uint32_t s = it % p.stages, ph = (it / p.stages) & 1u;
-      if (!mbar_wait(&c->empty_bar[s], ph ^ 1u, st.deadline)) {
-        set_status(p, MOE_E_TIMEOUT, 10);
-        ok = false;
-        break;
+    const int kb_first = (job.task >= 0 && st.pf_task == job.task) ? st.pf_count : 0;
+    st.pf_task = -1;
+    ok = issue_loads(p, job, smem, c, st, st.pipe_it + kb_first, kb_first, job.nkb, pol_a, pol_b) ==
+         job.nkb - kb_first;
+    if (!ok) set_status(p, MOE_E_TIMEOUT, 10);
+    // Cross-task overlap: when this is a gate/up or down tile and the next
+    // task (claimed ahead) is one too, start its first stages now; they fill
+    // as this tile's last MMAs release the stages.
+    const int nxt = ld_acquire_cta_shared(&c->next_task);
+    if (ok && p.prefetch && job.task >= 0 && nxt >= 0) {
+      GemmJob nj;
+      if (make_gemm_job(p, maps, nxt, nj)) {
+        fence_acq_rel_gpu();
+        fence_proxy_async_global();
+        const int n = min(p.stages, nj.nkb);
+        const uint64_t pa = nj.a_stream ? pol_first : pol_last;
+        const uint64_t pb = nj.a_stream ? pol_last : pol_first;
+        const int done = issue_loads(p, nj, smem, c, st, st.pipe_it + job.nkb, 0, n, pa, pb);
+        if (done == n) {
+          st.pf_task = nxt;
+          st.pf_count = n;
+        } else {
+          set_status(p, MOE_E_TIMEOUT, 13);
+          ok = false;
+        }
       }
-      char* stage = smem + (size_t)s * p.stage_bytes;
-      mbar_arrive_expect_tx(&c->full_bar[s], bytes);
-      const int kc = (job.kb0 + kb) * kBK;
-      tma_load_2d(stage, job.a0, &c->full_bar[s], kc, job.a_row0, pol_a);
-      if (two) tma_load_2d(stage + kABoxBytes, job.a1, &c->full_bar[s], kc, job.a1_row0, pol_a);
-      for (int bx = 0; bx < nbox; ++bx)
-        tma_load_2d(stage + job.b_off + bx * kBBoxBytes, job.b, &c->full_bar[s], kc,
-                    job.b_row0 + bx * kBBoxRows, pol_b);
     }
   } else if (warp == 1 && lane == 0) {
     const uint32_t idesc = idesc_bf16(kBM, (uint32_t)job.n_mma);
@@ -708,27 +763,64 @@ __device__ bool gemm_mainloop(const Params& p, const GemmJob& job, char* smem, C
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.f + __expf(-z)); }
 
-__device__ void gateup_task(const Params& p, const Maps& maps, int g, int ft, char* smem,
-                            Ctrl* c, CtaState& st) {
+// The GEMM job of a gate/up or down task id (false for other task types or
+// an inconsistent group).
+__device__ bool make_gemm_job(const Params& p, const Maps& maps, int task, GemmJob& job) {
+  const int type = task_type(task), pl = task_payload(task);
+  if (type == kTaskGateUp) {
+    const int g = pl / p.n_ftiles, ft = pl - g * p.n_ftiles;
+    const Group G = load_group(p, g);
+    if (!group_ok(p, G) || ft < 0 || ft >= p.n_ftiles) return false;
+    job.a0 = &maps.wg;
+    job.a1 = &maps.wu;
+    job.b = G.e < p.E ? &maps.xp : &maps.x;
+    job.a_row0 = G.e * p.f + ft * kBM;
+    job.a1_row0 = job.a_row0;
+    job.b_row0 = G.src_row0;
+    job.b_rows = G.nrows;
+    job.n_mma = ((G.nrows + 15) / 16) * 16;
+    job.b_off = 2 * kABoxBytes;
+    job.kb0 = 0;
+    job.nkb = p.d / kBK;
+    job.a_stream = true;
+    job.task = task;
+    return true;
+  }
+  if (type == kTaskDown) {
+    const int n_down = p.n_dtiles * p.ks;
+    const int g = pl / n_down, r = pl - g * n_down;
+    const int dt = r / p.ks, ksplit = r - dt * p.ks;
+    const Group G = load_group(p, g);
+    if (!group_ok(p, G) || dt >= p.n_dtiles) return false;
+    job.a0 = &maps.wd;
+    job.a1 = &maps.wd;
+    job.b = &maps.h;
+    job.a_row0 = G.e * p.d + dt * 2 * kBM;
+    job.a1_row0 = job.a_row0 + kBM;
+    job.b_row0 = G.row0;
+    job.b_rows = G.nrows;
+    job.n_mma = ((G.nrows + 15) / 16) * 16;
+    job.b_off = 2 * kABoxBytes;
+    job.kb0 = ksplit * p.kb_down;
+    job.nkb = p.kb_down;
+    job.a_stream = true;
+    job.task = task;
+    return true;
+  }
+  return false;
+}
+
+__device__ void gateup_task(const Params& p, const Maps& maps, int task, char* smem, Ctrl* c,
+                            CtaState& st) {
+  const int pl = task_payload(task);
+  const int g = pl / p.n_ftiles, ft = pl - g * p.n_ftiles;
   const Group G = load_group(p, g);
-  if (!group_ok(p, G) || ft < 0 || ft >= p.n_ftiles) {
+  GemmJob job;
+  if (!make_gemm_job(p, maps, task, job)) {
     if (threadIdx.x == 0) set_status(p, MOE_E_DEVICE, 21);
     return;
   }
-  GemmJob job;
-  job.a0 = &maps.wg;
-  job.a1 = &maps.wu;
-  job.b = G.e < p.E ? &maps.xp : &maps.x;
-  job.a_row0 = G.e * p.f + ft * kBM;
-  job.a1_row0 = job.a_row0;
-  job.b_row0 = G.src_row0;
-  job.b_rows = G.nrows;
-  job.n_mma = ((G.nrows + 15) / 16) * 16;
-  job.b_off = 2 * kABoxBytes;
-  job.kb0 = 0;
-  job.nkb = p.d / kBK;
-  job.a_stream = true;
-  const bool ok = gemm_mainloop(p, job, smem, c, st);
+  const bool ok = gemm_mainloop(p, maps, job, smem, c, st);
   if (ok) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q = warp & 3, half = warp >> 2;
@@ -749,27 +841,19 @@ __device__ void gateup_task(const Params& p, const Maps& maps, int g, int ft, ch
   st.gemm_count++;
 }
 
-__device__ void down_task(const Params& p, const Maps& maps, int g, int dt, int ksplit,
-                          char* smem, Ctrl* c, CtaState& st) {
+__device__ void down_task(const Params& p, const Maps& maps, int task, char* smem, Ctrl* c,
+                          CtaState& st) {
+  const int n_down = p.n_dtiles * p.ks;
+  const int pl = task_payload(task);
+  const int g = pl / n_down, r = pl - g * n_down;
+  const int dt = r / p.ks, ksplit = r - dt * p.ks;
   const Group G = load_group(p, g);
-  if (!group_ok(p, G) || dt < 0 || dt >= p.n_dtiles || ksplit < 0 || ksplit >= p.ks) {
+  GemmJob job;
+  if (!make_gemm_job(p, maps, task, job)) {
     if (threadIdx.x == 0) set_status(p, MOE_E_DEVICE, 22);
     return;
   }
-  GemmJob job;
-  job.a0 = &maps.wd;
-  job.a1 = &maps.wd;
-  job.b = &maps.h;
-  job.a_row0 = G.e * p.d + dt * 2 * kBM;
-  job.a1_row0 = job.a_row0 + kBM;
-  job.b_row0 = G.row0;
-  job.b_rows = G.nrows;
-  job.n_mma = ((G.nrows + 15) / 16) * 16;
-  job.b_off = 2 * kABoxBytes;
-  job.kb0 = ksplit * p.kb_down;
-  job.nkb = p.kb_down;
-  job.a_stream = true;
-  const bool ok = gemm_mainloop(p, job, smem, c, st);
+  const bool ok = gemm_mainloop(p, maps, job, smem, c, st);
   if (ok) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q = warp & 3, half = warp >> 2;
@@ -837,10 +921,14 @@ __device__ __forceinline__ void topk_insert(float (&tv)[KL], int (&te)[KL], floa
   }
 }
 
-template <int KL>
-__device__ __forceinline__ void route_epilogue(const Params& p, Ctrl* c, int t0, int nt) {
+// Logits of token row m come from `src(ch, v)`, which fills v[0..15] with
+// columns ch*16 .. ch*16+15; it is called by warps 0-3 only, uniformly.
+template <int KL, class Src>
+__device__ __forceinline__ void route_epilogue(const Params& p, Ctrl* c, int tile, int nt,
+                                               Src src) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = p.E, k = p.k;
+  const int t0 = tile * kRouteTokens;
   float tv[KL];
   int te[KL];
 #pragma unroll
@@ -852,10 +940,9 @@ __device__ __forceinline__ void route_epilogue(const Params& p, Ctrl* c, int t0,
   const bool valid = warp < 4 && m < nt;
   float mx = -INFINITY, sum = 0.f;
   if (warp < 4) {
-    const uint32_t lane_addr = c->tmem_base + ((uint32_t)(warp * 32) << 16);
     for (int ch = 0; ch * 16 < E; ++ch) {
       float v[16];
-      tmem_ld16(lane_addr + ch * 16, v);
+      src(ch, v);
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const int e = ch * 16 + i;
@@ -907,15 +994,30 @@ __device__ __forceinline__ void route_epilogue(const Params& p, Ctrl* c, int t0,
   }
   for (int e = threadIdx.x; e < E; e += kThreads) {
     const uint32_t* mk = c->mask + e * 4;
-    p.tile_cnt[(size_t)(t0 / kRouteTokens) * E + e] =
-        __popc(mk[0]) + __popc(mk[1]) + __popc(mk[2]) + __popc(mk[3]);
+    p.tile_cnt[(size_t)tile * E + e] = __popc(mk[0]) + __popc(mk[1]) + __popc(mk[2]) + __popc(mk[3]);
   }
 }
 
-__device__ void route_task(const Params& p, const Maps& maps, int tau, char* smem, Ctrl* c,
-                           CtaState& st) {
-  const int t0 = tau * kRouteTokens;
+template <class Src>
+__device__ __forceinline__ void route_epilogue_k(const Params& p, Ctrl* c, int tile, int nt, Src src) {
+  if (p.k <= 2) route_epilogue<2>(p, c, tile, nt, src);
+  else if (p.k <= 4) route_epilogue<4>(p, c, tile, nt, src);
+  else if (p.k <= 8) route_epilogue<8>(p, c, tile, nt, src);
+  else route_epilogue<16>(p, c, tile, nt, src);
+}
+
+// One router task: tile `tile`, K split `split` of p.route_ks.  With a single
+// split the epilogue reads the logits from TMEM.  With several, each split
+// stores its fp32 partial logits; the split that finishes last sums all of
+// them in split order (fixed, so the result does not depend on timing) and
+// runs the epilogue.  Returns true when this call completed the tile.
+__device__ bool route_task(const Params& p, const Maps& maps, int tile, int split, char* smem,
+                           Ctrl* c, CtaState& st) {
+  const int t0 = tile * kRouteTokens;
   const int nt = min(kRouteTokens, p.T - t0);
+  const int ks = p.route_ks;
+  const int nkb = p.d / kBK;
+  const int epad = ((p.E + 15) / 16) * 16;
   for (int i = threadIdx.x; i < kMaxE * 4; i += kThreads) c->mask[i] = 0u;
   for (int e = threadIdx.x; e < p.E; e += kThreads) c->bias_s[e] = p.bias ? __ldg(p.bias + e) : 0.f;
   GemmJob job;
@@ -926,20 +1028,70 @@ __device__ void route_task(const Params& p, const Maps& maps, int tau, char* sme
   job.a1_row0 = 0;
   job.b_row0 = 0;
   job.b_rows = p.E;
-  job.n_mma = ((p.E + 15) / 16) * 16;
+  job.n_mma = epad;
   job.b_off = kABoxBytes;
-  job.kb0 = 0;
-  job.nkb = p.d / kBK;
+  job.kb0 = split * nkb / ks;
+  job.nkb = (split + 1) * nkb / ks - job.kb0;
   job.a_stream = true;
-  const bool ok = gemm_mainloop(p, job, smem, c, st);
+  job.task = -1;
+  const bool ok = gemm_mainloop(p, maps, job, smem, c, st);
+  bool tile_done = false;
   if (ok) {
-    if (p.k <= 2) route_epilogue<2>(p, c, t0, nt);
-    else if (p.k <= 4) route_epilogue<4>(p, c, t0, nt);
-    else if (p.k <= 8) route_epilogue<8>(p, c, t0, nt);
-    else route_epilogue<16>(p, c, t0, nt);
+    const int warp = threadIdx.x >> 5;
+    const uint32_t lane_addr = c->tmem_base + ((uint32_t)((warp & 3) * 32) << 16);
+    if (ks == 1) {
+      route_epilogue_k(p, c, tile, nt, [&](int ch, float* v) { tmem_ld16(lane_addr + ch * 16, v); });
+      tile_done = true;
+    } else {
+      // partial logits of this split: [tile][split][128][epad] fp32
+      if (warp < 4) {
+        const int m = warp * 32 + (threadIdx.x & 31);
+        float4* dst = reinterpret_cast<float4*>(
+            p.rpart + (((size_t)tile * ks + split) * kRouteTokens + m) * epad);
+        for (int ch = 0; ch * 16 < epad; ++ch) {
+          float v[16];
+          tmem_ld16(lane_addr + ch * 16, v);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            dst[ch * 4 + q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        }
+      }
+      tc_fence_before();
+      release_writes();
+      if (threadIdx.x == 0) c->flag = atom_add_acq_rel(p.rsplit_done + tile, 1) + 1 == ks;
+      __syncthreads();
+      if (c->flag) {
+        fence_acq_rel_gpu();
+        // sum the splits into shared memory [128][epad], all threads, split order
+        float* sum = reinterpret_cast<float*>(smem);
+        const float4* src = reinterpret_cast<const float4*>(p.rpart + (size_t)tile * ks * kRouteTokens * epad);
+        const int n4 = kRouteTokens * epad / 4;
+        for (int i = threadIdx.x; i < n4; i += kThreads) {
+          float4 v[kMaxRouteKs];
+#pragma unroll
+          for (int s2 = 0; s2 < kMaxRouteKs; ++s2)
+            if (s2 < ks) v[s2] = __ldcg(src + (size_t)s2 * n4 + i);
+          float4 a = v[0];
+#pragma unroll
+          for (int s2 = 1; s2 < kMaxRouteKs; ++s2)
+            if (s2 < ks) {
+              a.x += v[s2].x; a.y += v[s2].y; a.z += v[s2].z; a.w += v[s2].w;
+            }
+          reinterpret_cast<float4*>(sum)[i] = a;
+        }
+        __syncthreads();
+        const int m = (warp & 3) * 32 + (threadIdx.x & 31);
+        route_epilogue_k(p, c, tile, nt, [&](int ch, float* v) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] = sum[m * epad + ch * 16 + i];
+        });
+        tile_done = true;
+      }
+    }
   }
   tc_fence_before();
   st.gemm_count++;
+  return tile_done;
 }
 
 // ------------------------------------------------------------------ notifications
@@ -965,13 +1117,43 @@ __device__ __forceinline__ void push_gen_warp(const Params& p, const QueueRef& q
   for (int i = lane; i < n; i += 32) st_release(q.ring + base + i, id_of(i) + 1);
 }
 
-// All gathers of an expert done: release its gate/up tiles, f-tile major and
-// sibling minor.
-__device__ void notify_gather_done(const Params& p, int g) {
+// Gather finished.  Release policy (temporal scheduling):
+//  - kReleaseAll: when the last gather of the layer is done, every routed
+//    gate/up tile is pushed at once, f-tile major across all groups, so all
+//    experts finish their gate/up work together and the down tiles of every
+//    expert become ready in one wide burst;
+//  - kReleaseExpert: when the last gather of an expert is done, its tiles are
+//    pushed (f-tile major across its sibling groups).
+__device__ void notify_gather_done(const Params& p, int g, Ctrl* c) {
   release_writes();
+  const Group G = load_group(p, g);
+  if (p.release == kReleaseAll) {
+    if (threadIdx.x == 0) {
+      const int old = atom_add_acq_rel(&p.sched->gathers_done, 1);
+      c->flag = (old + 1 == ld_relaxed(&p.sched->n_gather));
+      if (c->flag) {
+        const int nr = ld_relaxed(&p.sched->n_groups) - p.n_shared_groups;
+        c->ival[0] = nr;
+        c->ival[1] = queue_reserve(gemm_queue(p), nr * p.n_ftiles);
+      }
+    }
+    __syncthreads();
+    if (c->flag) {
+      const int nr = c->ival[0], base = c->ival[1], nf = p.n_ftiles;
+      const QueueRef q = gemm_queue(p);
+      if (base + nr * nf > q.cap) {
+        if (threadIdx.x == 0) set_status(p, MOE_E_DEVICE, 7);
+        return;
+      }
+      for (int i = threadIdx.x; i < nr * nf; i += kThreads) {
+        const int gg = p.n_shared_groups + i % nr, ft = i / nr;
+        st_release(q.ring + base + i, task_id(kTaskGateUp, gg * nf + ft) + 1);
+      }
+    }
+    return;
+  }
   if (threadIdx.x < 32) {
     int ready = 0;
-    const Group G = load_group(p, g);
     if (threadIdx.x == 0) {
       const int old = atom_add_acq_rel(p.gather_done + G.sib0, 1);
       ready = (old + 1 == G.gchunks);

@@ -1,0 +1,123 @@
+"""The in-kernel scheduler on the GPU: every task runs exactly once, results do
+not depend on the grid, the CTA roles or the release policy (bit-identical to
+the one-kernel-per-stage ablation), a lost dependency notification ends in a
+clean timeout status with the context still usable, and the forward pass can
+be captured in a CUDA graph."""
+import numpy as np
+import pytest
+
+import _harness as hz
+import oracle
+from persistent_megakernel_sm_gb300 import MOE_E_TIMEOUT, MOE_OK
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def case():
+    w, inp = hz.custom_case(300, 256, 16, 4, 384, 1, 0.6)
+    dev = hz.upload(inp)
+    ref, _ = oracle.layer(inp["x"], inp["router_w"], inp["bias"], inp["w_gate"], inp["w_up"],
+                          inp["w_down"], k=w.k, S=w.S)
+    return w, inp, dev, ref
+
+
+def _run(w, dev, **opts):
+    layer = hz.make_layer(w, **opts)
+    out, routing = hz.run_layer(layer, w, dev)
+    return layer, out, routing
+
+
+def test_every_task_runs_exactly_once(case):
+    w, inp, dev, ref = case
+    layer, out, _ = _run(w, dev, trace=1 << 14)
+    hz.check_out(out, ref)
+    tr = layer.trace()
+    real = tr["task"] != 0x7FFFFFFF
+    tasks = tr["task"][real]
+    assert len(np.unique(tasks)) == len(tasks), "a task ran twice"
+    assert layer.stat("tasks") == len(tasks)
+    types = set((tasks >> 28).tolist())
+    assert types == {1, 2, 3, 4, 5}, types
+    # every CTA recorded its exit after its last task
+    exits = tr["cta"][~real]
+    assert len(exits) == layer.stat("grid") and len(np.unique(exits)) == len(exits)
+    # dependency order: per group, gate/up before down; a combine after all downs
+    t_end = tr["t_end"][real]
+    t_start = tr["t_start"][real]
+    ty = tasks >> 28
+    assert t_start[ty == 5].min() >= t_end[ty == 1].max()
+    layer.close()
+
+
+@pytest.mark.parametrize("opts", [
+    dict(grid_ctas=1),
+    dict(grid_ctas=3, mover_ctas=1),
+    dict(grid_ctas=37, mover_ctas=20),
+    dict(release=1),
+    dict(claim_ahead=0),
+    dict(claim_ahead=2),
+    dict(release=1, claim_ahead=1, grid_ctas=64),
+])
+def test_schedule_does_not_change_bits(case, opts):
+    w, inp, dev, ref = case
+    base_layer, base, _ = _run(w, dev, mode=1)
+    layer, out, routing = _run(w, dev, **opts)
+    hz.check_out(out, ref)
+    assert np.array_equal(out, base), f"result depends on the schedule {opts}"
+    layer.close()
+    base_layer.close()
+
+
+def test_dropped_notification_times_out_cleanly(case):
+    import torch
+    w, inp, dev, ref = case
+    layer = hz.make_layer(w, timeout_ns=50_000_000, fault_drop_task=3)
+    out = torch.empty((w.T, w.d), dtype=torch.bfloat16, device="cuda")
+    layer.set_router_bias(dev["bias"])
+    layer.forward(dev["x"], dev["router_w"], dev["w_gate"], dev["w_up"], dev["w_down"], out)
+    assert layer.status() == MOE_E_TIMEOUT
+    # the context is still usable and the next pass is correct
+    layer.set_option("fault_drop_task", -1)
+    got, _ = hz.run_layer(layer, w, dev)
+    hz.check_out(got, ref)
+    assert layer.status() == MOE_OK
+    layer.close()
+
+
+def test_cuda_graph_capture_and_replay(case):
+    import torch
+    w, inp, dev, ref = case
+    layer = hz.make_layer(w)
+    layer.set_router_bias(dev["bias"])
+    out = torch.empty((w.T, w.d), dtype=torch.bfloat16, device="cuda")
+    eager, _ = hz.run_layer(layer, w, dev)
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            layer.forward(dev["x"], dev["router_w"], dev["w_gate"], dev["w_up"], dev["w_down"], out)
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(3):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert layer.status() == MOE_OK
+        assert np.array_equal(hz.from_dev_bf16(out), eager)
+    layer.close()
+
+
+def test_forward_host_matches_device_forward(case):
+    import torch
+    w, inp, dev, ref = case
+    layer = hz.make_layer(w)
+    layer.set_router_bias(dev["bias"])
+    eager, _ = hz.run_layer(layer, w, dev)
+    x_host = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    out_host = torch.zeros((w.T, w.d), dtype=torch.bfloat16).pin_memory()
+    for _ in range(2):
+        layer.forward_host(w.T, x_host.data_ptr(), dev["router_w"], dev["w_gate"], dev["w_up"],
+                           dev["w_down"], out_host.data_ptr())
+        assert np.array_equal(out_host.view(torch.int16).numpy().view(np.uint16), eager)
+    layer.close()
