@@ -19,6 +19,7 @@ constexpr int kBBoxBytes = kBBoxRows * kBK * 2;  // 4 KB
 constexpr int kGatherRows = 32;     // permuted rows per gather task
 constexpr int kRouteTokens = 128;   // tokens per router tile (the MMA M)
 constexpr int kMaxRouteKs = 8;      // K splits of a router tile, at most
+constexpr int kShards = 8;          // shards of each task queue
 constexpr int kMaxE = 256;
 constexpr int kMaxK = 16;
 constexpr int kTmemCols = 512;
@@ -58,11 +59,11 @@ struct Group {
 };
 
 // Scheduler state.  Zeroed before every launch.
-// A queue word packs the queue's head (claims, low 32 bits) and tail
-// (dynamic pushes, high 32 bits) so one load sees both and one CAS claims.
+// A queue shard word packs the shard's claims (low 32 bits) and dynamic
+// pushes (high 32 bits), so one load sees both and one CAS claims.
 struct Sched {
-  unsigned long long mover_q;
-  unsigned long long gemm_q;
+  unsigned long long mover_q[kShards];
+  unsigned long long gemm_q[kShards];
   int status;
   int route_done;
   int plan_done;
@@ -107,7 +108,7 @@ struct Params {
   int y_f32;         // Y holds fp32 partial sums [ks][rows][d]; else bf16 [rows][d]
   int rows_y;        // rows of one Y partial (T*k + T*S)
   int max_groups;    // capacity of the group arrays
-  int mover_cap, gemm_cap;  // ring capacities
+  int mover_seg, gemm_seg;  // ring capacity of one shard
   int fault_drop;    // -1, or the index of the GEMM completion to drop
   int mover_override;
   int ahead_depth;   // claim the next task early when this many wait (0 = never)
@@ -140,8 +141,8 @@ struct Params {
   int* gather_done;  // [max_groups]
   int* gu_done;      // [max_groups]
   int* comb_done;    // [n_comb]
-  int* ring_mover;   // [mover_cap] task id + 1, 0 = not yet pushed
-  int* ring_gemm;    // [gemm_cap]  task id + 1, 0 = not yet pushed
+  int* ring_mover;   // [kShards][mover_seg] task id + 1, 0 = not yet pushed
+  int* ring_gemm;    // [kShards][gemm_seg]  task id + 1, 0 = not yet pushed
   Sched* sched;
   float* rpart;      // [n_route][route_ks][128][E padded to 16] partial router logits
   int* rsplit_done;  // [n_route] router K splits finished

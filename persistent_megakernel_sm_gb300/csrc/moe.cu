@@ -97,26 +97,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   CtaState st;
   cta_setup(p, maps, smem, c, st, true);
   int executed = 0, gemm_tasks = 0, mover_tasks = 0, ahead = 0;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   while (true) {
-    if (threadIdx.x == 0) {
-      c->t_claim = globaltimer();
+    if (warp == 0) {  // warp 0 takes the task held from the claim ahead, or claims one
+      if (lane == 0) c->t_claim = globaltimer();
       const int held = c->next_task;
-      c->next_task = -1;
-      c->task = held >= 0 ? held : claim_next(p, st);
-      c->t_start = globaltimer();
+      __syncwarp();
+      const int t = held >= 0 ? held : claim_next(p, st);
+      if (lane == 0) {
+        c->next_task = -1;
+        c->task = t;
+        c->t_start = globaltimer();
+      }
     }
     __syncthreads();
     const int task = c->task;
     if (task < 0) break;
     ++executed;
-    // claim ahead: an otherwise idle lane takes the next task now, so the
-    // claim's round trips overlap this task (and the producer can start the
-    // next GEMM tile's loads early); only when the queue is deep, so that
-    // holding a task cannot starve another CTA, and never behind a router
-    // tile, which gates everything else
-    if (threadIdx.x == 64 && p.ahead_depth > 0 && task_type(task) != kTaskRoute) {
+    // claim ahead: warp 2 (idle during a GEMM tile's main loop) takes the
+    // next task now, so the claim's round trips overlap this task (and the
+    // producer can start the next GEMM tile's loads early); only when the
+    // first-choice queue is deep, so holding a task cannot starve another CTA,
+    // and never behind a router tile, which gates everything else
+    if (warp == 2 && p.ahead_depth > 0 && task_type(task) != kTaskRoute) {
       const int r = claim_once(p, st, p.ahead_depth);
-      if (r >= 0) {
+      if (lane == 0 && r >= 0) {
         st_release_cta_shared(&c->next_task, r);
         ++ahead;
       }
@@ -176,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       unsigned long long* r = p.trace + (size_t)i * 4;
       r[0] = ((unsigned long long)blockIdx.x << 32) | 0x7fffffffu;
       r[1] = ((unsigned long long)st.polls << 8) | (unsigned long long)st.exit_reason;
-      r[2] = *reinterpret_cast<volatile unsigned long long*>(&p.sched->gemm_q);
+      r[2] = *reinterpret_cast<volatile unsigned long long*>(&p.sched->gemm_q[0]);
       r[3] = globaltimer();
     }
   }
@@ -420,8 +425,8 @@ void layout(moe_layer* h, const Bounds& b) {
   h->o_cd = take((size_t)b.n_comb * 4);
   h->o_zero_end = o;
   h->o_ring = o;
-  h->o_ring_m = take((size_t)b.mover_cap * 4);
-  h->o_ring_g = take((size_t)b.gemm_cap * 4);
+  h->o_ring_m = take((size_t)kShards * (b.mover_cap / kShards * 2 + 64) * 4);
+  h->o_ring_g = take((size_t)kShards * (b.gemm_cap / kShards * 2 + 64) * 4);
   h->o_ring_end = o;
   h->ws_bytes = o;
 }
@@ -701,8 +706,8 @@ int moe_layer_forward(moe_layer_t* h, int T, const void* x, const void* router_w
   const long long Tk = (long long)T * h->k;
   p.max_groups = p.n_shared_groups + cdiv(Tk, tl.bn) + (int)std::min<long long>(h->E, Tk);
   if (p.max_groups > h->B.max_groups) return fail(MOE_E_INVAL, "group capacity exceeded");
-  p.mover_cap = h->B.mover_cap;
-  p.gemm_cap = h->B.gemm_cap;
+  p.mover_seg = h->B.mover_cap / kShards * 2 + 64;
+  p.gemm_seg = h->B.gemm_cap / kShards * 2 + 64;
   p.fault_drop = h->fault_drop;
   p.mover_override = h->mover_override;
   p.trace = h->trace;

@@ -22,6 +22,7 @@ struct Ctrl {
   int next_task;
   int flag;
   int ival[8];
+  int qbase[kShards];
   int tok[kThreads];      // scratch: token ids / combine tiles per row
   int cnt[kMaxE];         // scratch: per-expert counts
   int aux[kMaxE];
@@ -123,25 +124,34 @@ __device__ __forceinline__ bool group_ok(const Params& p, const Group& G) {
 }
 
 // ------------------------------------------------------------------ queues
-// Two ticket queues.  Slots [0, n_static) of a queue are implicit tasks known
-// at launch (router tiles for the mover queue, shared-expert gate/up tiles
-// for the GEMM queue).  Later slots are reserved by pushers with an atomic add
-// on `tail` and filled with a release store of (task id + 1); ring entries
-// start at 0 (empty), so one zero memset resets the whole scheduler.
+// Two task queues (movers: router tiles, gathers, combines; GEMM workers:
+// gate/up and down tiles), each split into kShards shards.  A shard is one
+// 64-bit word -- claims so far (low 32 bits) and dynamic pushes (high 32 bits)
+// -- plus a ring segment.  Pushes spread their tasks round-robin over the
+// shards; a warp claims by loading every shard word of both queues at once
+// and CAS-ing the word of one shard with work, starting at its home shard
+// (blockIdx mod kShards) -- the per-SM local queues with stealing of
+// xxqk.cn/news/665650 section 4.4 (pitfall 3), each shared by a few CTAs.
+// A CAS never takes a slot that has not been pushed, so a claimer never
+// waits on work that does not exist yet; sharding keeps the number of CTAs
+// contending for one word small.  Tasks known at launch (router tiles,
+// shared-expert gate/up tiles) are implicit: static index s lives in shard
+// s mod kShards at local slot s / kShards.  Ring entries hold task id + 1
+// (0 = not yet written), so one zero memset resets a queue.
 
 struct QueueRef {
-  unsigned long long* word;  // head (low 32) | tail (high 32)
-  int* ring;
+  unsigned long long* word;  // [kShards]
+  int* ring;                 // [kShards][seg]
   int n_static;
-  int cap;
+  int seg;
 };
 
 __device__ __forceinline__ QueueRef mover_queue(const Params& p) {
-  return QueueRef{&p.sched->mover_q, p.ring_mover, p.n_route_tasks, p.mover_cap};
+  return QueueRef{p.sched->mover_q, p.ring_mover, p.n_route_tasks, p.mover_seg};
 }
 
 __device__ __forceinline__ QueueRef gemm_queue(const Params& p) {
-  return QueueRef{&p.sched->gemm_q, p.ring_gemm, p.n_static_gemm, p.gemm_cap};
+  return QueueRef{p.sched->gemm_q, p.ring_gemm, p.n_static_gemm, p.gemm_seg};
 }
 
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
@@ -150,125 +160,189 @@ __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long
   return v;
 }
 
-// Reserve n slots at the tail of a queue; returns the first dynamic index.
-__device__ __forceinline__ int queue_reserve(const QueueRef& q, int n) {
-  const unsigned long long old = atomicAdd(q.word, (unsigned long long)n << 32);
-  return (int)(old >> 32);
+__device__ __forceinline__ int shard_static(int n_static, int j) {
+  return n_static > j ? (n_static - j + kShards - 1) / kShards : 0;
 }
 
-// Try to claim one task: >= 0 task id, -1 nothing claimable now, -2 this
-// queue is finished, -3 abort.  `min_depth`: claim only if at least that many
-// tasks are waiting (used to claim ahead without starving other CTAs).
-// When at least `fa_depth` tasks wait, the claim is one fetch-and-add on the
-// head (all claimers are served at the L2's atomic rate); otherwise a CAS
-// that never takes a slot that has not been pushed.  A fetch-and-add can only
-// overshoot the tail if more than fa_depth claims race with it; the overshot
-// ticket then waits for its slot to be pushed, or turns out void when the
-// queue's final size is known and lies below it.
-__device__ int try_claim(const Params& p, const QueueRef& q, unsigned long long v, int total_dyn,
-                         uint64_t deadline, int min_depth, int fa_depth) {
-  while (true) {
-    const int h = (int)(v & 0xffffffffu);
-    const int avail = q.n_static + (int)(v >> 32);
-    if (h >= avail) {
-      if (total_dyn >= 0 && h >= q.n_static + total_dyn) return -2;
-      return -1;
+// Tasks i in [0, n) of a push go to shard (r0 + i) mod kShards, at local
+// index base_j + i / kShards; shard j receives push_count(n, r0, j) of them.
+__device__ __forceinline__ int push_count(int n, int r0, int j) {
+  const int off = (j - r0 + kShards) % kShards;
+  return off < n ? (n - off + kShards - 1) / kShards : 0;
+}
+
+__device__ __forceinline__ int push_start(int key) {
+  return (int)(((unsigned)key * 2654435761u) >> 16) & (kShards - 1);
+}
+
+// Push the n tasks id_of(i).  Called by all 32 lanes of one warp.
+template <class F>
+__device__ __forceinline__ void push_gen_warp(const Params& p, const QueueRef& q, int n, F id_of) {
+  const int lane = threadIdx.x & 31;
+  if (n <= 0) return;
+  const int r0 = push_start(id_of(0));
+  int base = 0;
+  if (lane < kShards) {
+    const int cnt = push_count(n, r0, lane);
+    if (cnt > 0) {
+      base = (int)(atomicAdd(q.word + lane, (unsigned long long)cnt << 32) >> 32);
+      if (base + cnt > q.seg) set_status(p, MOE_E_DEVICE, 1);
     }
-    if (avail - h < min_depth) return -1;
-    int slot = -1;
-    if (avail - h >= fa_depth) {
-      slot = (int)(atomicAdd(q.word, 1ull) & 0xffffffffu);
-    } else {
-      const unsigned long long seen = atomicCAS(q.word, v, v + 1);
-      if (seen != v) {
-        v = seen;  // lost the race: retry at once with the fresh word
-        continue;
-      }
-      slot = h;
-    }
-    if (slot < q.n_static) return -(1000 + slot);  // implicit task, decoded by the caller
-    int e;
-    while ((e = ld_acquire(q.ring + (slot - q.n_static))) == 0) {
-      if (ld_relaxed(&p.sched->status) != 0) return -3;
-      if (total_dyn >= 0 && slot >= q.n_static + total_dyn)
-        return -2;  // an overshot ticket beyond the final size: nothing to run
-      if (globaltimer() > deadline) {
-        set_status(p, MOE_E_TIMEOUT, 2);
-        return -3;
-      }
-    }
-    return e - 1;
+  }
+  for (int i0 = 0; i0 < n; i0 += 32) {  // whole-warp rounds: every lane shuffles
+    const int i = i0 + lane;
+    const int j = (r0 + i) & (kShards - 1);
+    const int bj = __shfl_sync(0xffffffffu, base, j);
+    if (i < n && bj + i / kShards < q.seg)
+      st_release(q.ring + j * q.seg + bj + i / kShards, id_of(i) + 1);
   }
 }
 
-// One scheduling decision: the preferred queue first, then the other one.
-// Returns a task id, -1 if nothing is claimable now, -2 if both queues are
-// finished, -3 to abort.  The plan's totals are cached once seen, so a claim
-// costs one load of both queue words, one atomic and one ring-entry load.
+// Push by the whole CTA (every thread calls it).
+template <class F>
+__device__ __forceinline__ void push_gen_block(const Params& p, const QueueRef& q, int n, F id_of,
+                                               Ctrl* c) {
+  if (n <= 0) return;
+  const int r0 = push_start(id_of(0));
+  if (threadIdx.x < kShards) {
+    const int cnt = push_count(n, r0, threadIdx.x);
+    int base = 0;
+    if (cnt > 0) {
+      base = (int)(atomicAdd(q.word + threadIdx.x, (unsigned long long)cnt << 32) >> 32);
+      if (base + cnt > q.seg) set_status(p, MOE_E_DEVICE, 1);
+    }
+    c->qbase[threadIdx.x] = base;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += kThreads) {
+    const int j = (r0 + i) & (kShards - 1);
+    const int slot = c->qbase[j] + i / kShards;
+    if (slot < q.seg) st_release(q.ring + j * q.seg + slot, id_of(i) + 1);
+  }
+}
+
+// Task of local slot `h` of shard `j`: implicit static task or ring entry
+// (waited for: the slot was reserved, its entry may still be in flight).
+// Returns the task id, or -3 on abort.  One lane only.
+__device__ int resolve_slot(const Params& p, const QueueRef& q, bool is_mover, int j, int h,
+                            uint64_t deadline) {
+  const int nst = shard_static(q.n_static, j);
+  if (h < nst) {
+    const int sidx = h * kShards + j;
+    if (is_mover) return task_id(kTaskRoute, sidx);
+    const int nsg = p.n_shared_groups;  // shared-expert gate/up tiles, f-tile major
+    return task_id(kTaskGateUp, (sidx % nsg) * p.n_ftiles + sidx / nsg);
+  }
+  const int* e = q.ring + j * q.seg + (h - nst);
+  int v;
+  while ((v = ld_acquire(e)) == 0) {
+    if (ld_relaxed(&p.sched->status) != 0) return -3;
+    if (globaltimer() > deadline) {
+      set_status(p, MOE_E_TIMEOUT, 2);
+      return -3;
+    }
+  }
+  return v - 1;
+}
+
+__device__ __forceinline__ int warp_sum_i(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// One scheduling decision, by a whole warp: the preferred queue first, then
+// the other one.  Returns a task id (the same on every lane), -1 if nothing
+// is claimable now, -2 if both queues are finished, -3 to abort, -4 to retry
+// at once (a CAS was lost).  `min_depth` > 1 claims ahead: only from the
+// first-choice queue and only when it holds at least that many tasks.
 __device__ int claim_once(const Params& p, CtaState& st, int min_depth) {
+  const int lane = threadIdx.x & 31;
+  const unsigned full = 0xffffffffu;
   Sched* s = p.sched;
-  if (!st.plan_seen && ld_acquire(&s->plan_done) != 0) {
-    st.plan_seen = true;
-    st.role_mover = (int)blockIdx.x < ld_relaxed(&s->n_movers);
-    st.n_gather = ld_relaxed(&s->n_gather);
-    st.mover_total = ld_relaxed(&s->mover_total_dyn);
-    st.gemm_total = ld_relaxed(&s->gemm_total_dyn);
+  if (!st.plan_seen) {  // lane 0 reads, every lane takes its values: decisions stay uniform
+    int seen = 0, nm = 0, ng = 0, mt = 0, gt = 0;
+    if (lane == 0 && ld_acquire(&s->plan_done) != 0) {
+      seen = 1;
+      nm = ld_relaxed(&s->n_movers);
+      ng = ld_relaxed(&s->n_gather);
+      mt = ld_relaxed(&s->mover_total_dyn);
+      gt = ld_relaxed(&s->gemm_total_dyn);
+    }
+    if (__shfl_sync(full, seen, 0)) {
+      st.plan_seen = true;
+      st.role_mover = (int)blockIdx.x < __shfl_sync(full, nm, 0);
+      st.n_gather = __shfl_sync(full, ng, 0);
+      st.mover_total = __shfl_sync(full, mt, 0);
+      st.gemm_total = __shfl_sync(full, gt, 0);
+    }
   }
   const QueueRef mq = mover_queue(p), gq = gemm_queue(p);
-  const unsigned long long mw = ld_acquire_u64(mq.word);
-  const unsigned long long gw = ld_acquire_u64(gq.word);
-  bool gathers_left = false;
-  if (st.plan_seen) gathers_left = (int)(mw & 0xffffffffu) < p.n_route_tasks + st.n_gather;
+  // lanes 0..7: the mover queue's shards, lanes 8..15: the GEMM queue's
+  const bool mine = lane < 2 * kShards;
+  const bool is_m = lane < kShards;
+  const int j = lane & (kShards - 1);
+  unsigned long long w = 0;
+  if (mine) w = ld_acquire_u64((is_m ? mq.word : gq.word) + j);
+  const int nst = mine ? shard_static(is_m ? mq.n_static : gq.n_static, j) : 0;
+  const int h = (int)(w & 0xffffffffu);
+  const int avail = nst + (int)(w >> 32);
+  const int claimed_m = warp_sum_i(mine && is_m ? h : 0);
+  const int claimed_g = warp_sum_i(mine && !is_m ? h : 0);
+  const int depth_m = warp_sum_i(mine && is_m ? max(avail - h, 0) : 0);
+  const int depth_g = warp_sum_i(mine && !is_m ? max(avail - h, 0) : 0);
+  const bool gathers_left = st.plan_seen && claimed_m < p.n_route_tasks + st.n_gather;
   // Before the plan every CTA prefers router tiles, and afterwards every CTA
   // prefers gathers while any is unclaimed: both gate all the GEMM work.
   // Otherwise each CTA prefers its own role's queue and steals from the other.
   const bool mover_first = !st.plan_seen || gathers_left || st.role_mover;
-  int finished = 0;
-  // claiming ahead (min_depth > 1) looks at the first-choice queue only, so a
-  // held task can never jump the priority order
   const int npass = min_depth > 1 ? 1 : 2;
+  const int home = (int)blockIdx.x & (kShards - 1);
   for (int pass = 0; pass < npass; ++pass) {
-    const bool use_mover = (pass == 0) == mover_first;
-    const QueueRef& q = use_mover ? mq : gq;
-    const int total = st.plan_seen ? (use_mover ? st.mover_total : st.gemm_total) : -1;
-    int r = try_claim(p, q, use_mover ? mw : gw, total, st.deadline, min_depth, p.fa_depth);
-    if (r == -3) return -3;
-    if (r == -2) {
-      ++finished;
-      continue;
+    const bool use_m = (pass == 0) == mover_first;
+    const int depth = use_m ? depth_m : depth_g;
+    if (depth < max(min_depth, 1)) continue;
+    const unsigned ball = __ballot_sync(full, mine && is_m == use_m && h < avail);
+    const unsigned sm = (use_m ? ball : (ball >> kShards)) & ((1u << kShards) - 1u);
+    if (!sm) continue;
+    // first shard with work at or after the home shard
+    const unsigned rot = ((sm >> home) | (sm << (kShards - home))) & ((1u << kShards) - 1u);
+    const int pick = (home + __ffs(rot) - 1) & (kShards - 1);
+    const int plane = (use_m ? 0 : kShards) + pick;
+    int r = -4;
+    if (lane == plane) {
+      const QueueRef& q = use_m ? mq : gq;
+      const unsigned long long seen = atomicCAS(q.word + pick, w, w + 1);
+      if (seen == w) r = resolve_slot(p, q, use_m, pick, h, st.deadline);
     }
-    if (r == -1) continue;
-    if (r <= -1000) {
-      const int slot = -(r + 1000);
-      if (use_mover) {
-        r = task_id(kTaskRoute, slot);
-      } else {  // shared-expert gate/up tiles, f-tile major across the groups
-        const int nsg = p.n_shared_groups;
-        r = task_id(kTaskGateUp, (slot % nsg) * p.n_ftiles + slot / nsg);
-      }
-    }
-    if (pass == 1 && st.plan_seen) atomicAdd(&s->stat_stolen, 1);
-    return r;
+    r = __shfl_sync(full, r, plane);
+    if (r >= 0 && pass == 1 && st.plan_seen && lane == 0) atomicAdd(&s->stat_stolen, 1);
+    return r;  // a task, -3, or -4 (lost the CAS: retry)
   }
-  if (finished == npass && npass == 2) return -2;
-  if (ld_relaxed(&s->status) != 0) return -3;
+  const bool fin_m = st.plan_seen && claimed_m >= mq.n_static + st.mover_total;
+  const bool fin_g = st.plan_seen && claimed_g >= gq.n_static + st.gemm_total;
+  if (npass == 2 && fin_m && fin_g) return -2;
+  const int bad = lane == 0 ? ld_relaxed(&s->status) : 0;
+  if (__shfl_sync(full, bad, 0) != 0) return -3;
   return -1;
 }
 
-// Decide this CTA's next task (thread 0), waiting with back-off until one is
-// claimable.  Returns a task id or -1 to exit.
+// Decide this CTA's next task (one whole warp), waiting with back-off until
+// one is claimable.  Returns a task id or -1 to exit (the same on every lane).
 __device__ int claim_next(const Params& p, CtaState& st) {
   uint32_t backoff = 32;
   while (true) {
     const int r = claim_once(p, st, 1);
     if (r >= 0) return r;
+    if (r == -4) continue;
     ++st.polls;
     if (r == -2 || r == -3) {
       st.exit_reason = r == -2 ? 1 : 2;
       return -1;
     }
-    if (globaltimer() > st.deadline) {
-      set_status(p, MOE_E_TIMEOUT, 3);
+    const int late = (threadIdx.x & 31) == 0 ? globaltimer() > st.deadline : 0;
+    if (__shfl_sync(0xffffffffu, late, 0)) {
+      if ((threadIdx.x & 31) == 0) set_status(p, MOE_E_TIMEOUT, 3);
       st.exit_reason = 3;
       return -1;
     }
@@ -384,9 +458,14 @@ __device__ void plan_task(const Params& p, char* scratch, Ctrl* c, bool push) {
       const int nrows = min(rows_per, n_r - m * rows_per);
       const int row0 = off_e + m * rows_per;
       p.groups[g] = Group{e_r, row0, nrows, row0, sib0, nmt, my_chunks, 0};
-      if (push) {
+      if (push) {  // gather i of the layer: shard i mod kShards, local slot i / kShards
         const int nc = gather_chunks(nrows);
-        for (int q = 0; q < nc; ++q) p.ring_mover[cb + q] = task_id(kTaskGather, g * 8 + q) + 1;
+        for (int q = 0; q < nc; ++q) {
+          const int i = cb + q;
+          if ((i / kShards) < p.mover_seg)
+            p.ring_mover[(i & (kShards - 1)) * p.mover_seg + i / kShards] =
+                task_id(kTaskGather, g * 8 + q) + 1;
+        }
         cb += nc;
       }
     }
@@ -449,8 +528,13 @@ __device__ void plan_task(const Params& p, char* scratch, Ctrl* c, bool push) {
   }
   if (push) {
     release_writes();
+    if (tid < kShards) {
+      const int cnt = push_count(n_gather, 0, tid);
+      if (cnt > p.mover_seg) set_status(p, MOE_E_DEVICE, 8);
+      if (cnt > 0) atomicAdd(p.sched->mover_q + tid, (unsigned long long)cnt << 32);
+    }
+    __syncthreads();
     if (tid == 0) {
-      queue_reserve(mover_queue(p), n_gather);
       __threadfence();
       st_release(&p.sched->plan_done, 1);
     }
@@ -1103,20 +1187,6 @@ __device__ __forceinline__ bool drop_for_fault(const Params& p) {
   return atomicAdd(&p.sched->fault_seen, 1) == p.fault_drop;
 }
 
-// Push the n tasks id_of(i), i = 0..n-1.  Called by all 32 lanes of one warp.
-template <class F>
-__device__ __forceinline__ void push_gen_warp(const Params& p, const QueueRef& q, int n, F id_of) {
-  const int lane = threadIdx.x & 31;
-  int base = 0;
-  if (lane == 0) base = queue_reserve(q, n);
-  base = __shfl_sync(0xffffffffu, base, 0);
-  if (base + n > q.cap) {
-    if (lane == 0) set_status(p, MOE_E_DEVICE, 1);
-    return;
-  }
-  for (int i = lane; i < n; i += 32) st_release(q.ring + base + i, id_of(i) + 1);
-}
-
 // Gather finished.  Release policy (temporal scheduling):
 //  - kReleaseAll: when the last gather of the layer is done, every routed
 //    gate/up tile is pushed at once, f-tile major across all groups, so all
@@ -1131,24 +1201,14 @@ __device__ void notify_gather_done(const Params& p, int g, Ctrl* c) {
     if (threadIdx.x == 0) {
       const int old = atom_add_acq_rel(&p.sched->gathers_done, 1);
       c->flag = (old + 1 == ld_relaxed(&p.sched->n_gather));
-      if (c->flag) {
-        const int nr = ld_relaxed(&p.sched->n_groups) - p.n_shared_groups;
-        c->ival[0] = nr;
-        c->ival[1] = queue_reserve(gemm_queue(p), nr * p.n_ftiles);
-      }
+      c->ival[0] = ld_relaxed(&p.sched->n_groups) - p.n_shared_groups;
     }
     __syncthreads();
     if (c->flag) {
-      const int nr = c->ival[0], base = c->ival[1], nf = p.n_ftiles;
-      const QueueRef q = gemm_queue(p);
-      if (base + nr * nf > q.cap) {
-        if (threadIdx.x == 0) set_status(p, MOE_E_DEVICE, 7);
-        return;
-      }
-      for (int i = threadIdx.x; i < nr * nf; i += kThreads) {
-        const int gg = p.n_shared_groups + i % nr, ft = i / nr;
-        st_release(q.ring + base + i, task_id(kTaskGateUp, gg * nf + ft) + 1);
-      }
+      const int nr = c->ival[0], nf = p.n_ftiles, ns0 = p.n_shared_groups;
+      push_gen_block(p, gemm_queue(p), nr * nf, [=](int i) {
+        return task_id(kTaskGateUp, (ns0 + i % nr) * nf + i / nr);
+      }, c);
     }
     return;
   }
@@ -1215,8 +1275,9 @@ __device__ void notify_down_done(const Params& p, int g, Ctrl* c) {
     const int old = atom_add_acq_rel(p.comb_done + ct, len);
     if (old + len == comb_target(p, ct)) {
       const QueueRef q = mover_queue(p);
-      const int slot = queue_reserve(q, 1);
-      if (slot < q.cap) st_release(q.ring + slot, task_id(kTaskCombine, ct) + 1);
+      const int j = push_start(ct);
+      const int slot = (int)(atomicAdd(q.word + j, 1ull << 32) >> 32);
+      if (slot < q.seg) st_release(q.ring + j * q.seg + slot, task_id(kTaskCombine, ct) + 1);
       else set_status(p, MOE_E_DEVICE, 5);
     }
   }
