@@ -44,7 +44,7 @@
  *   - a handle serves one stream at a time; calls on one handle are not
  *     thread-safe.
  * Limits: d % 128 == 0, f % 128 == 0, 1 <= k <= E <= 256, k <= 16, S <= 1,
- * 0 <= T <= T_max given to moe_layer_reserve.
+ * 0 <= T <= T_max given to moe_layer_reserve, T_max <= 32768.
  */
 #ifndef MOE_H_
 #define MOE_H_

@@ -36,6 +36,7 @@ enum TaskType : int {
   kTaskGateUp = 3,   // GEMM: H = bf16(silu(Xp Wg^T) * (Xp Wu^T)), one f tile
   kTaskDown = 4,     // GEMM: Y = H Wd^T, two d tiles, one K split
   kTaskCombine = 5,  // mover: out = bf16(sum_j w_j Y[pos] + Y_shared)
+  kTaskPlan = 6,     // (trace records only) the plan, run inline after the last router tile
 };
 
 __host__ __device__ constexpr int task_id(int type, int payload) { return (type << 28) | payload; }
@@ -55,7 +56,7 @@ struct Group {
   int sib0;      // first sibling group of the same expert
   int nsib;      // sibling groups of the expert
   int gchunks;   // gather tasks of all siblings
-  int pad;
+  int pad;       // the expert's first permuted row (offsets[e]); unused for the shared expert
 };
 
 // Scheduler state.  Zeroed before every launch.
@@ -128,6 +129,7 @@ struct Params {
   float* wgt;        // [T, k]
   int* rank;         // [T, k] rank of (t, j) among the tile's tokens of its expert
   int* tile_cnt;     // [n_route, E] per-tile counts, then exclusive prefix over tiles
+  uint32_t* rmask;   // [n_route, E, 4] router tile: 128-bit mask of the tokens choosing e
   int* counts;       // [E]
   int* offsets;      // [E + 1]
   int* perm;         // [T * k]

@@ -138,7 +138,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncthreads();
         if (c->flag) {
           fence_acq_rel_gpu();
+          const unsigned long long t_plan = globaltimer();
           plan_task(p, smem, c, true);
+          if (threadIdx.x == 0 && p.trace) {
+            const int i = atomicAdd(&p.sched->trace_n, 1);
+            if (i < p.trace_cap) {
+              unsigned long long* r = p.trace + (size_t)i * 4;
+              r[0] = ((unsigned long long)blockIdx.x << 32) | (unsigned)task_id(kTaskPlan, 0);
+              r[1] = t_plan;
+              r[2] = t_plan;
+              r[3] = globaltimer();
+            }
+            for (int ph = 0; ph < 7; ++ph) {  // phase boundaries of the plan
+              const int k2 = atomicAdd(&p.sched->trace_n, 1);
+              if (k2 < p.trace_cap) {
+                unsigned long long* r = p.trace + (size_t)k2 * 4;
+                r[0] = ((unsigned long long)blockIdx.x << 32) | (unsigned)task_id(kTaskPlan, 1 + ph);
+                r[1] = r[2] = r[3] = c->plan_t[ph];
+              }
+            }
+          }
         }
       }
     } else if (type == kTaskGather) {
@@ -363,7 +382,7 @@ struct moe_layer {
   Bounds B{};
   // offsets into ws
   size_t o_idx, o_wgt, o_rank, o_tile, o_counts, o_offsets, o_perm, o_pos, o_xp, o_h, o_y,
-      o_groups, o_rpart, o_rsd, o_zero, o_gd, o_gu, o_cd, o_sched, o_zero_end, o_ring, o_ring_m, o_ring_g,
+      o_groups, o_rpart, o_rsd, o_rmask, o_zero, o_gd, o_gu, o_cd, o_sched, o_zero_end, o_ring, o_ring_m, o_ring_g,
       o_ring_end;
   // host staging for moe_layer_forward_host
   void* x_dev_stage = nullptr;
@@ -408,6 +427,7 @@ void layout(moe_layer* h, const Bounds& b) {
   h->o_wgt = take(Tk * 4);
   h->o_rank = take(Tk * 4);
   h->o_tile = take((size_t)b.n_route * h->E * 4);
+  h->o_rmask = take((size_t)b.n_route * h->E * 16);
   h->o_counts = take(h->E * 4);
   h->o_offsets = take((h->E + 1) * 4);
   h->o_perm = take(Tk * 4);
@@ -533,7 +553,8 @@ long long moe_layer_workspace_bytes(const moe_layer_t* h, int T_max) {
 
 int moe_layer_reserve(moe_layer_t* h, int T_max, void* stream) {
   if (!h) return fail(MOE_E_INVAL, "null handle");
-  if (T_max < 1 || (long long)T_max * h->k >= (1ll << 26)) return fail(MOE_E_INVAL, "T_max out of range");
+  if (T_max < 1 || T_max > kMaxE * kRouteTokens)
+    return fail(MOE_E_INVAL, "T_max out of range (1..32768)");
   CK(cudaGetDevice(&h->device));
   CK(cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device));
   int cc_major = 0, cc_minor = 0;
@@ -691,7 +712,6 @@ int moe_layer_forward(moe_layer_t* h, int T, const void* x, const void* router_w
     // two k blocks per split, at most 16 splits)
     const int nkb = h->d / kBK;
     int ks = std::min(kMaxRouteKs, std::min(nkb / 2, std::max(h->num_sms, 1) / p.n_route));
-    if (p.n_route > 16) ks = 1;  // enough tiles to spread already
     p.route_ks = std::max(1, ks);
     p.n_route_tasks = p.n_route * p.route_ks;
   }
@@ -725,6 +745,7 @@ int moe_layer_forward(moe_layer_t* h, int T, const void* x, const void* router_w
   p.wgt = reinterpret_cast<float*>(w + h->o_wgt);
   p.rank = reinterpret_cast<int*>(w + h->o_rank);
   p.tile_cnt = reinterpret_cast<int*>(w + h->o_tile);
+  p.rmask = reinterpret_cast<uint32_t*>(w + h->o_rmask);
   p.counts = reinterpret_cast<int*>(w + h->o_counts);
   p.offsets = reinterpret_cast<int*>(w + h->o_offsets);
   p.perm = reinterpret_cast<int*>(w + h->o_perm);

@@ -23,6 +23,7 @@ struct Ctrl {
   int flag;
   int ival[8];
   int qbase[kShards];
+  unsigned long long plan_t[8];  // plan phase timestamps (trace only)
   int tok[kThreads];      // scratch: token ids / combine tiles per row
   int cnt[kMaxE];         // scratch: per-expert counts
   int aux[kMaxE];
@@ -393,13 +394,22 @@ __device__ void plan_task(const Params& p, char* scratch, Ctrl* c, bool push) {
   int* order = c->aux;   // experts by decreasing count
   int* offs = c->aux2;   // offsets per expert
 
+  if (threadIdx.x == 0) c->plan_t[0] = globaltimer();
   // per expert: exclusive prefix of the router tiles' counts (the tile bases)
   // and the total; in shared memory when the [tiles, E] table fits
   const int ntile = p.n_route;
   const bool in_smem = (size_t)ntile * E * 4 <= (size_t)p.stages * p.stage_bytes;
   int* tb = in_smem ? reinterpret_cast<int*>(scratch) : p.tile_cnt;
-  if (in_smem) {
-    for (int i = tid; i < ntile * E; i += kThreads) tb[i] = __ldcg(p.tile_cnt + i);
+  if (in_smem) {  // E is a multiple of 4 or the table is small: int4 where aligned
+    const int n = ntile * E;
+    if ((n & 3) == 0) {
+      const int4* src = reinterpret_cast<const int4*>(p.tile_cnt);
+      int4* dst = reinterpret_cast<int4*>(tb);
+#pragma unroll 8
+      for (int i = tid; i < n / 4; i += kThreads) dst[i] = __ldcg(src + i);
+    } else {
+      for (int i = tid; i < n; i += kThreads) tb[i] = __ldcg(p.tile_cnt + i);
+    }
     __syncthreads();
   }
   if (tid < E) {
@@ -413,7 +423,13 @@ __device__ void plan_task(const Params& p, char* scratch, Ctrl* c, bool push) {
     cnt[tid] = run;
     p.counts[tid] = run;
   }
+  if (in_smem) {  // the gathers read the tile bases from global memory
+    __syncthreads();
+    const int n = ntile * E;
+    for (int i = tid; i < n; i += kThreads) p.tile_cnt[i] = tb[i];
+  }
   __syncthreads();
+  if (threadIdx.x == 0) c->plan_t[1] = globaltimer();
   int total = 0;
   const int off = block_exclusive_scan(tid < E ? cnt[tid] : 0, &total, c);
   if (tid < E) {
@@ -421,6 +437,7 @@ __device__ void plan_task(const Params& p, char* scratch, Ctrl* c, bool push) {
     offs[tid] = off;
   }
   if (tid == 0) p.offsets[E] = total;
+  if (threadIdx.x == 0) c->plan_t[2] = globaltimer();
   // experts ordered by (count desc, expert asc)
   if (tid < E) {
     const int me = cnt[tid];
@@ -432,6 +449,7 @@ __device__ void plan_task(const Params& p, char* scratch, Ctrl* c, bool push) {
     order[r] = tid;
   }
   __syncthreads();
+  if (threadIdx.x == 0) c->plan_t[3] = globaltimer();
   // groups: order slot r -> expert order[r]
   int e_r = tid < E ? order[tid] : 0;
   int n_r = tid < E ? cnt[e_r] : 0;
@@ -457,7 +475,7 @@ __device__ void plan_task(const Params& p, char* scratch, Ctrl* c, bool push) {
       const int g = sib0 + m;
       const int nrows = min(rows_per, n_r - m * rows_per);
       const int row0 = off_e + m * rows_per;
-      p.groups[g] = Group{e_r, row0, nrows, row0, sib0, nmt, my_chunks, 0};
+      p.groups[g] = Group{e_r, row0, nrows, row0, sib0, nmt, my_chunks, off_e};
       if (push) {  // gather i of the layer: shard i mod kShards, local slot i / kShards
         const int nc = gather_chunks(nrows);
         for (int q = 0; q < nc; ++q) {
@@ -471,31 +489,9 @@ __device__ void plan_task(const Params& p, char* scratch, Ctrl* c, bool push) {
     }
   }
   __syncthreads();
-  // the canonical permutation: row = offset of e + base of (tile, e) + rank
-  {
-    const int n = p.T * k;
-    constexpr int U = 4;
-    for (int b = tid; b < n; b += kThreads * U) {
-      int e[U], r[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int ent = b + u * kThreads;
-        e[u] = ent < n ? __ldcg(p.idx + ent) : 0;
-        r[u] = ent < n ? __ldcg(p.rank + ent) : 0;
-      }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int ent = b + u * kThreads;
-        if (ent < n) {
-          const int t = ent / k;
-          const int* q = tb + (size_t)(t / p.rt) * E + e[u];
-          const int row = offs[e[u]] + (in_smem ? *q : __ldcg(q)) + r[u];
-          p.perm[row] = t;
-          p.pos[ent] = row;
-        }
-      }
-    }
-  }
+  if (threadIdx.x == 0) c->plan_t[4] = globaltimer();
+  if (threadIdx.x == 0) c->plan_t[4] = globaltimer();
+  if (threadIdx.x == 0) c->plan_t[5] = globaltimer();
   // cost model (spatial split): CTA-seconds of mover work against GEMM work
   if (tid == 0) {
     const int n_groups = p.n_shared_groups + n_routed;
@@ -510,22 +506,23 @@ __device__ void plan_task(const Params& p, char* scratch, Ctrl* c, bool push) {
     if (p.mover_override > 0) {
       movers = min(p.mover_override, max(N - 1, 1));
     } else {
-      const double ybytes = p.y_f32 ? 4.0 * p.ks : 2.0;
-      const double Tk = (double)p.T * k;
-      const double b_move = Tk * p.d * 2.0 * 2.0 +                      // gather: read + write
-                            ((double)p.T * (k + p.S)) * p.d * ybytes +  // combine reads
-                            (double)p.T * p.d * 2.0;                    // combine writes
+      const float ybytes = p.y_f32 ? 4.f * p.ks : 2.f;
+      const float Tk = (float)p.T * k;
+      const float b_move = Tk * p.d * 2.f * 2.f +                     // gather: read + write
+                           ((float)p.T * (k + p.S)) * p.d * ybytes +  // combine reads
+                           (float)p.T * p.d * 2.f;                    // combine writes
       int touched = p.S;
       for (int e = 0; e < E; ++e) touched += cnt[e] > 0;
-      const double flops = 6.0 * (Tk + (double)p.T * p.S) * p.d * p.f;
-      const double wbytes = (double)touched * 3.0 * p.f * p.d * 2.0;
-      const double a = b_move / p.beta_move;                              // CTA-seconds
-      const double b = fmax(flops / p.phi_gemm, (double)N * wbytes / p.hbm_bw);
-      movers = (int)lrint((double)N * a / (a + b));
+      const float flops = 6.f * (Tk + (float)p.T * p.S) * p.d * p.f;
+      const float wbytes = (float)touched * 3.f * p.f * p.d * 2.f;
+      const float a = b_move / p.beta_move;                            // CTA-seconds
+      const float b = fmaxf(flops / p.phi_gemm, (float)N * wbytes / p.hbm_bw);
+      movers = __float2int_rn((float)N * a / (a + b));
       movers = max(1, min(movers, max(N - 1, 1)));
     }
     s->n_movers = movers;
   }
+  if (threadIdx.x == 0) c->plan_t[6] = globaltimer();
   if (push) {
     release_writes();
     if (tid < kShards) {
@@ -557,7 +554,43 @@ __device__ void gather_task(const Params& p, int g, int chunk, char* smem, Ctrl*
   }
   const int r0 = G.row0 + chunk * kGatherRows;
   const int nr = min(kGatherRows, G.nrows - chunk * kGatherRows);
-  if (threadIdx.x < nr) c->tok[threadIdx.x] = __ldcg(p.perm + r0 + threadIdx.x);
+  // Permuted row r of expert e is the (r - off_e)-th token of e in router-tile
+  // order: the tile tau with base[tau][e] <= r - off_e < base[tau+1][e], and
+  // inside it the token of the (r - off_e - base[tau][e])-th set bit of the
+  // tile's mask of e.  This writes perm[r] and pos[t, j] for the chunk's rows.
+  int* col = c->aux;  // base[tau][e] for all router tiles tau
+  for (int tau = threadIdx.x; tau < p.n_route; tau += kThreads)
+    col[tau] = __ldcg(p.tile_cnt + (size_t)tau * p.E + G.e);
+  __syncthreads();
+  if (threadIdx.x < nr) {
+    const int r = r0 + threadIdx.x;
+    const int local = r - G.pad;
+    int lo = 0, hi = p.n_route - 1;  // last tile whose base <= local
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (col[mid] <= local) lo = mid;
+      else hi = mid - 1;
+    }
+    int rank = local - col[lo];
+    const uint4 mk = __ldcg(reinterpret_cast<const uint4*>(p.rmask) + (size_t)lo * p.E + G.e);
+    const uint32_t words[4] = {mk.x, mk.y, mk.z, mk.w};
+    int bit = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int pc = __popc(words[q]);
+      if (rank >= 0 && rank < pc) {
+        uint32_t wv = words[q];
+        for (int z = 0; z < rank; ++z) wv &= wv - 1u;  // drop the lowest set bits
+        bit = q * 32 + __ffs(wv) - 1;
+      }
+      rank -= pc;
+    }
+    const int t = lo * kRouteTokens + bit;
+    c->tok[threadIdx.x] = t;
+    p.perm[r] = t;
+    for (int j = 0; j < p.k; ++j)
+      if (__ldcg(p.idx + (size_t)t * p.k + j) == G.e) p.pos[(size_t)t * p.k + j] = r;
+  }
   __syncthreads();
   if (threadIdx.x == 0) {
     const uint32_t row_bytes = (uint32_t)p.d * 2;
@@ -734,7 +767,7 @@ struct GemmJob {
   int n_mma;              // MMA N (multiple of 16, <= 256)
   int b_off;              // byte offset of the B tile inside a stage (1024-aligned)
   int kb0, nkb;           // first k block and number of k blocks
-  bool a_stream;          // A is streamed once (evict-first); else B is
+  bool a_stream;          // A is read by this task only (L2 evict-first); else kept (evict-last)
   int task;               // task id (-1: not a queue task)
 };
 
@@ -777,8 +810,10 @@ __device__ bool gemm_mainloop(const Params& p, const Maps& maps, const GemmJob& 
     fence_proxy_async_shared();
     const uint64_t pol_first = policy_evict_first();
     const uint64_t pol_last = policy_evict_last();
+    // A (weights) streams through L2 unless a sibling tile re-reads it soon;
+    // B (token rows) is re-read by the expert's other tiles: keep it
     const uint64_t pol_a = job.a_stream ? pol_first : pol_last;
-    const uint64_t pol_b = job.a_stream ? pol_last : pol_first;
+    const uint64_t pol_b = pol_last;
     const int kb_first = (job.task >= 0 && st.pf_task == job.task) ? st.pf_count : 0;
     st.pf_task = -1;
     ok = issue_loads(p, job, smem, c, st, st.pipe_it + kb_first, kb_first, job.nkb, pol_a, pol_b) ==
@@ -795,7 +830,7 @@ __device__ bool gemm_mainloop(const Params& p, const Maps& maps, const GemmJob& 
         fence_proxy_async_global();
         const int n = min(p.stages, nj.nkb);
         const uint64_t pa = nj.a_stream ? pol_first : pol_last;
-        const uint64_t pb = nj.a_stream ? pol_last : pol_first;
+        const uint64_t pb = pol_last;
         const int done = issue_loads(p, nj, smem, c, st, st.pipe_it + job.nkb, 0, n, pa, pb);
         if (done == n) {
           st.pf_task = nxt;
@@ -866,7 +901,7 @@ __device__ bool make_gemm_job(const Params& p, const Maps& maps, int task, GemmJ
     job.b_off = 2 * kABoxBytes;
     job.kb0 = 0;
     job.nkb = p.d / kBK;
-    job.a_stream = true;
+    job.a_stream = G.nsib == 1;
     job.task = task;
     return true;
   }
@@ -887,7 +922,7 @@ __device__ bool make_gemm_job(const Params& p, const Maps& maps, int task, GemmJ
     job.b_off = 2 * kABoxBytes;
     job.kb0 = ksplit * p.kb_down;
     job.nkb = p.kb_down;
-    job.a_stream = true;
+    job.a_stream = G.nsib == 1;
     job.task = task;
     return true;
   }
@@ -1079,6 +1114,7 @@ __device__ __forceinline__ void route_epilogue(const Params& p, Ctrl* c, int til
   for (int e = threadIdx.x; e < E; e += kThreads) {
     const uint32_t* mk = c->mask + e * 4;
     p.tile_cnt[(size_t)tile * E + e] = __popc(mk[0]) + __popc(mk[1]) + __popc(mk[2]) + __popc(mk[3]);
+    reinterpret_cast<uint4*>(p.rmask)[(size_t)tile * E + e] = make_uint4(mk[0], mk[1], mk[2], mk[3]);
   }
 }
 
@@ -1116,7 +1152,7 @@ __device__ bool route_task(const Params& p, const Maps& maps, int tile, int spli
   job.b_off = kABoxBytes;
   job.kb0 = split * nkb / ks;
   job.nkb = (split + 1) * nkb / ks - job.kb0;
-  job.a_stream = true;
+  job.a_stream = true;  // x rows: read by this tile only; Wr (B) is shared by all tiles
   job.task = -1;
   const bool ok = gemm_mainloop(p, maps, job, smem, c, st);
   bool tile_done = false;
