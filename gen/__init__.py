@@ -18,6 +18,8 @@ skew      4096   4096   64   6   1408   0  fitted so counts follow Zipf(1.2)
 prefill   8192   7168   256  8   2048   1  b_e ~ N(0, 0.3^2)
 ========  =====  =====  ===  ==  =====  =  ==================================
 
+(``decode_small``: decode with f = 2048, a small case for profiler captures.)
+
 Distributions: x ~ N(0, 1); router_w ~ N(0, 1/d); w_gate, w_up ~ N(0, 1/d);
 w_down ~ N(0, 1/f) ("N(0, 1/fan_in)" read as a variance).  Every workload uses
 seed 0.  Layouts: x [T, d], router_w [E, d], w_gate / w_up [E+S, f, d],
@@ -88,6 +90,9 @@ WORKLOADS = {
     "fine": Workload("fine", 512, 2048, 128, 8, 768, 0, ("normal", 0.5)),
     "skew": Workload("skew", 4096, 4096, 64, 6, 1408, 0, ("zipf", 1.2)),
     "prefill": Workload("prefill", 8192, 7168, 256, 8, 2048, 1, ("normal", 0.3)),
+    # decode's shape with a narrower expert (f = 2048): 403 MB of weights, above
+    # the L2 size, for profiling captures that must stay small
+    "decode_small": Workload("decode_small", 256, 4096, 8, 2, 2048, 0, ()),
 }
 
 
