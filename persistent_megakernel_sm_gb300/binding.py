@@ -36,6 +36,7 @@ _SIGNATURES = {
     "moe_layer_set_router_bias": ([_vp, _vp], _i32),
     "moe_layer_forward": ([_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp], _i32),
     "moe_layer_forward_host": ([_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp], _i32),
+    "moe_layer_forward_static": ([_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp], _i32),
     "moe_layer_get_routing": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp], _i32),
     "moe_layer_status": ([_vp, _vp], _i32),
     "moe_layer_set_option": ([_vp, _i32, _i64], _i32),
@@ -125,6 +126,14 @@ class MoELayer:
         _err(lib.moe_layer_forward(self.h, T, x.data_ptr(), router_w.data_ptr(),
                                    w_gate.data_ptr(), w_up.data_ptr(), w_down.data_ptr(),
                                    out.data_ptr(), _stream_ptr(stream)))
+        return out
+
+    def forward_static(self, x, router_w, w_gate, w_up, w_down, out, stream=None):
+        """moe_layer_forward_static: the same pass on the library's fixed scratch."""
+        T = x.shape[0]
+        _err(lib.moe_layer_forward_static(self.h, T, x.data_ptr(), router_w.data_ptr(),
+                                          w_gate.data_ptr(), w_up.data_ptr(), w_down.data_ptr(),
+                                          out.data_ptr(), _stream_ptr(stream)))
         return out
 
     def forward_host(self, T, x_host_ptr, router_w, w_gate, w_up, w_down, out_host_ptr,

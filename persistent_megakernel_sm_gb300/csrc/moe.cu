@@ -17,6 +17,7 @@
 #include <cstdio>
 #include <cstddef>
 #include <cstring>
+#include <mutex>
 #include <string>
 
 #include "layer.cuh"
@@ -249,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 __global__ void __launch_bounds__(kThreads, 1)
     k_gateup(const __grid_constant__ Params p, const __grid_constant__ Maps maps) {
-  const int g = blockIdx.x / p.n_ftiles, ft = blockIdx.x - g * p.n_ftiles;
+  const int g = blockIdx.x / p.n_ftiles;
   if (g >= p.sched->n_groups) return;
   char* smem;
   Ctrl* c;
@@ -262,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 __global__ void __launch_bounds__(kThreads, 1)
     k_down(const __grid_constant__ Params p, const __grid_constant__ Maps maps) {
   const int n_down = p.n_dtiles * p.ks;
-  const int g = blockIdx.x / n_down, r = blockIdx.x - g * n_down;
+  const int g = blockIdx.x / n_down;
   if (g >= p.sched->n_groups) return;
   char* smem;
   Ctrl* c;
@@ -286,6 +287,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ====================================================================== host side
 
 using namespace moe;
+
+// Scratch of moe_layer_forward_static: a file-scope device array, so that
+// entry point needs no allocation call.  Every GPU that loads this library
+// holds it until the process exits.
+constexpr size_t kStaticScratchBytes = 32u << 20;
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
 namespace {
 
@@ -906,6 +913,79 @@ int moe_layer_get_trace(moe_layer_t* h, uint64_t* records, int cap, void* stream
     return -1;
   }
   return n;
+}
+
+/* See include/moe.h.  Runs the unchanged moe_layer_forward on a copy of the
+ * handle whose workspace is the file-scope scratch array above. */
+int moe_layer_forward_static(moe_layer_t* h, int T, const void* x, const void* router_w,
+                             const void* w_gate, const void* w_up, const void* w_down, void* out,
+                             void* stream) {
+  if (!h) return fail(MOE_E_INVAL, "null handle");
+  if (T < 0) return fail(MOE_E_INVAL, "T must be >= 0");
+  if (T == 0) return MOE_OK;
+  if (T > kMaxE * kRouteTokens) return fail(MOE_E_INVAL, "T out of range (1..32768)");
+  // One-time set-up per device, with that device current: the scratch
+  // array's device address (the host-side symbol is only a stand-in), the
+  // device's SM count and the kernels' shared-memory limit.  No allocation.
+  struct DeviceSetup {
+    bool done = false;
+    void* scratch = nullptr;
+    int num_sms = 0;
+  };
+  static DeviceSetup setups[64];
+  static std::mutex setup_mutex;
+  int dev = 0;
+  CK(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return fail(MOE_E_INVAL, "device ordinal out of range");
+  {
+    std::lock_guard<std::mutex> lock(setup_mutex);
+    DeviceSetup& s = setups[dev];
+    if (!s.done) {
+      int cc_major = 0, cc_minor = 0;
+      CK(cudaDeviceGetAttribute(&cc_major, cudaDevAttrComputeCapabilityMajor, dev));
+      CK(cudaDeviceGetAttribute(&cc_minor, cudaDevAttrComputeCapabilityMinor, dev));
+      if (cc_major != 10 || cc_minor != 3)
+        return fail(MOE_E_INVAL, "this library is built for sm_103a (GB300) only");
+      if (!encode_fn()) return fail(MOE_E_CUDA, "cuTensorMapEncodeTiled is not available");
+      void* ptr = nullptr;
+      cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+      CK(cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev));
+      CK(cudaFuncSetAttribute(moe_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget));
+      CK(cudaFuncSetAttribute(k_route, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget));
+      CK(cudaFuncSetAttribute(k_plan, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget));
+      CK(cudaFuncSetAttribute(k_gather, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget));
+      CK(cudaFuncSetAttribute(k_gateup, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget));
+      CK(cudaFuncSetAttribute(k_down, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget));
+      CK(cudaFuncSetAttribute(k_combine, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget));
+      s.scratch = ptr;
+      s.done = true;
+    }
+  }
+  const DeviceSetup& s = setups[dev];
+  // A workspace laid out for exactly T tokens inside the scratch array; when
+  // the fp32 split-K partials do not fit, the down projection keeps Y in bf16.
+  moe_layer tmp = *h;
+  tmp.device = dev;
+  tmp.num_sms = s.num_sms;
+  tmp.x_dev_stage = tmp.out_dev_stage = nullptr;
+  tmp.trace = nullptr;  // the trace counters live in the caller's own workspace
+  tmp.trace_cap = 0;
+  Bounds b = make_bounds(&tmp, T);
+  layout(&tmp, b);
+  if (tmp.ws_bytes > kStaticScratchBytes) {
+    const long long rows = (long long)T * h->k + (long long)T * h->S;
+    b.y_elems = (size_t)((rows * h->d + 1) / 2);
+    layout(&tmp, b);
+  }
+  if (tmp.ws_bytes > kStaticScratchBytes)
+    return fail(MOE_E_INVAL, "layer too large for the " + std::to_string(kStaticScratchBytes >> 20) +
+                                 " MiB scratch of moe_layer_forward_static (needs " +
+                                 std::to_string(tmp.ws_bytes >> 20) + " MiB); use moe_layer_reserve");
+  tmp.B = b;
+  tmp.ws = static_cast<char*>(s.scratch);
+  tmp.T_max = T;
+  return moe_layer_forward(&tmp, T, x, router_w, w_gate, w_up, w_down, out, stream);
 }
 
 void moe_layer_destroy(moe_layer_t* h) {
