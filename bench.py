@@ -63,6 +63,8 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--option", action="append", default=[], metavar="NAME=VALUE",
+                    help="a layer option (MoELayer.set_option) for the timed runs")
     return ap.parse_args(argv)
 
 
@@ -230,6 +232,9 @@ def run_ours(args):
     layer.reserve(w.T)
     layer.set_router_bias(bias)
     layer.set_option("mode", 0 if args.mode == "persistent" else 1)
+    for kv in args.option:
+        name, val = kv.split("=", 1)
+        layer.set_option(name, int(val))
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
 
@@ -334,6 +339,7 @@ def run_ours(args):
             "inputs": "seeded synthetic (gen module), weights ~N(0,1/fan_in)",
             "mover_ctas": movers, "grid_ctas": grid, "stolen_tasks": stolen,
             "wall_s_timed_region": wall,
+            "options": {kv.split("=", 1)[0]: int(kv.split("=", 1)[1]) for kv in args.option},
         },
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": kernels_per_step * K, "clocks": clocks,

@@ -47,7 +47,8 @@ __device__ __forceinline__ void cta_setup(const Params& p, const Maps& maps, cha
     mbar_init(&c->cbar[1], 1);
     fence_mbar_init();
     c->deadline = globaltimer() + p.timeout_ns;
-    c->next_task = -1;
+    c->mb_posted = c->mb_taken = c->mb_done = c->mb_handled = 0;
+    c->mb_late = -1;
   }
   if (with_tmem && warp == 1) {
     tmem_alloc(&c->tmem_base, kTmemCols);
@@ -78,6 +79,7 @@ __device__ __forceinline__ void cta_setup(const Params& p, const Maps& maps, cha
   st.n_gather = st.mover_total = st.gemm_total = 0;
   st.pf_task = -1;
   st.pf_count = 0;
+  st.taken = 0;
 }
 
 __device__ __forceinline__ void cta_teardown(Ctrl* c, bool with_tmem) {
@@ -90,43 +92,59 @@ __device__ __forceinline__ void cta_teardown(Ctrl* c, bool with_tmem) {
 }
 
 // ------------------------------------------------------------------ persistent megakernel
+// Nine warps per CTA.  Warps 0-7 (the compute warps) run tasks: the producer
+// (warp 0 lane 0) and MMA issuer (warp 1 lane 0) of the GEMM tiles, the
+// epilogues, the bulk-copy movers.  Warp 8 (the scheduler warp) never runs
+// task code: it claims the next task while the current one runs -- at once
+// when the first-choice queue is deep, else when the running task reaches its
+// late phase (a GEMM tile's last loads issued, a mover's last round) -- and
+// it runs the notifications of finished tasks (GPU-scope release, counter
+// bumps, pushes) while the compute warps already run the next task.  The two
+// sides talk through the shared-memory mailbox in Ctrl.
 
-__global__ void __launch_bounds__(kThreads, 1)
-    moe_persistent_kernel(const __grid_constant__ Params p, const __grid_constant__ Maps maps) {
-  char* smem;
-  Ctrl* c;
-  CtaState st;
-  cta_setup(p, maps, smem, c, st, true);
-  int executed = 0, gemm_tasks = 0, mover_tasks = 0, ahead = 0;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+__device__ __forceinline__ void trace_record(const Params& p, unsigned long long w0,
+                                             unsigned long long a, unsigned long long b,
+                                             unsigned long long e) {
+  const int i = atomicAdd(&p.sched->trace_n, 1);
+  if (i < p.trace_cap) {
+    unsigned long long* r = p.trace + (size_t)i * 4;
+    r[0] = w0;
+    r[1] = a;
+    r[2] = b;
+    r[3] = e;
+  }
+}
+
+__device__ void compute_loop(const Params& p, const Maps& maps, char* smem, Ctrl* c,
+                             CtaState& st) {
+  int executed = 0, gemm_tasks = 0, mover_tasks = 0, done = 0;
   while (true) {
-    if (warp == 0) {  // warp 0 takes the task held from the claim ahead, or claims one
-      if (lane == 0) c->t_claim = globaltimer();
-      const int held = c->next_task;
-      __syncwarp();
-      const int t = held >= 0 ? held : claim_next(p, st);
-      if (lane == 0) {
-        c->next_task = -1;
-        c->task = t;
-        c->t_start = globaltimer();
+    if (threadIdx.x == 0) {  // take the next posted task, or the exit token
+      uint32_t backoff = 32;
+      int t = -1;
+      while (true) {
+        if (ld_acquire_cta_shared(&c->mb_posted) > st.taken) {
+          t = c->mb_task[st.taken & 1];
+          c->t_claim = c->mb_tclaim[st.taken & 1];
+          ++st.taken;
+          st_release_cta_shared(&c->mb_taken, st.taken);
+          break;
+        }
+        if (ld_relaxed(&p.sched->status) != 0) break;
+        if (globaltimer() > st.deadline) {
+          set_status(p, MOE_E_TIMEOUT, 30);
+          break;
+        }
+        __nanosleep(backoff);
+        if (backoff < 256) backoff <<= 1;
       }
+      c->task = t;
+      c->t_start = globaltimer();
     }
-    __syncthreads();
+    cta_sync();
     const int task = c->task;
     if (task < 0) break;
     ++executed;
-    // claim ahead: warp 2 (idle during a GEMM tile's main loop) takes the
-    // next task now, so the claim's round trips overlap this task (and the
-    // producer can start the next GEMM tile's loads early); only when the
-    // first-choice queue is deep, so holding a task cannot starve another CTA,
-    // and never behind a router tile, which gates everything else
-    if (warp == 2 && p.ahead_depth > 0 && task_type(task) != kTaskRoute) {
-      const int r = claim_once(p, st, p.ahead_depth);
-      if (lane == 0 && r >= 0) {
-        st_release_cta_shared(&c->next_task, r);
-        ++ahead;
-      }
-    }
     const int type = task_type(task), pl = task_payload(task);
     if (type == kTaskRoute) {
       const int tile = pl / p.route_ks, split = pl - tile * p.route_ks;
@@ -136,73 +154,55 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int old = atom_add_acq_rel(&p.sched->route_done, 1);
           c->flag = (old + 1 == p.n_route);
         }
-        __syncthreads();
-        if (c->flag) {
+        cta_sync();
+        if (c->flag) {  // the last router tile: this CTA runs the plan
           fence_acq_rel_gpu();
           const unsigned long long t_plan = globaltimer();
           plan_task(p, smem, c, true);
           if (threadIdx.x == 0 && p.trace) {
-            const int i = atomicAdd(&p.sched->trace_n, 1);
-            if (i < p.trace_cap) {
-              unsigned long long* r = p.trace + (size_t)i * 4;
-              r[0] = ((unsigned long long)blockIdx.x << 32) | (unsigned)task_id(kTaskPlan, 0);
-              r[1] = t_plan;
-              r[2] = t_plan;
-              r[3] = globaltimer();
-            }
-            for (int ph = 0; ph < 7; ++ph) {  // phase boundaries of the plan
-              const int k2 = atomicAdd(&p.sched->trace_n, 1);
-              if (k2 < p.trace_cap) {
-                unsigned long long* r = p.trace + (size_t)k2 * 4;
-                r[0] = ((unsigned long long)blockIdx.x << 32) | (unsigned)task_id(kTaskPlan, 1 + ph);
-                r[1] = r[2] = r[3] = c->plan_t[ph];
-              }
-            }
+            const unsigned long long w0 = (unsigned long long)blockIdx.x << 32;
+            trace_record(p, w0 | (unsigned)task_id(kTaskPlan, 0), t_plan, t_plan, globaltimer());
+            for (int ph = 0; ph < 7; ++ph)  // phase boundaries of the plan
+              trace_record(p, w0 | (unsigned)task_id(kTaskPlan, 1 + ph), c->plan_t[ph],
+                           c->plan_t[ph], c->plan_t[ph]);
           }
         }
       }
     } else if (type == kTaskGather) {
       ++mover_tasks;
-      const int g = pl >> 3, ch = pl & 7;
-      gather_task(p, g, ch, smem, c, st);
-      notify_gather_done(p, g, c);
+      gather_task(p, pl >> 3, pl & 7, smem, c, st);
     } else if (type == kTaskGateUp) {
       ++gemm_tasks;
-      const int g = pl / p.n_ftiles;
       gateup_task(p, maps, task, smem, c, st);
-      notify_gateup_done(p, g);
     } else if (type == kTaskDown) {
       ++gemm_tasks;
-      const int g = pl / (p.n_dtiles * p.ks);
       down_task(p, maps, task, smem, c, st);
-      notify_down_done(p, g, c);
     } else if (type == kTaskCombine) {
       ++mover_tasks;
       combine_task(p, pl, smem, c, st);
-      __syncthreads();
     } else {
       if (threadIdx.x == 0) set_status(p, MOE_E_DEVICE, 6);
       break;
     }
-    if (threadIdx.x == 0 && p.trace) {
-      const int i = atomicAdd(&p.sched->trace_n, 1);
-      if (i < p.trace_cap) {
-        unsigned long long* r = p.trace + (size_t)i * 4;
-        r[0] = ((unsigned long long)blockIdx.x << 32) | (unsigned)task;
-        r[1] = c->t_claim;
-        r[2] = c->t_start;
-        r[3] = globaltimer();
+    // hand the finished task to the scheduler warp: every compute thread's
+    // writes (async proxy included) come before thread 0's CTA-scope release
+    fence_proxy_async_global();
+    cta_sync();
+    if (threadIdx.x == 0) {
+      if (p.trace)
+        trace_record(p, ((unsigned long long)blockIdx.x << 32) | (unsigned)task, c->t_claim,
+                     c->t_start, globaltimer());
+      while (done - ld_acquire_cta_shared(&c->mb_handled) >= 2) {  // ring of two
+        if (ld_relaxed(&p.sched->status) != 0) break;
+        if (globaltimer() > st.deadline) {
+          set_status(p, MOE_E_TIMEOUT, 31);
+          break;
+        }
+        __nanosleep(64);
       }
-    }
-  }
-  if (threadIdx.x == 0 && p.trace) {  // exit record: reason and both queue words
-    const int i = atomicAdd(&p.sched->trace_n, 1);
-    if (i < p.trace_cap) {
-      unsigned long long* r = p.trace + (size_t)i * 4;
-      r[0] = ((unsigned long long)blockIdx.x << 32) | 0x7fffffffu;
-      r[1] = ((unsigned long long)st.polls << 8) | (unsigned long long)st.exit_reason;
-      r[2] = *reinterpret_cast<volatile unsigned long long*>(&p.sched->gemm_q[0]);
-      r[3] = globaltimer();
+      c->mb_done_task[done & 1] = task;
+      ++done;
+      st_release_cta_shared(&c->mb_done, done);
     }
   }
   if (threadIdx.x == 0) {
@@ -210,7 +210,106 @@ __global__ void __launch_bounds__(kThreads, 1)
     atomicAdd(&p.sched->stat_gemm, gemm_tasks);
     atomicAdd(&p.sched->stat_mover, mover_tasks);
   }
-  if (threadIdx.x == 64) atomicAdd(&p.sched->stat_ahead, ahead);
+}
+
+__device__ void scheduler_loop(const Params& p, Ctrl* c, CtaState& st) {
+  const int lane = threadIdx.x & 31;
+  const unsigned full = 0xffffffffu;
+  int posted = 0, handled = 0, ahead = 0, polled_seq = -1;
+  bool exit_posted = false;
+  uint32_t backoff = 32;
+  auto post = [&](int t) {
+    if (lane == 0) {
+      c->mb_task[posted & 1] = t;
+      c->mb_tclaim[posted & 1] = globaltimer();
+    }
+    ++posted;
+    __syncwarp();
+    if (lane == 0) st_release_cta_shared(&c->mb_posted, posted);
+  };
+  while (true) {
+    bool progress = false;
+    // notifications of the finished tasks
+    const int done = __shfl_sync(full, ld_acquire_cta_shared(&c->mb_done), 0);
+    if (handled < done) {
+      fence_acq_rel_gpu();  // the compute warps' writes, acquired above, before our releases
+      while (handled < done) {
+        sched_notify(p, c->mb_done_task[handled & 1]);
+        ++handled;
+      }
+      __syncwarp();
+      if (lane == 0) st_release_cta_shared(&c->mb_handled, handled);
+      progress = true;
+    }
+    const int status = __shfl_sync(full, lane == 0 ? ld_relaxed(&p.sched->status) : 0, 0);
+    if (status != 0) {
+      st.exit_reason = 2;
+      break;
+    }
+    if (exit_posted) {
+      if (handled >= posted - 1) break;  // every real task finished and notified
+    } else {
+      const int taken = __shfl_sync(full, ld_acquire_cta_shared(&c->mb_taken), 0);
+      if (posted == taken) {  // nothing waiting in the mailbox
+        const bool idle = taken == done;
+        const bool late = __shfl_sync(full, ld_acquire_cta_shared(&c->mb_late), 0) == taken;
+        int min_depth = 0;
+        if (idle || late) {
+          min_depth = 1;
+        } else if (p.ahead_depth > 0 && polled_seq != taken) {
+          min_depth = p.ahead_depth;  // early claim: once per task, deep queue only
+          polled_seq = taken;
+        }
+        if (min_depth > 0) {
+          const int r = claim_once(p, st, min_depth);
+          if (r >= 0) {
+            post(r);
+            if (!idle) ++ahead;
+            progress = true;
+          } else if (r == -4) {
+            progress = true;  // lost a CAS: retry at once
+          } else if (r == -2 || r == -3) {
+            st.exit_reason = r == -2 ? 1 : 2;
+            post(-1);
+            exit_posted = true;
+            progress = true;
+          } else if (idle) {
+            ++st.polls;
+            const int late_t = __shfl_sync(full, lane == 0 ? (globaltimer() > st.deadline) : 0, 0);
+            if (late_t) {
+              if (lane == 0) set_status(p, MOE_E_TIMEOUT, 3);
+              st.exit_reason = 3;
+              break;
+            }
+          }
+        }
+      }
+    }
+    if (progress) {
+      backoff = 32;
+    } else {
+      __nanosleep(backoff);
+      if (backoff < 512) backoff <<= 1;
+    }
+  }
+  if (lane == 0) {
+    atomicAdd(&p.sched->stat_ahead, ahead);
+    if (p.trace)  // exit record: reason and polls, the GEMM queue's first word
+      trace_record(p, ((unsigned long long)blockIdx.x << 32) | 0x7fffffffu,
+                   ((unsigned long long)st.polls << 8) | (unsigned long long)st.exit_reason,
+                   *reinterpret_cast<volatile unsigned long long*>(&p.sched->gemm_q[0]),
+                   globaltimer());
+  }
+}
+
+__global__ void __launch_bounds__(kThreads + 32, 1)
+    moe_persistent_kernel(const __grid_constant__ Params p, const __grid_constant__ Maps maps) {
+  char* smem;
+  Ctrl* c;
+  CtaState st;
+  cta_setup(p, maps, smem, c, st, true);
+  if (threadIdx.x < kThreads) compute_loop(p, maps, smem, c, st);
+  else scheduler_loop(p, c, st);
   cta_teardown(c, true);
 }
 
@@ -480,6 +579,8 @@ int choose_tiling(const moe_layer* h, int T, Tiling* t) {
   const int ctrl = (int)align_up(sizeof(Ctrl), 1024);
   t->stages = std::min(8, (kSmemBudget - 1024 - ctrl) / t->stage_bytes);
   if (t->stages < 2) return fail(MOE_E_INVAL, "tile too large for shared memory");
+  if ((size_t)t->stages * t->stage_bytes < route_smem_bytes(h->E))
+    return fail(MOE_E_INVAL, "router logits do not fit in shared memory");
   t->smem = 1024 + t->stages * t->stage_bytes + ctrl;
   // down-projection K split: fp32 partials when the batch is small
   const int kblocks = h->f / kBK;
@@ -492,7 +593,7 @@ int choose_tiling(const moe_layer* h, int T, Tiling* t) {
   t->y_f32 = ks > 1 ? 1 : ((size_t)rows * h->d <= h->B.y_elems ? 1 : 0);
   t->rt = kRouteTokens;
   // combine tile: ~one per SM, (k+S) rows per token, <= 256 (token, slot) pairs
-  int ct = cdiv(T, std::max(h->num_sms, 1));
+  int ct = cdiv(T, 2 * std::max(h->num_sms, 1));
   ct = std::max(1, std::min(ct, kThreads / h->k));
   t->ct = ct;
   return MOE_OK;
@@ -790,7 +891,7 @@ int moe_layer_forward(moe_layer_t* h, int T, const void* x, const void* router_w
     p.ahead_depth = h->ahead_opt < 0 ? grid : h->ahead_opt;
     // fetch-and-add claims when more tasks wait than there are claimers
     p.fa_depth = (p.ahead_depth > 0 ? 2 : 1) * grid + 8;
-    moe_persistent_kernel<<<grid, kThreads, tl.smem, s>>>(p, m);
+    moe_persistent_kernel<<<grid, kThreads + 32, tl.smem, s>>>(p, m);
     CK(cudaGetLastError());
   } else {
     h->last_grid = 0;

@@ -19,11 +19,21 @@ struct Ctrl {
   unsigned long long t_claim, t_start;
   uint32_t tmem_base;
   int task;
-  int next_task;
   int flag;
+  // mailbox between the scheduler warp and the compute warps (persistent
+  // kernel): tasks posted to the compute warps (a ring of two: the running
+  // task's slot and the next one), finished tasks handed back for their
+  // notifications (a ring of two), and the sequence number of the task whose
+  // late phase has begun (the scheduler claims the next task then)
+  int mb_task[2];
+  unsigned long long mb_tclaim[2];
+  int mb_posted, mb_taken, mb_late;
+  int mb_done_task[2];
+  int mb_done, mb_handled;
   int ival[8];
   int qbase[kShards];
   unsigned long long plan_t[8];  // plan phase timestamps (trace only)
+  int pl_cb[kMaxE], pl_sib[kMaxE], pl_cpg[kMaxE];  // plan: per expert slot
   int tok[kThreads];      // scratch: token ids / combine tiles per row
   int cnt[kMaxE];         // scratch: per-expert counts
   int aux[kMaxE];
@@ -32,7 +42,7 @@ struct Ctrl {
   uint64_t gbar;                 // bulk-copy barrier of the gather
   uint64_t cbar[2];              // bulk-copy barriers of the combine (two buffers)
   uint32_t mask[kMaxE * 4];      // router: 128-bit token mask per expert
-  float bias_s[kMaxE];
+  alignas(16) float bias_s[kMaxE];
 };
 
 // Per-thread state that lives across tasks.
@@ -48,6 +58,7 @@ struct CtaState {
   bool plan_seen;         // the plan's totals below are cached
   int n_gather, mover_total, gemm_total;
   int pf_task, pf_count;  // producer: task whose first k blocks are already loading
+  int taken;              // compute thread 0: tasks taken from the mailbox
 };
 
 // ------------------------------------------------------------------ helpers
@@ -97,12 +108,45 @@ __device__ __forceinline__ void set_status(const Params& p, int code, int info) 
   if (atomicCAS(&p.sched->status, 0, code) == 0) p.sched->err_info = info;
 }
 
+// Barriers of the kThreads compute threads (named barrier 1).  The persistent
+// kernel adds a scheduler warp that never joins them, so task code must not
+// use __syncthreads.
+__device__ __forceinline__ void cta_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
+}
+
+__device__ __forceinline__ int cta_sync_and(int pred) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.s32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, %2, p;\n\t"
+      "selp.s32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred), "n"(kThreads)
+      : "memory");
+  return r;
+}
+
+__device__ __forceinline__ int cta_sync_count(int pred) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.s32 p, %1, 0;\n\t"
+      "bar.red.popc.u32 %0, 1, %2, p;\n\t}"
+      : "=r"(r)
+      : "r"(pred), "n"(kThreads)
+      : "memory");
+  return r;
+}
+
 // Release this CTA's global writes (generic and, for TMA readers, async
-// proxy) before a dependency counter is bumped.  Called by every thread.
+// proxy) before a dependency counter is bumped.  Called by every compute
+// thread.
 __device__ __forceinline__ void release_writes() {
   fence_proxy_async_global();
   __threadfence();
-  __syncthreads();
+  cta_sync();
 }
 
 // Group descriptor: shared-expert groups [0, n_shared_groups) are known at
@@ -214,7 +258,7 @@ __device__ __forceinline__ void push_gen_block(const Params& p, const QueueRef& 
     }
     c->qbase[threadIdx.x] = base;
   }
-  __syncthreads();
+  cta_sync();
   for (int i = threadIdx.x; i < n; i += kThreads) {
     const int j = (r0 + i) & (kShards - 1);
     const int slot = c->qbase[j] + i / kShards;
@@ -362,9 +406,9 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* total, Ctrl* c) 
     const int y = __shfl_up_sync(0xffffffffu, x, o);
     if (lane >= o) x += y;
   }
-  __syncthreads();
+  cta_sync();
   if (lane == 31) c->ival[warp] = x;
-  __syncthreads();
+  cta_sync();
   int wbase = 0, tot = 0;
 #pragma unroll
   for (int w = 0; w < kThreads / 32; ++w) {
@@ -372,7 +416,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* total, Ctrl* c) 
     if (w < warp) wbase += s;
     tot += s;
   }
-  __syncthreads();
+  cta_sync();
   *total = tot;
   return wbase + x - v;
 }
@@ -410,7 +454,7 @@ __device__ void plan_task(const Params& p, char* scratch, Ctrl* c, bool push) {
     } else {
       for (int i = tid; i < n; i += kThreads) tb[i] = __ldcg(p.tile_cnt + i);
     }
-    __syncthreads();
+    cta_sync();
   }
   if (tid < E) {
     int run = 0;
@@ -424,11 +468,11 @@ __device__ void plan_task(const Params& p, char* scratch, Ctrl* c, bool push) {
     p.counts[tid] = run;
   }
   if (in_smem) {  // the gathers read the tile bases from global memory
-    __syncthreads();
+    cta_sync();
     const int n = ntile * E;
     for (int i = tid; i < n; i += kThreads) p.tile_cnt[i] = tb[i];
   }
-  __syncthreads();
+  cta_sync();
   if (threadIdx.x == 0) c->plan_t[1] = globaltimer();
   int total = 0;
   const int off = block_exclusive_scan(tid < E ? cnt[tid] : 0, &total, c);
@@ -442,13 +486,14 @@ __device__ void plan_task(const Params& p, char* scratch, Ctrl* c, bool push) {
   if (tid < E) {
     const int me = cnt[tid];
     int r = 0;
+#pragma unroll 8
     for (int e2 = 0; e2 < E; ++e2) {
       const int o = cnt[e2];
       r += (o > me) || (o == me && e2 < tid);
     }
     order[r] = tid;
   }
-  __syncthreads();
+  cta_sync();
   if (threadIdx.x == 0) c->plan_t[3] = globaltimer();
   // groups: order slot r -> expert order[r]
   int e_r = tid < E ? order[tid] : 0;
@@ -468,31 +513,41 @@ __device__ void plan_task(const Params& p, char* scratch, Ctrl* c, bool push) {
     return;
   }
   // routed groups follow the shared-expert groups (see load_group)
-  {
-    int cb = chunk_base;
-    const int sib0 = p.n_shared_groups + gfirst;
-    for (int m = 0; m < nmt; ++m) {
-      const int g = sib0 + m;
-      const int nrows = min(rows_per, n_r - m * rows_per);
-      const int row0 = off_e + m * rows_per;
-      p.groups[g] = Group{e_r, row0, nrows, row0, sib0, nmt, my_chunks, off_e};
-      if (push) {  // gather i of the layer: shard i mod kShards, local slot i / kShards
-        const int nc = gather_chunks(nrows);
-        for (int q = 0; q < nc; ++q) {
-          const int i = cb + q;
-          if ((i / kShards) < p.mover_seg)
-            p.ring_mover[(i & (kShards - 1)) * p.mover_seg + i / kShards] =
-                task_id(kTaskGather, g * 8 + q) + 1;
-        }
-        cb += nc;
+  const int sib0 = p.n_shared_groups + gfirst;
+  for (int m = 0; m < nmt; ++m) {
+    const int nrows = min(rows_per, n_r - m * rows_per);
+    const int row0 = off_e + m * rows_per;
+    p.groups[sib0 + m] = Group{e_r, row0, nrows, row0, sib0, nmt, my_chunks, off_e};
+  }
+  if (push) {
+    // gather i of the layer: the expert slot whose chunk range holds i, then
+    // the group (every group of a slot but its last is full) and the chunk;
+    // written by all threads, shard i mod kShards, local slot i / kShards
+    if (tid < E) {
+      c->pl_cb[tid] = chunk_base;
+      c->pl_sib[tid] = sib0;
+      c->pl_cpg[tid] = rows_per > 0 ? gather_chunks(rows_per) : 1;
+    }
+    cta_sync();
+    for (int i = tid; i < n_gather; i += kThreads) {
+      int lo = 0, hi = E - 1;  // last slot whose chunk base is <= i
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (c->pl_cb[mid] <= i) lo = mid;
+        else hi = mid - 1;
       }
+      const int local = i - c->pl_cb[lo];
+      const int m = local / c->pl_cpg[lo], q = local - m * c->pl_cpg[lo];
+      if ((i / kShards) < p.mover_seg)
+        p.ring_mover[(i & (kShards - 1)) * p.mover_seg + i / kShards] =
+            task_id(kTaskGather, (c->pl_sib[lo] + m) * 8 + q) + 1;
     }
   }
-  __syncthreads();
-  if (threadIdx.x == 0) c->plan_t[4] = globaltimer();
+  cta_sync();
   if (threadIdx.x == 0) c->plan_t[4] = globaltimer();
   if (threadIdx.x == 0) c->plan_t[5] = globaltimer();
   // cost model (spatial split): CTA-seconds of mover work against GEMM work
+  const int touched_routed = cta_sync_count(tid < E && cnt[tid] > 0);
   if (tid == 0) {
     const int n_groups = p.n_shared_groups + n_routed;
     const int n_down = p.n_dtiles * p.ks;
@@ -511,8 +566,7 @@ __device__ void plan_task(const Params& p, char* scratch, Ctrl* c, bool push) {
       const float b_move = Tk * p.d * 2.f * 2.f +                     // gather: read + write
                            ((float)p.T * (k + p.S)) * p.d * ybytes +  // combine reads
                            (float)p.T * p.d * 2.f;                    // combine writes
-      int touched = p.S;
-      for (int e = 0; e < E; ++e) touched += cnt[e] > 0;
+      const int touched = p.S + touched_routed;
       const float flops = 6.f * (Tk + (float)p.T * p.S) * p.d * p.f;
       const float wbytes = (float)touched * 3.f * p.f * p.d * 2.f;
       const float a = b_move / p.beta_move;                            // CTA-seconds
@@ -530,13 +584,13 @@ __device__ void plan_task(const Params& p, char* scratch, Ctrl* c, bool push) {
       if (cnt > p.mover_seg) set_status(p, MOE_E_DEVICE, 8);
       if (cnt > 0) atomicAdd(p.sched->mover_q + tid, (unsigned long long)cnt << 32);
     }
-    __syncthreads();
+    cta_sync();
     if (tid == 0) {
       __threadfence();
       st_release(&p.sched->plan_done, 1);
     }
   } else {
-    __syncthreads();
+    cta_sync();
   }
 }
 
@@ -561,7 +615,7 @@ __device__ void gather_task(const Params& p, int g, int chunk, char* smem, Ctrl*
   int* col = c->aux;  // base[tau][e] for all router tiles tau
   for (int tau = threadIdx.x; tau < p.n_route; tau += kThreads)
     col[tau] = __ldcg(p.tile_cnt + (size_t)tau * p.E + G.e);
-  __syncthreads();
+  cta_sync();
   if (threadIdx.x < nr) {
     const int r = r0 + threadIdx.x;
     const int local = r - G.pad;
@@ -591,13 +645,14 @@ __device__ void gather_task(const Params& p, int g, int chunk, char* smem, Ctrl*
     for (int j = 0; j < p.k; ++j)
       if (__ldcg(p.idx + (size_t)t * p.k + j) == G.e) p.pos[(size_t)t * p.k + j] = r;
   }
-  __syncthreads();
+  cta_sync();
   if (threadIdx.x == 0) {
     const uint32_t row_bytes = (uint32_t)p.d * 2;
     const int cap = max(1, (int)(((size_t)p.stages * p.stage_bytes) / row_bytes));
     fence_proxy_async_shared();
     for (int r = 0; r < nr; r += cap) {
       const int n = min(cap, nr - r);
+      if (r + cap >= nr) st_release_cta_shared(&c->mb_late, st.taken);  // last round
       mbar_arrive_expect_tx(&c->gbar, (uint32_t)n * row_bytes);
       for (int i = 0; i < n; ++i)
         bulk_load(smem + (size_t)i * row_bytes, p.x + (size_t)c->tok[r + i] * p.d, row_bytes,
@@ -666,7 +721,7 @@ __device__ void combine_task(const Params& p, int ctile, char* smem, Ctrl* c, Ct
     c->tok[i] = __ldcg(p.pos + (size_t)t0 * k + i);
     c->wsum[i] = __ldcg(p.wgt + (size_t)t0 * k + i);
   }
-  __syncthreads();
+  cta_sync();
   const int nsrc = k + p.S;
   const int nsplit = p.y_f32 ? p.ks : 1;
   const int ebytes = p.y_f32 ? 4 : 2;
@@ -674,6 +729,7 @@ __device__ void combine_task(const Params& p, int ctile, char* smem, Ctrl* c, Ct
   const size_t per_tok = (size_t)nsrc * nsplit * row_bytes;
   const size_t mem = (size_t)p.stages * p.stage_bytes;
   if (per_tok > mem) {  // one token's rows do not fit: sum straight from global
+    if (threadIdx.x == 0) st_release_cta_shared(&c->mb_late, st.taken);
     combine_direct(p, t0, nt, c);
     return;
   }
@@ -707,9 +763,10 @@ __device__ void combine_task(const Params& p, int ctile, char* smem, Ctrl* c, Ct
   uint4* out = reinterpret_cast<uint4*>(p.out);
   for (int r = 0; r < rounds; ++r) {
     const int b = r % nbuf;
+    if (threadIdx.x == 0 && r == rounds - 1) st_release_cta_shared(&c->mb_late, st.taken);
     const bool got = mbar_wait(&c->cbar[b], (st.comb_phase >> b) & 1u, st.deadline);
     st.comb_phase ^= 1u << b;
-    if (!__syncthreads_and(got ? 1 : 0)) {
+    if (!cta_sync_and(got ? 1 : 0)) {
       if (threadIdx.x == 0) set_status(p, MOE_E_TIMEOUT, 24);
       return;
     }
@@ -742,7 +799,7 @@ __device__ void combine_task(const Params& p, int ctile, char* smem, Ctrl* c, Ct
       }
       out[(size_t)(t0 + t) * nvec + q] = f32x8_to_bf16(acc);
     }
-    __syncthreads();  // buffer b is free again
+    cta_sync();  // buffer b is free again
     if (threadIdx.x == 0 && r + nbuf < rounds) issue(r + nbuf);
   }
 }
@@ -819,10 +876,26 @@ __device__ bool gemm_mainloop(const Params& p, const Maps& maps, const GemmJob& 
     ok = issue_loads(p, job, smem, c, st, st.pipe_it + kb_first, kb_first, job.nkb, pol_a, pol_b) ==
          job.nkb - kb_first;
     if (!ok) set_status(p, MOE_E_TIMEOUT, 10);
-    // Cross-task overlap: when this is a gate/up or down tile and the next
-    // task (claimed ahead) is one too, start its first stages now; they fill
-    // as this tile's last MMAs release the stages.
-    const int nxt = ld_acquire_cta_shared(&c->next_task);
+    // Cross-task overlap: this gate/up or down tile has issued all its loads,
+    // so its late phase begins (the scheduler warp may claim the next task
+    // now).  Until this tile's MMAs complete, wait for that task; when it is
+    // a GEMM tile too, start its first stages now -- they fill as this tile's
+    // last MMAs release the stages.
+    int nxt = -1;
+    if (ok && job.task >= 0) {
+      st_release_cta_shared(&c->mb_late, st.taken);
+      const uint32_t acc_parity = st.gemm_count & 1u;
+      while (true) {
+        if (ld_acquire_cta_shared(&c->mb_posted) > st.taken) {
+          nxt = c->mb_task[st.taken & 1];
+          break;
+        }
+        if (mbar_try_wait(&c->acc_bar, acc_parity) || globaltimer() > st.deadline ||
+            ld_relaxed(&p.sched->status) != 0)
+          break;
+        __nanosleep(64);
+      }
+    }
     if (ok && p.prefetch && job.task >= 0 && nxt >= 0) {
       GemmJob nj;
       if (make_gemm_job(p, maps, nxt, nj)) {
@@ -871,11 +944,11 @@ __device__ bool gemm_mainloop(const Params& p, const Maps& maps, const GemmJob& 
   st.pipe_it += job.nkb;
   // everyone waits for the accumulators
   __syncwarp();
-  const int ok_all = __syncthreads_and(ok ? 1 : 0);
+  const int ok_all = cta_sync_and(ok ? 1 : 0);
   if (!ok_all) return false;
   const bool done = mbar_wait(&c->acc_bar, st.gemm_count & 1u, st.deadline);
   if (!done) set_status(p, MOE_E_TIMEOUT, 12);
-  if (!__syncthreads_and(done ? 1 : 0)) return false;
+  if (!cta_sync_and(done ? 1 : 0)) return false;
   tc_fence_after();
   return true;
 }
@@ -1016,38 +1089,70 @@ __device__ void down_task(const Params& p, const Maps& maps, int task, char* sme
 // ------------------------------------------------------------------ router (tcgen05)
 // Router tile: tokens [tau*128, tau*128 + nt).  Logits on the tensor core:
 // D[token, e] = x[token, :] . Wr[e, :], tokens as the M = 128 operand and the
-// E experts (padded to 16) as N; fp32 accumulation in TMEM.  Epilogue: one
-// thread per token walks its E logits (+ bias) once, keeping the running max
-// and sum of the softmax and the top-k list (logit descending, expert
-// ascending on ties -- the softmax is monotone, so this is the order of p).
-// Then p_j = exp(L_j - max) / sum and w_j = p_j / sum of the kept p.  Ranks
-// inside the tile come from a 128-bit token mask per expert.
+// E experts (padded to 16) as N; fp32 accumulation in TMEM.  The epilogue
+// (below) keeps each token's top-k list in the order logit descending, expert
+// ascending on ties -- the softmax is monotone, so this is the order of p.
+// Ranks inside the tile come from a 128-bit token mask per expert.
 
-template <int KL>
-__device__ __forceinline__ void topk_insert(float (&tv)[KL], int (&te)[KL], float v, int e) {
-  if (!(v > tv[KL - 1])) return;
-  float cv = v;
-  int ce = e;
+// Row stride (floats) of the router tile's logits in shared memory: epad + 4
+// keeps rows 16-byte aligned and puts the float4 reads of 8 consecutive rows
+// (one quarter warp) on distinct banks.
+__device__ __forceinline__ int route_row_stride(int E) { return ((E + 15) / 16) * 16 + 4; }
+
+// Shared-memory bytes the router epilogue needs (logits + exchange area).
+__host__ __device__ __forceinline__ size_t route_smem_bytes(int E) {
+  return (size_t)kRouteTokens * (((E + 15) / 16) * 16 + 4) * 4 +
+         (size_t)(2 + 2 * kMaxK) * kRouteTokens * 4;
+}
+
+// The top-k order: larger logit first, smaller expert first on equal logits.
+// After topk_cx, (av, ae) is the earlier of the two pairs.  Bitwise, not
+// short-circuit, logic keeps the exchange a run of predicated selects.
+__device__ __forceinline__ void topk_cx(float& av, int& ae, float& bv, int& be) {
+  const bool sw = (bv > av) | ((bv == av) & (be < ae));
+  const float v = av;
+  const int e = ae;
+  av = sw ? bv : av;
+  ae = sw ? be : ae;
+  bv = sw ? v : bv;
+  be = sw ? e : be;
+}
+
+// Merge the sorted list b (length KL) into the sorted top-KL list t: the
+// better of t[i] and b[KL-1-i] is a bitonic sequence holding the KL best of
+// both, which log2(KL) half-cleaner stages sort.  Branch-free: every lane of a
+// warp runs the same instructions, whatever its data.
+template <int KL, int NB>
+__device__ __forceinline__ void topk_merge(float (&tv)[KL], int (&te)[KL], float (&bv)[NB],
+                                           int (&be)[NB]) {
+  constexpr int M = NB < KL ? NB : KL;
 #pragma unroll
-  for (int s = 0; s < KL; ++s) {
-    const bool sw = cv > tv[s];
-    const float ov = tv[s];
-    const int oe = te[s];
-    tv[s] = sw ? cv : ov;
-    te[s] = sw ? ce : oe;
-    cv = sw ? ov : cv;
-    ce = sw ? oe : ce;
+  for (int i = 0; i < M; ++i) topk_cx(tv[KL - M + i], te[KL - M + i], bv[M - 1 - i], be[M - 1 - i]);
+#pragma unroll
+  for (int s = KL / 2; s >= 1; s >>= 1) {
+#pragma unroll
+    for (int i = 0; i < KL; ++i)
+      if ((i & s) == 0) topk_cx(tv[i], te[i], tv[i + s], te[i + s]);
   }
 }
 
-// Logits of token row m come from `src(ch, v)`, which fills v[0..15] with
-// columns ch*16 .. ch*16+15; it is called by warps 0-3 only, uniformly.
-template <int KL, class Src>
-__device__ __forceinline__ void route_epilogue(const Params& p, Ctrl* c, int tile, int nt,
-                                               Src src) {
+// Epilogue of one router tile whose logits (without bias) sit in shared
+// memory, token m's row at lg + m * ls.  Two threads per token: warps 0-3
+// take experts [0, eh) and warps 4-7 [eh, E).  Pass 1 keeps each half's
+// top-KL list, four logits at a time (sorted by a 4-input network, then
+// merged); the upper half hands its list to the lower one, whose merged list
+// starts with the row maximum.  Pass 2 sums exp(L - max) over each half.
+// Then p_j = exp(L_j - max) / sum and w_j = p_j / sum of the kept p.
+template <int KL>
+__device__ __noinline__ void route_epilogue(const Params& p, Ctrl* c, int tile, int nt,
+                                            const float* lg, int ls, float* xch) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = p.E, k = p.k;
   const int t0 = tile * kRouteTokens;
+  const int m = (warp & 3) * 32 + lane;
+  const int upper = warp >> 2;
+  const int eh = ((E + 7) / 8) * 4;  // a multiple of 4: float4 aligned
+  const int e0 = upper ? eh : 0, e1 = upper ? E : min(eh, E);
   float tv[KL];
   int te[KL];
 #pragma unroll
@@ -1055,29 +1160,67 @@ __device__ __forceinline__ void route_epilogue(const Params& p, Ctrl* c, int til
     tv[s] = -INFINITY;
     te[s] = 0x7fffffff;
   }
-  const int m = warp * 32 + lane;
-  const bool valid = warp < 4 && m < nt;
-  float mx = -INFINITY, sum = 0.f;
-  if (warp < 4) {
-    for (int ch = 0; ch * 16 < E; ++ch) {
-      float v[16];
-      src(ch, v);
+  const float4* row = reinterpret_cast<const float4*>(lg + (size_t)m * ls);
+  const float4* brow = reinterpret_cast<const float4*>(c->bias_s);
+#pragma unroll 1
+  for (int e4 = e0; e4 < e1; e4 += 4) {
+    const float4 v4 = row[e4 >> 2], b4 = brow[e4 >> 2];
+    float nv[4] = {v4.x + b4.x, v4.y + b4.y, v4.z + b4.z, v4.w + b4.w};
+    int ne[4];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int e = ch * 16 + i;
-        if (e < E) {
-          const float L = v[i] + c->bias_s[e];
-          if (L > mx) {
-            sum = sum * __expf(mx - L) + 1.f;
-            mx = L;
-          } else {
-            sum += __expf(L - mx);
-          }
-          topk_insert<KL>(tv, te, L, e);
-        }
+    for (int j = 0; j < 4; ++j) {
+      ne[j] = e4 + j;
+      if (e4 + j >= e1) {
+        nv[j] = -INFINITY;
+        ne[j] = 0x7fffffff;
       }
     }
+    topk_cx(nv[0], ne[0], nv[1], ne[1]);
+    topk_cx(nv[2], ne[2], nv[3], ne[3]);
+    topk_cx(nv[0], ne[0], nv[2], ne[2]);
+    topk_cx(nv[1], ne[1], nv[3], ne[3]);
+    topk_cx(nv[1], ne[1], nv[2], ne[2]);
+    topk_merge<KL, 4>(tv, te, nv, ne);
   }
+  // exchange area: [2 + 2 * KL][128] words, token-minor (conflict-free)
+  float* x_max = xch;
+  float* x_sum = xch + kRouteTokens;
+  float* x_v = xch + 2 * kRouteTokens;
+  int* x_e = reinterpret_cast<int*>(xch) + (2 + KL) * kRouteTokens;
+  if (upper) {
+#pragma unroll
+    for (int s = 0; s < KL; ++s) {
+      x_v[s * kRouteTokens + m] = tv[s];
+      x_e[s * kRouteTokens + m] = te[s];
+    }
+  }
+  cta_sync();
+  if (!upper) {
+    float bv[KL];
+    int be[KL];
+#pragma unroll
+    for (int s = 0; s < KL; ++s) {
+      bv[s] = x_v[s * kRouteTokens + m];
+      be[s] = x_e[s * kRouteTokens + m];
+    }
+    topk_merge<KL, KL>(tv, te, bv, be);
+    x_max[m] = tv[0];
+  }
+  cta_sync();
+  const float mx = x_max[m];
+  float sum = 0.f;
+#pragma unroll 1
+  for (int e4 = e0; e4 < e1; e4 += 4) {
+    const float4 v4 = row[e4 >> 2], b4 = brow[e4 >> 2];
+    const float nv[4] = {v4.x + b4.x, v4.y + b4.y, v4.z + b4.z, v4.w + b4.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (e4 + j < e1) sum += __expf(nv[j] - mx);
+  }
+  if (upper) x_sum[m] = sum;
+  cta_sync();
+  const bool valid = !upper && m < nt;
+  if (!upper) sum += x_sum[m];
   float pk[KL];
   float kept = 0.f;
 #pragma unroll
@@ -1096,7 +1239,7 @@ __device__ __forceinline__ void route_epilogue(const Params& p, Ctrl* c, int til
       }
     }
   }
-  __syncthreads();
+  cta_sync();
   if (valid) {
     const size_t o = (size_t)(t0 + m) * k;
     const int wd = m >> 5;
@@ -1118,12 +1261,12 @@ __device__ __forceinline__ void route_epilogue(const Params& p, Ctrl* c, int til
   }
 }
 
-template <class Src>
-__device__ __forceinline__ void route_epilogue_k(const Params& p, Ctrl* c, int tile, int nt, Src src) {
-  if (p.k <= 2) route_epilogue<2>(p, c, tile, nt, src);
-  else if (p.k <= 4) route_epilogue<4>(p, c, tile, nt, src);
-  else if (p.k <= 8) route_epilogue<8>(p, c, tile, nt, src);
-  else route_epilogue<16>(p, c, tile, nt, src);
+__device__ __forceinline__ void route_epilogue_k(const Params& p, Ctrl* c, int tile, int nt,
+                                                 const float* lg, int ls, float* xch) {
+  if (p.k <= 2) route_epilogue<2>(p, c, tile, nt, lg, ls, xch);
+  else if (p.k <= 4) route_epilogue<4>(p, c, tile, nt, lg, ls, xch);
+  else if (p.k <= 8) route_epilogue<8>(p, c, tile, nt, lg, ls, xch);
+  else route_epilogue<16>(p, c, tile, nt, lg, ls, xch);
 }
 
 // One router task: tile `tile`, K split `split` of p.route_ks.  With a single
@@ -1139,7 +1282,8 @@ __device__ bool route_task(const Params& p, const Maps& maps, int tile, int spli
   const int nkb = p.d / kBK;
   const int epad = ((p.E + 15) / 16) * 16;
   for (int i = threadIdx.x; i < kMaxE * 4; i += kThreads) c->mask[i] = 0u;
-  for (int e = threadIdx.x; e < p.E; e += kThreads) c->bias_s[e] = p.bias ? __ldg(p.bias + e) : 0.f;
+  for (int e = threadIdx.x; e < kMaxE; e += kThreads)
+    c->bias_s[e] = (p.bias && e < p.E) ? __ldg(p.bias + e) : 0.f;
   GemmJob job;
   job.a0 = &maps.xr;
   job.a1 = nullptr;
@@ -1159,8 +1303,25 @@ __device__ bool route_task(const Params& p, const Maps& maps, int tile, int spli
   if (ok) {
     const int warp = threadIdx.x >> 5;
     const uint32_t lane_addr = c->tmem_base + ((uint32_t)((warp & 3) * 32) << 16);
+    const int ls = route_row_stride(p.E);
+    float* lg = reinterpret_cast<float*>(smem);  // [128][ls] logits
+    float* xch = lg + (size_t)kRouteTokens * ls;
+    const int nch = epad / 16;
     if (ks == 1) {
-      route_epilogue_k(p, c, tile, nt, [&](int ch, float* v) { tmem_ld16(lane_addr + ch * 16, v); });
+      // TMEM -> shared: warps w and w + 4 share TMEM lanes, each takes half the chunks
+      const int m = (warp & 3) * 32 + (threadIdx.x & 31);
+      const int c0 = (warp >> 2) * ((nch + 1) / 2), c1 = (warp >> 2) ? nch : (nch + 1) / 2;
+      float4* dst = reinterpret_cast<float4*>(lg + (size_t)m * ls);
+      for (int ch = c0; ch < c1; ++ch) {
+        float v[16];
+        tmem_ld16(lane_addr + ch * 16, v);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          dst[ch * 4 + q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      }
+      tc_fence_before();
+      cta_sync();
+      route_epilogue_k(p, c, tile, nt, lg, ls, xch);
       tile_done = true;
     } else {
       // partial logits of this split: [tile][split][128][epad] fp32
@@ -1168,7 +1329,7 @@ __device__ bool route_task(const Params& p, const Maps& maps, int tile, int spli
         const int m = warp * 32 + (threadIdx.x & 31);
         float4* dst = reinterpret_cast<float4*>(
             p.rpart + (((size_t)tile * ks + split) * kRouteTokens + m) * epad);
-        for (int ch = 0; ch * 16 < epad; ++ch) {
+        for (int ch = 0; ch < nch; ++ch) {
           float v[16];
           tmem_ld16(lane_addr + ch * 16, v);
 #pragma unroll
@@ -1179,32 +1340,45 @@ __device__ bool route_task(const Params& p, const Maps& maps, int tile, int spli
       tc_fence_before();
       release_writes();
       if (threadIdx.x == 0) c->flag = atom_add_acq_rel(p.rsplit_done + tile, 1) + 1 == ks;
-      __syncthreads();
+      cta_sync();
       if (c->flag) {
         fence_acq_rel_gpu();
-        // sum the splits into shared memory [128][epad], all threads, split order
-        float* sum = reinterpret_cast<float*>(smem);
+        // sum the splits into the shared logits, in split order: each thread
+        // owns up to 16 float4 of the tile per round and loads that slice of
+        // every split in turn (16 independent loads in flight per thread)
         const float4* src = reinterpret_cast<const float4*>(p.rpart + (size_t)tile * ks * kRouteTokens * epad);
-        const int n4 = kRouteTokens * epad / 4;
-        for (int i = threadIdx.x; i < n4; i += kThreads) {
-          float4 v[kMaxRouteKs];
+        const int r4 = epad / 4, n4 = kRouteTokens * r4;
+        constexpr int kPer = 16;
+        for (int base = 0; base < n4; base += kPer * kThreads) {
+          float4 acc[kPer];
 #pragma unroll
-          for (int s2 = 0; s2 < kMaxRouteKs; ++s2)
-            if (s2 < ks) v[s2] = __ldcg(src + (size_t)s2 * n4 + i);
-          float4 a = v[0];
+          for (int u = 0; u < kPer; ++u) {
+            const int i = base + u * kThreads + threadIdx.x;
+            acc[u] = i < n4 ? __ldcg(src + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+          for (int s2 = 1; s2 < ks; ++s2) {
+            float4 v[kPer];
 #pragma unroll
-          for (int s2 = 1; s2 < kMaxRouteKs; ++s2)
-            if (s2 < ks) {
-              a.x += v[s2].x; a.y += v[s2].y; a.z += v[s2].z; a.w += v[s2].w;
+            for (int u = 0; u < kPer; ++u) {
+              const int i = base + u * kThreads + threadIdx.x;
+              v[u] = i < n4 ? __ldcg(src + (size_t)s2 * n4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
-          reinterpret_cast<float4*>(sum)[i] = a;
-        }
-        __syncthreads();
-        const int m = (warp & 3) * 32 + (threadIdx.x & 31);
-        route_epilogue_k(p, c, tile, nt, [&](int ch, float* v) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] = sum[m * epad + ch * 16 + i];
-        });
+            for (int u = 0; u < kPer; ++u) {
+              acc[u].x += v[u].x; acc[u].y += v[u].y; acc[u].z += v[u].z; acc[u].w += v[u].w;
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < kPer; ++u) {
+            const int i = base + u * kThreads + threadIdx.x;
+            if (i < n4) {
+              const int rw = i / r4;
+              reinterpret_cast<float4*>(lg + (size_t)rw * ls)[i - rw * r4] = acc[u];
+            }
+          }
+        }
+        cta_sync();
+        route_epilogue_k(p, c, tile, nt, lg, ls, xch);
         tile_done = true;
       }
     }
@@ -1215,8 +1389,11 @@ __device__ bool route_task(const Params& p, const Maps& maps, int tile, int spli
 }
 
 // ------------------------------------------------------------------ notifications
-// (persistent mode) Called by all threads after a task; bumps the dependency
-// counters the task feeds and pushes the tasks that became ready.
+// (persistent mode) Run by the scheduler warp, all 32 lanes, after the
+// compute warps handed a finished task over (their writes were released to
+// this warp at CTA scope; sched_notify makes them visible at GPU scope
+// first).  They bump the dependency counters the task feeds and push the
+// tasks that became ready, while the compute warps already run the next task.
 
 __device__ __forceinline__ bool drop_for_fault(const Params& p) {
   if (p.fault_drop < 0) return false;
@@ -1230,58 +1407,56 @@ __device__ __forceinline__ bool drop_for_fault(const Params& p) {
 //    expert become ready in one wide burst;
 //  - kReleaseExpert: when the last gather of an expert is done, its tiles are
 //    pushed (f-tile major across its sibling groups).
-__device__ void notify_gather_done(const Params& p, int g, Ctrl* c) {
-  release_writes();
+__device__ void notify_gather_done(const Params& p, int g) {
+  const int lane = threadIdx.x & 31;
   const Group G = load_group(p, g);
   if (p.release == kReleaseAll) {
-    if (threadIdx.x == 0) {
+    int last = 0, nr = 0;
+    if (lane == 0) {
       const int old = atom_add_acq_rel(&p.sched->gathers_done, 1);
-      c->flag = (old + 1 == ld_relaxed(&p.sched->n_gather));
-      c->ival[0] = ld_relaxed(&p.sched->n_groups) - p.n_shared_groups;
+      last = (old + 1 == ld_relaxed(&p.sched->n_gather));
+      nr = ld_relaxed(&p.sched->n_groups) - p.n_shared_groups;
     }
-    __syncthreads();
-    if (c->flag) {
-      const int nr = c->ival[0], nf = p.n_ftiles, ns0 = p.n_shared_groups;
-      push_gen_block(p, gemm_queue(p), nr * nf, [=](int i) {
+    last = __shfl_sync(0xffffffffu, last, 0);
+    nr = __shfl_sync(0xffffffffu, nr, 0);
+    if (last) {
+      const int nf = p.n_ftiles, ns0 = p.n_shared_groups;
+      push_gen_warp(p, gemm_queue(p), nr * nf, [=](int i) {
         return task_id(kTaskGateUp, (ns0 + i % nr) * nf + i / nr);
-      }, c);
+      });
     }
     return;
   }
-  if (threadIdx.x < 32) {
-    int ready = 0;
-    if (threadIdx.x == 0) {
-      const int old = atom_add_acq_rel(p.gather_done + G.sib0, 1);
-      ready = (old + 1 == G.gchunks);
-    }
-    ready = __shfl_sync(0xffffffffu, ready, 0);
-    if (ready) {
-      const int nf = p.n_ftiles, ns = G.nsib, s0 = G.sib0;
-      push_gen_warp(p, gemm_queue(p), ns * nf, [=](int i) {
-        return task_id(kTaskGateUp, (s0 + i % ns) * nf + i / ns);
-      });
-    }
+  int ready = 0;
+  if (lane == 0) {
+    const int old = atom_add_acq_rel(p.gather_done + G.sib0, 1);
+    ready = (old + 1 == G.gchunks);
+  }
+  ready = __shfl_sync(0xffffffffu, ready, 0);
+  if (ready) {
+    const int nf = p.n_ftiles, ns = G.nsib, s0 = G.sib0;
+    push_gen_warp(p, gemm_queue(p), ns * nf, [=](int i) {
+      return task_id(kTaskGateUp, (s0 + i % ns) * nf + i / ns);
+    });
   }
 }
 
 // All gate/up tiles of an expert done: release its down tiles, interleaved
 // the same way.
 __device__ void notify_gateup_done(const Params& p, int g) {
-  release_writes();
-  if (threadIdx.x < 32) {
-    int ready = 0;
-    const Group G = load_group(p, g);
-    if (threadIdx.x == 0 && !drop_for_fault(p)) {
-      const int old = atom_add_acq_rel(p.gu_done + G.sib0, 1);
-      ready = (old + 1 == G.nsib * p.n_ftiles);
-    }
-    ready = __shfl_sync(0xffffffffu, ready, 0);
-    if (ready) {
-      const int nd = p.n_dtiles * p.ks, ns = G.nsib, s0 = G.sib0;
-      push_gen_warp(p, gemm_queue(p), ns * nd, [=](int i) {
-        return task_id(kTaskDown, (s0 + i % ns) * nd + i / ns);
-      });
-    }
+  const int lane = threadIdx.x & 31;
+  const Group G = load_group(p, g);
+  int ready = 0;
+  if (lane == 0 && !drop_for_fault(p)) {
+    const int old = atom_add_acq_rel(p.gu_done + G.sib0, 1);
+    ready = (old + 1 == G.nsib * p.n_ftiles);
+  }
+  ready = __shfl_sync(0xffffffffu, ready, 0);
+  if (ready) {
+    const int nd = p.n_dtiles * p.ks, ns = G.nsib, s0 = G.sib0;
+    push_gen_warp(p, gemm_queue(p), ns * nd, [=](int i) {
+      return task_id(kTaskDown, (s0 + i % ns) * nd + i / ns);
+    });
   }
 }
 
@@ -1292,31 +1467,46 @@ __device__ __forceinline__ int comb_target(const Params& p, int ctile) {
   return nt * (p.k + p.S) * p.n_dtiles * p.ks;
 }
 
-__device__ void notify_down_done(const Params& p, int g, Ctrl* c) {
-  release_writes();
-  if (threadIdx.x == 0) c->flag = drop_for_fault(p) ? 1 : 0;
+// A down tile finished: every combine tile its rows belong to gains those
+// rows.  The group's tokens ascend, so its rows form runs of one combine tile
+// each; every run (cut at 32-row chunk boundaries) is one counter add, and
+// the add that reaches the target pushes the combine task.
+__device__ void notify_down_done(const Params& p, int g) {
+  const int lane = threadIdx.x & 31;
+  int drop = lane == 0 ? (drop_for_fault(p) ? 1 : 0) : 0;
+  if (__shfl_sync(0xffffffffu, drop, 0)) return;
   const Group G = load_group(p, g);
-  // combine tile of every row of the group (tokens ascending inside a group)
-  const int tid = threadIdx.x;
-  if (tid < G.nrows) {
-    const int t = G.e < p.E ? __ldcg(p.perm + G.row0 + tid) : G.src_row0 + tid;
-    c->tok[tid] = t / p.ct;
-  }
-  __syncthreads();
-  if (c->flag) return;
-  if (tid < G.nrows && (tid == 0 || c->tok[tid] != c->tok[tid - 1])) {
-    const int ct = c->tok[tid];
-    int len = 1;
-    while (tid + len < G.nrows && c->tok[tid + len] == ct) ++len;
-    const int old = atom_add_acq_rel(p.comb_done + ct, len);
-    if (old + len == comb_target(p, ct)) {
-      const QueueRef q = mover_queue(p);
-      const int j = push_start(ct);
-      const int slot = (int)(atomicAdd(q.word + j, 1ull << 32) >> 32);
-      if (slot < q.seg) st_release(q.ring + j * q.seg + slot, task_id(kTaskCombine, ct) + 1);
-      else set_status(p, MOE_E_DEVICE, 5);
+  const bool routed = G.e < p.E;
+  for (int r0 = 0; r0 < G.nrows; r0 += 32) {
+    const int r = r0 + lane;
+    const bool in = r < G.nrows;
+    int ct = -1;
+    if (in) ct = (routed ? __ldcg(p.perm + G.row0 + r) : G.src_row0 + r) / p.ct;
+    const int up = __shfl_up_sync(0xffffffffu, ct, 1);
+    const bool start = in && (lane == 0 || ct != up);
+    const unsigned starts = __ballot_sync(0xffffffffu, start);
+    if (start) {
+      const unsigned after = lane == 31 ? 0u : (starts >> (lane + 1));
+      const int len = after ? __ffs(after) : min(32, G.nrows - r0) - lane;
+      const int old = atom_add_acq_rel(p.comb_done + ct, len);
+      if (old + len == comb_target(p, ct)) {
+        const QueueRef q = mover_queue(p);
+        const int j = push_start(ct);
+        const int slot = (int)(atomicAdd(q.word + j, 1ull << 32) >> 32);
+        if (slot < q.seg) st_release(q.ring + j * q.seg + slot, task_id(kTaskCombine, ct) + 1);
+        else set_status(p, MOE_E_DEVICE, 5);
+      }
     }
   }
+}
+
+// The notification of one finished task (any type; router tiles and combines
+// feed no counter here).
+__device__ void sched_notify(const Params& p, int task) {
+  const int type = task_type(task), pl = task_payload(task);
+  if (type == kTaskGather) notify_gather_done(p, pl >> 3);
+  else if (type == kTaskGateUp) notify_gateup_done(p, pl / p.n_ftiles);
+  else if (type == kTaskDown) notify_down_done(p, pl / (p.n_dtiles * p.ks));
 }
 
 }  // namespace moe
