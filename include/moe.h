@@ -91,6 +91,11 @@ typedef struct moe_layer moe_layer_t;
 #define MOE_OPT_PREFETCH 12    /* 1 (default): while a GEMM tile finishes, the
                                   TMA producer starts loading the next tile
                                   claimed ahead; 0: off                        */
+#define MOE_OPT_BANDS 13       /* 1 (default): the down tiles of the last
+                                  quarter of d run at low priority and the
+                                  combine is split in two d bands, so the
+                                  first band's combine overlaps them; 0: one
+                                  band                                         */
 
 /* statistics keys for moe_layer_get_stat (values of the last forward;
  * moe_layer_status must have been called after it) */

@@ -82,7 +82,9 @@ struct Sched {
   int stat_ahead;
   int n_gather;         // gather tasks pushed by the plan (mover slots after the router tasks)
   int gathers_done;
-  int pad[11];
+  int gemm_lo_total_dyn;  // low-priority GEMM tasks (the last d band's down tiles)
+  unsigned long long gemm_lo_q[kShards];
+  int pad[10];
 };
 
 struct Params {
@@ -103,7 +105,9 @@ struct Params {
   int release;       // kReleaseAll or kReleaseExpert
   int prefetch;      // producer starts the next claimed GEMM tile's loads early
   int ct;            // tokens per combine tile
-  int n_comb;        // combine tiles
+  int n_comb;        // combine tasks: combine tiles x d bands
+  int n_bands;       // d bands of the down tiles and the combines (1 or 2)
+  int dt_lo0;        // first d tile of the last band, whose down tiles have low priority
   int n_shared_groups;
   int n_static_gemm; // shared-expert gate/up tasks, ready at launch
   int y_f32;         // Y holds fp32 partial sums [ks][rows][d]; else bf16 [rows][d]
@@ -145,6 +149,7 @@ struct Params {
   int* comb_done;    // [n_comb]
   int* ring_mover;   // [kShards][mover_seg] task id + 1, 0 = not yet pushed
   int* ring_gemm;    // [kShards][gemm_seg]  task id + 1, 0 = not yet pushed
+  int* ring_gemm_lo; // [kShards][gemm_seg]  the low-priority GEMM queue
   Sched* sched;
   float* rpart;      // [n_route][route_ks][128][E padded to 16] partial router logits
   int* rsplit_done;  // [n_route] router K splits finished

@@ -479,6 +479,7 @@ struct moe_layer {
   int ahead_opt = -1;
   int release = kReleaseExpert;
   int prefetch = 1;
+  int bands = 1;
   int trace_cap = 0;
   unsigned long long* trace = nullptr;
   const float* bias = nullptr;
@@ -488,7 +489,7 @@ struct moe_layer {
   Bounds B{};
   // offsets into ws
   size_t o_idx, o_wgt, o_rank, o_tile, o_counts, o_offsets, o_perm, o_pos, o_xp, o_h, o_y,
-      o_groups, o_rpart, o_rsd, o_rmask, o_zero, o_gd, o_gu, o_cd, o_sched, o_zero_end, o_ring, o_ring_m, o_ring_g,
+      o_groups, o_rpart, o_rsd, o_rmask, o_zero, o_gd, o_gu, o_cd, o_sched, o_zero_end, o_ring, o_ring_m, o_ring_g, o_ring_gl,
       o_ring_end;
   // host staging for moe_layer_forward_host
   void* x_dev_stage = nullptr;
@@ -509,7 +510,7 @@ Bounds make_bounds(const moe_layer* h, int T) {
   b.n_route = std::max(1, cdiv(T, kRouteTokens));
   const int shared_groups = h->S ? cdiv(T, 32) : 0;
   b.max_groups = shared_groups + cdiv(Tk, 32) + std::min<long long>(h->E, Tk) + 1;
-  b.n_comb = std::max(T, 1);
+  b.n_comb = 2 * std::max(T, 1);  // one token per tile, two d bands
   b.mover_cap = cdiv(Tk, 32) + b.max_groups + b.n_comb + 16;
   const int n_ft = h->f / 128, n_dt = cdiv(h->d, 256);
   b.gemm_cap = b.max_groups * (n_ft + n_dt * 4) + 16;
@@ -553,6 +554,7 @@ void layout(moe_layer* h, const Bounds& b) {
   h->o_ring = o;
   h->o_ring_m = take((size_t)kShards * (b.mover_cap / kShards * 2 + 64) * 4);
   h->o_ring_g = take((size_t)kShards * (b.gemm_cap / kShards * 2 + 64) * 4);
+  h->o_ring_gl = take((size_t)kShards * (b.gemm_cap / kShards * 2 + 64) * 4);
   h->o_ring_end = o;
   h->ws_bytes = o;
 }
@@ -771,6 +773,9 @@ int moe_layer_set_option(moe_layer_t* h, int key, long long v) {
     case MOE_OPT_PREFETCH:
       h->prefetch = v ? 1 : 0;
       break;
+    case MOE_OPT_BANDS:
+      h->bands = v ? 1 : 0;
+      break;
     case MOE_OPT_ROUTE_TOKENS:
       if (v != 0 && v != kRouteTokens) return fail(MOE_E_INVAL, "router tiles are 128 tokens");
       h->rt_opt = (int)v;
@@ -826,7 +831,11 @@ int moe_layer_forward(moe_layer_t* h, int T, const void* x, const void* router_w
   p.release = h->release;
   p.prefetch = h->prefetch;
   p.ct = tl.ct;
-  p.n_comb = cdiv(T, tl.ct);
+  // d bands: the down tiles of the last quarter of d (at least one tile)
+  // have low priority, so the other band's combines overlap them
+  p.n_bands = (h->bands && p.n_dtiles >= 2) ? 2 : 1;
+  p.dt_lo0 = p.n_bands == 2 ? p.n_dtiles - std::max(1, p.n_dtiles / 4) : p.n_dtiles;
+  p.n_comb = cdiv(T, tl.ct) * p.n_bands;
   p.n_shared_groups = h->S ? cdiv(T, tl.bn) : 0;
   p.n_static_gemm = p.n_shared_groups * p.n_ftiles;
   p.y_f32 = tl.y_f32;
@@ -867,6 +876,7 @@ int moe_layer_forward(moe_layer_t* h, int T, const void* x, const void* router_w
   p.comb_done = reinterpret_cast<int*>(w + h->o_cd);
   p.ring_mover = reinterpret_cast<int*>(w + h->o_ring_m);
   p.ring_gemm = reinterpret_cast<int*>(w + h->o_ring_g);
+  p.ring_gemm_lo = reinterpret_cast<int*>(w + h->o_ring_gl);
   p.sched = reinterpret_cast<Sched*>(w + h->o_sched);
   p.rpart = reinterpret_cast<float*>(w + h->o_rpart);
   p.rsplit_done = reinterpret_cast<int*>(w + h->o_rsd);

@@ -56,7 +56,7 @@ struct CtaState {
   int exit_reason;        // why claim_next gave up (trace only): 1 done, 2 abort, 3 deadline
   unsigned polls;         // claim attempts of thread 0 that found nothing (trace only)
   bool plan_seen;         // the plan's totals below are cached
-  int n_gather, mover_total, gemm_total;
+  int n_gather, mover_total, gemm_total, gemm_lo_total;
   int pf_task, pf_count;  // producer: task whose first k blocks are already loading
   int taken;              // compute thread 0: tasks taken from the mailbox
 };
@@ -162,6 +162,12 @@ __device__ __forceinline__ Group load_group(const Params& p, int g) {
   return Group{a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 }
 
+// d tiles [dt0, dt1) of d band `band` (down tiles of 256 rows of d each).
+__device__ __forceinline__ int band_dt0(const Params& p, int band) { return band ? p.dt_lo0 : 0; }
+__device__ __forceinline__ int band_dt1(const Params& p, int band) {
+  return (p.n_bands == 2 && band == 0) ? p.dt_lo0 : p.n_dtiles;
+}
+
 __device__ __forceinline__ bool group_ok(const Params& p, const Group& G) {
   return G.nrows >= 1 && G.nrows <= p.bn_max && G.e >= 0 && G.e <= p.E && G.row0 >= 0 &&
          G.row0 + G.nrows <= p.rows_y && G.nsib >= 1 && G.sib0 >= 0 &&
@@ -169,11 +175,12 @@ __device__ __forceinline__ bool group_ok(const Params& p, const Group& G) {
 }
 
 // ------------------------------------------------------------------ queues
-// Two task queues (movers: router tiles, gathers, combines; GEMM workers:
-// gate/up and down tiles), each split into kShards shards.  A shard is one
+// Three task queues (movers: router tiles, gathers, combines; GEMM workers:
+// gate/up and down tiles; low priority: the last d band's down tiles), each
+// split into kShards shards.  A shard is one
 // 64-bit word -- claims so far (low 32 bits) and dynamic pushes (high 32 bits)
 // -- plus a ring segment.  Pushes spread their tasks round-robin over the
-// shards; a warp claims by loading every shard word of both queues at once
+// shards; a warp claims by loading every shard word of every queue at once
 // and CAS-ing the word of one shard with work, starting at its home shard
 // (blockIdx mod kShards) -- the per-SM local queues with stealing of
 // xxqk.cn/news/665650 section 4.4 (pitfall 3), each shared by a few CTAs.
@@ -197,6 +204,13 @@ __device__ __forceinline__ QueueRef mover_queue(const Params& p) {
 
 __device__ __forceinline__ QueueRef gemm_queue(const Params& p) {
   return QueueRef{p.sched->gemm_q, p.ring_gemm, p.n_static_gemm, p.gemm_seg};
+}
+
+// Low-priority GEMM queue: the down tiles of the last d band, taken when the
+// GEMM queue is empty, so the combines of the other bands can start while
+// these still run.
+__device__ __forceinline__ QueueRef gemm_lo_queue(const Params& p) {
+  return QueueRef{p.sched->gemm_lo_q, p.ring_gemm_lo, 0, p.gemm_seg};
 }
 
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
@@ -297,22 +311,23 @@ __device__ __forceinline__ int warp_sum_i(int v) {
 }
 
 // One scheduling decision, by a whole warp: the preferred queue first, then
-// the other one.  Returns a task id (the same on every lane), -1 if nothing
-// is claimable now, -2 if both queues are finished, -3 to abort, -4 to retry
-// at once (a CAS was lost).  `min_depth` > 1 claims ahead: only from the
+// the other ones.  Returns a task id (the same on every lane), -1 if nothing
+// is claimable now, -2 if every queue is finished, -3 to abort, -4 to retry
+// at once (the CAS kept losing).  `min_depth` > 1 claims ahead: only from the
 // first-choice queue and only when it holds at least that many tasks.
 __device__ int claim_once(const Params& p, CtaState& st, int min_depth) {
   const int lane = threadIdx.x & 31;
   const unsigned full = 0xffffffffu;
   Sched* s = p.sched;
   if (!st.plan_seen) {  // lane 0 reads, every lane takes its values: decisions stay uniform
-    int seen = 0, nm = 0, ng = 0, mt = 0, gt = 0;
+    int seen = 0, nm = 0, ng = 0, mt = 0, gt = 0, lt = 0;
     if (lane == 0 && ld_acquire(&s->plan_done) != 0) {
       seen = 1;
       nm = ld_relaxed(&s->n_movers);
       ng = ld_relaxed(&s->n_gather);
       mt = ld_relaxed(&s->mover_total_dyn);
       gt = ld_relaxed(&s->gemm_total_dyn);
+      lt = ld_relaxed(&s->gemm_lo_total_dyn);
     }
     if (__shfl_sync(full, seen, 0)) {
       st.plan_seen = true;
@@ -320,53 +335,70 @@ __device__ int claim_once(const Params& p, CtaState& st, int min_depth) {
       st.n_gather = __shfl_sync(full, ng, 0);
       st.mover_total = __shfl_sync(full, mt, 0);
       st.gemm_total = __shfl_sync(full, gt, 0);
+      st.gemm_lo_total = __shfl_sync(full, lt, 0);
     }
   }
-  const QueueRef mq = mover_queue(p), gq = gemm_queue(p);
-  // lanes 0..7: the mover queue's shards, lanes 8..15: the GEMM queue's
-  const bool mine = lane < 2 * kShards;
-  const bool is_m = lane < kShards;
+  // lanes 0-7: the mover queue's shards, 8-15: the GEMM queue's, 16-23: the
+  // low-priority GEMM queue's (lanes 24-31 idle)
+  const int qi = lane >> 3;
+  const bool mine = qi < 3;
   const int j = lane & (kShards - 1);
+  const QueueRef q = qi == 0 ? mover_queue(p) : qi == 1 ? gemm_queue(p) : gemm_lo_queue(p);
   unsigned long long w = 0;
-  if (mine) w = ld_acquire_u64((is_m ? mq.word : gq.word) + j);
-  const int nst = mine ? shard_static(is_m ? mq.n_static : gq.n_static, j) : 0;
+  if (mine) w = ld_acquire_u64(q.word + j);
+  const int nst = mine ? shard_static(q.n_static, j) : 0;
   const int h = (int)(w & 0xffffffffu);
   const int avail = nst + (int)(w >> 32);
-  const int claimed_m = warp_sum_i(mine && is_m ? h : 0);
-  const int claimed_g = warp_sum_i(mine && !is_m ? h : 0);
-  const int depth_m = warp_sum_i(mine && is_m ? max(avail - h, 0) : 0);
-  const int depth_g = warp_sum_i(mine && !is_m ? max(avail - h, 0) : 0);
+  const int claimed_m = warp_sum_i(qi == 0 ? h : 0);
+  const int claimed_g = warp_sum_i(qi == 1 ? h : 0);
+  const int claimed_l = warp_sum_i(qi == 2 ? h : 0);
+  const int dep = mine ? max(avail - h, 0) : 0;
+  const int depth_m = warp_sum_i(qi == 0 ? dep : 0);
+  const int depth_g = warp_sum_i(qi == 1 ? dep : 0);
+  const int depth_l = warp_sum_i(qi == 2 ? dep : 0);
+  const unsigned ball = __ballot_sync(full, mine && h < avail);
   const bool gathers_left = st.plan_seen && claimed_m < p.n_route_tasks + st.n_gather;
   // Before the plan every CTA prefers router tiles, and afterwards every CTA
   // prefers gathers while any is unclaimed: both gate all the GEMM work.
-  // Otherwise each CTA prefers its own role's queue and steals from the other.
+  // Otherwise a mover CTA takes mover, GEMM, low-priority GEMM work in that
+  // order, a GEMM CTA GEMM, low-priority GEMM, mover work.
   const bool mover_first = !st.plan_seen || gathers_left || st.role_mover;
-  const int npass = min_depth > 1 ? 1 : 2;
+  const int npass = min_depth > 1 ? 1 : 3;
   const int home = (int)blockIdx.x & (kShards - 1);
   for (int pass = 0; pass < npass; ++pass) {
-    const bool use_m = (pass == 0) == mover_first;
-    const int depth = use_m ? depth_m : depth_g;
+    const int qq = mover_first ? pass : (pass == 2 ? 0 : pass + 1);
+    const int depth = qq == 0 ? depth_m : qq == 1 ? depth_g : depth_l;
     if (depth < max(min_depth, 1)) continue;
-    const unsigned ball = __ballot_sync(full, mine && is_m == use_m && h < avail);
-    const unsigned sm = (use_m ? ball : (ball >> kShards)) & ((1u << kShards) - 1u);
+    const unsigned sm = (ball >> (qq * kShards)) & ((1u << kShards) - 1u);
     if (!sm) continue;
     // first shard with work at or after the home shard
     const unsigned rot = ((sm >> home) | (sm << (kShards - home))) & ((1u << kShards) - 1u);
     const int pick = (home + __ffs(rot) - 1) & (kShards - 1);
-    const int plane = (use_m ? 0 : kShards) + pick;
+    const int plane = qq * kShards + pick;
     int r = -4;
     if (lane == plane) {
-      const QueueRef& q = use_m ? mq : gq;
-      const unsigned long long seen = atomicCAS(q.word + pick, w, w + 1);
-      if (seen == w) r = resolve_slot(p, q, use_m, pick, h, st.deadline);
+      // a lost CAS returns the word's current value: retry on it at once
+      // while the shard still holds work (no reload of the other words)
+      unsigned long long cur = w;
+      for (int attempt = 0; attempt < 8; ++attempt) {
+        const unsigned long long seen = atomicCAS(q.word + pick, cur, cur + 1);
+        if (seen == cur) {
+          r = resolve_slot(p, q, qq == 0, pick, (int)(cur & 0xffffffffu), st.deadline);
+          break;
+        }
+        cur = seen;
+        if ((int)(cur & 0xffffffffu) >= nst + (int)(cur >> 32)) break;  // drained
+      }
     }
     r = __shfl_sync(full, r, plane);
-    if (r >= 0 && pass == 1 && st.plan_seen && lane == 0) atomicAdd(&s->stat_stolen, 1);
-    return r;  // a task, -3, or -4 (lost the CAS: retry)
+    if (r >= 0 && pass > 0 && st.plan_seen && lane == 0) atomicAdd(&s->stat_stolen, 1);
+    return r;  // a task, -3, or -4 (the shard drained under us: retry)
   }
+  const QueueRef mq = mover_queue(p), gq = gemm_queue(p);
   const bool fin_m = st.plan_seen && claimed_m >= mq.n_static + st.mover_total;
   const bool fin_g = st.plan_seen && claimed_g >= gq.n_static + st.gemm_total;
-  if (npass == 2 && fin_m && fin_g) return -2;
+  const bool fin_l = st.plan_seen && claimed_l >= st.gemm_lo_total;
+  if (npass == 3 && fin_m && fin_g && fin_l) return -2;
   const int bad = lane == 0 ? ld_relaxed(&s->status) : 0;
   if (__shfl_sync(full, bad, 0) != 0) return -3;
   return -1;
@@ -551,9 +583,11 @@ __device__ void plan_task(const Params& p, char* scratch, Ctrl* c, bool push) {
   if (tid == 0) {
     const int n_groups = p.n_shared_groups + n_routed;
     const int n_down = p.n_dtiles * p.ks;
+    const int n_down_lo = p.n_bands == 2 ? (p.n_dtiles - p.dt_lo0) * p.ks : 0;
     Sched* s = p.sched;
     s->n_groups = n_groups;
-    s->gemm_total_dyn = n_routed * p.n_ftiles + n_groups * n_down;
+    s->gemm_total_dyn = n_routed * p.n_ftiles + n_groups * (n_down - n_down_lo);
+    s->gemm_lo_total_dyn = n_groups * n_down_lo;
     s->mover_total_dyn = n_gather + p.n_comb;
     s->n_gather = n_gather;
     int movers;
@@ -672,11 +706,14 @@ __device__ void gather_task(const Params& p, int g, int chunk, char* smem, Ctrl*
 }
 
 // ------------------------------------------------------------------ combine (mover)
-// Combine straight from global memory (rows too large for shared memory).
-__device__ void combine_direct(const Params& p, int t0, int nt, Ctrl* c) {
+// Combine straight from global memory (rows too large for shared memory):
+// columns [c0, c0 + 8 * nvec) of tokens [t0, t0 + nt).
+__device__ void combine_direct(const Params& p, int t0, int nt, int c0, int nvec, Ctrl* c) {
   const int k = p.k, nsrc = k + p.S;
-  const int nvec = p.d >> 3;
-  uint4* out = reinterpret_cast<uint4*>(p.out);
+  const int dvec = p.d >> 3;
+  uint4* out = reinterpret_cast<uint4*>(p.out) + (c0 >> 3);
+  const float* Yf = reinterpret_cast<const float*>(p.Y) + c0;
+  const uint4* Yb = reinterpret_cast<const uint4*>(p.Y) + (c0 >> 3);
   const size_t part = (size_t)p.rows_y * p.d;
   for (int i = threadIdx.x; i < nt * nvec; i += kThreads) {
     const int t = i / nvec, q = i - t * nvec;
@@ -688,32 +725,36 @@ __device__ void combine_direct(const Params& p, int t0, int nt, Ctrl* c) {
       const float w = j < k ? c->wsum[t * k + j] : 1.f;
       float y[8];
       if (p.y_f32) {
-        const float* Y = reinterpret_cast<const float*>(p.Y);
 #pragma unroll
         for (int u = 0; u < 8; ++u) y[u] = 0.f;
         for (int s = 0; s < p.ks; ++s) {
           const float4* src =
-              reinterpret_cast<const float4*>(Y + s * part + (size_t)row * p.d + q * 8);
+              reinterpret_cast<const float4*>(Yf + s * part + (size_t)row * p.d + q * 8);
           const float4 a = __ldcg(src), b = __ldcg(src + 1);
           y[0] += a.x; y[1] += a.y; y[2] += a.z; y[3] += a.w;
           y[4] += b.x; y[5] += b.y; y[6] += b.z; y[7] += b.w;
         }
       } else {
-        bf16x8_to_f32(__ldcg(reinterpret_cast<const uint4*>(p.Y) + (size_t)row * nvec + q), y);
+        bf16x8_to_f32(__ldcg(Yb + (size_t)row * dvec + q), y);
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) acc[u] = fmaf(w, y[u], acc[u]);
     }
-    out[(size_t)(t0 + t) * nvec + q] = f32x8_to_bf16(acc);
+    out[(size_t)(t0 + t) * dvec + q] = f32x8_to_bf16(acc);
   }
 }
 
 // out[t, :] = bf16( sum_j w[t,j] * Y[pos[t,j], :] + Y[T k + t, :] (shared) ),
 // fp32 sum in slot order, then the shared expert; with fp32 K-split partials
-// each source row is the sum of its splits.  The source rows of a few tokens
-// at a time are bulk-copied into one half of the pipeline's shared memory
-// while the other half is being summed (double buffering).
-__device__ void combine_task(const Params& p, int ctile, char* smem, Ctrl* c, CtaState& st) {
+// each source row is the sum of its splits.  One task covers a tile of
+// tokens and one d band (the columns of the band's down tiles).  The source
+// rows of a few tokens at a time are bulk-copied into one half of the
+// pipeline's shared memory while the other half is being summed (double
+// buffering).
+__device__ void combine_task(const Params& p, int ci, char* smem, Ctrl* c, CtaState& st) {
+  const int ctile = ci / p.n_bands, band = ci - ctile * p.n_bands;
+  const int c0 = band_dt0(p, band) * 2 * kBM;
+  const int c1 = min(p.d, band_dt1(p, band) * 2 * kBM);
   const int t0 = ctile * p.ct;
   const int nt = min(p.ct, p.T - t0);
   const int k = p.k;
@@ -725,12 +766,12 @@ __device__ void combine_task(const Params& p, int ctile, char* smem, Ctrl* c, Ct
   const int nsrc = k + p.S;
   const int nsplit = p.y_f32 ? p.ks : 1;
   const int ebytes = p.y_f32 ? 4 : 2;
-  const uint32_t row_bytes = (uint32_t)p.d * ebytes;
+  const uint32_t row_bytes = (uint32_t)(c1 - c0) * ebytes;  // one source row's band
   const size_t per_tok = (size_t)nsrc * nsplit * row_bytes;
   const size_t mem = (size_t)p.stages * p.stage_bytes;
   if (per_tok > mem) {  // one token's rows do not fit: sum straight from global
     if (threadIdx.x == 0) st_release_cta_shared(&c->mb_late, st.taken);
-    combine_direct(p, t0, nt, c);
+    combine_direct(p, t0, nt, c0, (c1 - c0) >> 3, c);
     return;
   }
   const int nbuf = per_tok * 2 <= mem ? 2 : 1;
@@ -738,7 +779,8 @@ __device__ void combine_task(const Params& p, int ctile, char* smem, Ctrl* c, Ct
   const int tpr = (int)(half / per_tok);   // tokens per round
   const int rounds = (nt + tpr - 1) / tpr;
   const size_t part_bytes = (size_t)p.rows_y * p.d * ebytes;
-  const char* Yb = reinterpret_cast<const char*>(p.Y);
+  const size_t y_row = (size_t)p.d * ebytes;
+  const char* Yb = reinterpret_cast<const char*>(p.Y) + (size_t)c0 * ebytes;
   auto issue = [&](int r) {  // thread 0: bulk loads of round r into buffer r % nbuf
     const int b = r % nbuf;
     const int ta = r * tpr, n = min(tpr, nt - ta);
@@ -750,7 +792,7 @@ __device__ void combine_task(const Params& p, int ctile, char* smem, Ctrl* c, Ct
         const int row = j < k ? c->tok[t * k + j] : p.T * k + t0 + t;
         for (int s = 0; s < nsplit; ++s)
           bulk_load(buf + ((size_t)(tt * nsrc + j) * nsplit + s) * row_bytes,
-                    Yb + s * part_bytes + (size_t)row * row_bytes, row_bytes, &c->cbar[b]);
+                    Yb + s * part_bytes + (size_t)row * y_row, row_bytes, &c->cbar[b]);
       }
     }
   };
@@ -759,8 +801,8 @@ __device__ void combine_task(const Params& p, int ctile, char* smem, Ctrl* c, Ct
     issue(0);
     if (nbuf == 2 && rounds > 1) issue(1);
   }
-  const int nvec = p.d >> 3;
-  uint4* out = reinterpret_cast<uint4*>(p.out);
+  const int nvec = (c1 - c0) >> 3, dvec = p.d >> 3;
+  uint4* out = reinterpret_cast<uint4*>(p.out) + (c0 >> 3);
   for (int r = 0; r < rounds; ++r) {
     const int b = r % nbuf;
     if (threadIdx.x == 0 && r == rounds - 1) st_release_cta_shared(&c->mb_late, st.taken);
@@ -797,7 +839,7 @@ __device__ void combine_task(const Params& p, int ctile, char* smem, Ctrl* c, Ct
 #pragma unroll
         for (int u = 0; u < 8; ++u) acc[u] = fmaf(w, y[u], acc[u]);
       }
-      out[(size_t)(t0 + t) * nvec + q] = f32x8_to_bf16(acc);
+      out[(size_t)(t0 + t) * dvec + q] = f32x8_to_bf16(acc);
     }
     cta_sync();  // buffer b is free again
     if (threadIdx.x == 0 && r + nbuf < rounds) issue(r + nbuf);
@@ -1452,29 +1494,38 @@ __device__ void notify_gateup_done(const Params& p, int g) {
     ready = (old + 1 == G.nsib * p.n_ftiles);
   }
   ready = __shfl_sync(0xffffffffu, ready, 0);
-  if (ready) {
+  if (ready) {  // bands before the last: GEMM queue; the last band: low priority
     const int nd = p.n_dtiles * p.ks, ns = G.nsib, s0 = G.sib0;
-    push_gen_warp(p, gemm_queue(p), ns * nd, [=](int i) {
+    const int nd_hi = p.n_bands == 2 ? p.dt_lo0 * p.ks : nd;
+    push_gen_warp(p, gemm_queue(p), ns * nd_hi, [=](int i) {
       return task_id(kTaskDown, (s0 + i % ns) * nd + i / ns);
     });
+    if (nd > nd_hi)
+      push_gen_warp(p, gemm_lo_queue(p), ns * (nd - nd_hi), [=](int i) {
+        return task_id(kTaskDown, (s0 + i % ns) * nd + nd_hi + i / ns);
+      });
   }
 }
 
-// Target of a combine tile's counter: every (token, slot) and shared row of
-// the tile, once per down task covering it.
-__device__ __forceinline__ int comb_target(const Params& p, int ctile) {
+// Target of the counter of combine task (ctile, band): every (token, slot)
+// and shared row of the tile, once per down task of the band covering it.
+__device__ __forceinline__ int comb_target(const Params& p, int ctile, int band) {
   const int nt = min(p.ct, p.T - ctile * p.ct);
-  return nt * (p.k + p.S) * p.n_dtiles * p.ks;
+  return nt * (p.k + p.S) * (band_dt1(p, band) - band_dt0(p, band)) * p.ks;
 }
 
-// A down tile finished: every combine tile its rows belong to gains those
-// rows.  The group's tokens ascend, so its rows form runs of one combine tile
-// each; every run (cut at 32-row chunk boundaries) is one counter add, and
-// the add that reaches the target pushes the combine task.
-__device__ void notify_down_done(const Params& p, int g) {
+// A down tile finished: every combine task of its d band whose token tile
+// holds some of its rows gains those rows.  The group's tokens ascend, so
+// its rows form runs of one combine tile each; every run (cut at 32-row
+// chunk boundaries) is one counter add, and the add that reaches the target
+// pushes the combine task.
+__device__ void notify_down_done(const Params& p, int task) {
   const int lane = threadIdx.x & 31;
   int drop = lane == 0 ? (drop_for_fault(p) ? 1 : 0) : 0;
   if (__shfl_sync(0xffffffffu, drop, 0)) return;
+  const int nd = p.n_dtiles * p.ks, pl = task_payload(task);
+  const int g = pl / nd, dt = (pl - g * nd) / p.ks;
+  const int band = (p.n_bands == 2 && dt >= p.dt_lo0) ? 1 : 0;
   const Group G = load_group(p, g);
   const bool routed = G.e < p.E;
   for (int r0 = 0; r0 < G.nrows; r0 += 32) {
@@ -1488,12 +1539,13 @@ __device__ void notify_down_done(const Params& p, int g) {
     if (start) {
       const unsigned after = lane == 31 ? 0u : (starts >> (lane + 1));
       const int len = after ? __ffs(after) : min(32, G.nrows - r0) - lane;
-      const int old = atom_add_acq_rel(p.comb_done + ct, len);
-      if (old + len == comb_target(p, ct)) {
+      const int ci = ct * p.n_bands + band;
+      const int old = atom_add_acq_rel(p.comb_done + ci, len);
+      if (old + len == comb_target(p, ct, band)) {
         const QueueRef q = mover_queue(p);
-        const int j = push_start(ct);
+        const int j = push_start(ci);
         const int slot = (int)(atomicAdd(q.word + j, 1ull << 32) >> 32);
-        if (slot < q.seg) st_release(q.ring + j * q.seg + slot, task_id(kTaskCombine, ct) + 1);
+        if (slot < q.seg) st_release(q.ring + j * q.seg + slot, task_id(kTaskCombine, ci) + 1);
         else set_status(p, MOE_E_DEVICE, 5);
       }
     }
@@ -1506,7 +1558,7 @@ __device__ void sched_notify(const Params& p, int task) {
   const int type = task_type(task), pl = task_payload(task);
   if (type == kTaskGather) notify_gather_done(p, pl >> 3);
   else if (type == kTaskGateUp) notify_gateup_done(p, pl / p.n_ftiles);
-  else if (type == kTaskDown) notify_down_done(p, pl / (p.n_dtiles * p.ks));
+  else if (type == kTaskDown) notify_down_done(p, task);
 }
 
 }  // namespace moe
