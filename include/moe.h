@@ -96,6 +96,16 @@ typedef struct moe_layer moe_layer_t;
                                   combine is split in two d bands, so the
                                   first band's combine overlaps them; 0: one
                                   band                                         */
+#define MOE_OPT_ROUTE_SPLITS 14 /* K splits of a router tile (1..8; 0 = auto:
+                                  enough to spread the tiles over the SMs)    */
+#define MOE_OPT_L2_PREFETCH 15 /* persistent mode: bytes of the first gate/up
+                                  weight tiles (experts in index order) to
+                                  prefetch into L2 once the router is done,
+                                  while the plan and gathers run; the plan
+                                  then keeps experts in index order.
+                                  0 (default) = off; -1 = 96 MiB when S = 0
+                                  and the mean expert load is at most half a
+                                  GEMM tile, else off                          */
 
 /* statistics keys for moe_layer_get_stat (values of the last forward;
  * moe_layer_status must have been called after it) */

@@ -22,7 +22,7 @@ MOE_MODE_PERSISTENT, MOE_MODE_MULTIKERNEL = 0, 1
 OPTIONS = {
     "mode": 1, "timeout_ns": 2, "mover_ctas": 3, "grid_ctas": 4, "split_k": 5,
     "tokens_per_tile": 6, "fault_drop_task": 7, "route_tokens": 8, "claim_ahead": 9,
-    "trace": 10, "release": 11, "prefetch": 12, "bands": 13,
+    "trace": 10, "release": 11, "prefetch": 12, "bands": 13, "route_splits": 14, "l2_prefetch": 15,
 }
 STATS = {"mover_ctas": 1, "tasks": 2, "grid": 3, "gemm_tasks": 4, "mover_tasks": 5, "stolen": 6,
          "ahead": 7, "trace_records": 8}

@@ -117,6 +117,8 @@ struct Params {
   int fault_drop;    // -1, or the index of the GEMM completion to drop
   int mover_override;
   int ahead_depth;   // claim the next task early when this many wait (0 = never)
+  int index_order;   // the plan keeps experts in index order (not by count)
+  long long l2_pf_bytes;  // gate/up weight bytes prefetched into L2 at launch (0 = none)
   int fa_depth;      // claims are fetch-and-adds when this many tasks wait
   unsigned long long timeout_ns;
   // cost model constants
@@ -127,6 +129,8 @@ struct Params {
   const __nv_bfloat16* x;
   const __nv_bfloat16* wr;
   const float* bias;
+  const __nv_bfloat16* w_gate;  // [E+S, f, d] (the L2 prefetch reads its address)
+  const __nv_bfloat16* w_up;
   __nv_bfloat16* out;
   // routing workspace
   int* idx;          // [T, k]

@@ -115,6 +115,29 @@ __device__ __forceinline__ void trace_record(const Params& p, unsigned long long
   }
 }
 
+// Once the router is done and until the first gate/up tiles start, HBM only
+// carries the plan and the gathers: pull the gate/up weight tiles the first
+// GEMM wave will read into L2 -- tiles (expert, f tile) in index order, the
+// order the plan then keeps (Params::index_order) -- spread over the CTAs,
+// up to l2_pf_bytes.  One lane, asynchronous.
+__device__ void prefetch_first_weights(const Params& p) {
+  const size_t tile_bytes = (size_t)kBM * p.d * 2;  // one 128-row f tile of w_gate or w_up
+  const long long n_tiles =
+      min((long long)p.E * p.n_ftiles, p.l2_pf_bytes / (long long)(2 * tile_bytes));
+  constexpr uint32_t kChunk = 128u << 10;
+  for (long long i = blockIdx.x; i < n_tiles; i += gridDim.x) {
+    const int e = (int)(i / p.n_ftiles), ft = (int)(i - (long long)e * p.n_ftiles);
+    const size_t row0 = (size_t)e * p.f + (size_t)ft * kBM;
+    const char* g = reinterpret_cast<const char*>(p.w_gate + row0 * p.d);
+    const char* u = reinterpret_cast<const char*>(p.w_up + row0 * p.d);
+    for (size_t o = 0; o < tile_bytes; o += kChunk) {
+      const uint32_t n = (uint32_t)min((size_t)kChunk, tile_bytes - o);
+      bulk_prefetch_l2(g + o, n);
+      bulk_prefetch_l2(u + o, n);
+    }
+  }
+}
+
 __device__ void compute_loop(const Params& p, const Maps& maps, char* smem, Ctrl* c,
                              CtaState& st) {
   int executed = 0, gemm_tasks = 0, mover_tasks = 0, done = 0;
@@ -216,7 +239,7 @@ __device__ void scheduler_loop(const Params& p, Ctrl* c, CtaState& st) {
   const int lane = threadIdx.x & 31;
   const unsigned full = 0xffffffffu;
   int posted = 0, handled = 0, ahead = 0, polled_seq = -1;
-  bool exit_posted = false;
+  bool exit_posted = false, prefetched = p.l2_pf_bytes <= 0;
   uint32_t backoff = 32;
   auto post = [&](int t) {
     if (lane == 0) {
@@ -240,6 +263,13 @@ __device__ void scheduler_loop(const Params& p, Ctrl* c, CtaState& st) {
       __syncwarp();
       if (lane == 0) st_release_cta_shared(&c->mb_handled, handled);
       progress = true;
+    }
+    if (!prefetched) {  // the L2 weight prefetch, once every router tile is done
+      const int rd = __shfl_sync(full, lane == 0 ? ld_relaxed(&p.sched->route_done) : 0, 0);
+      if (rd >= p.n_route) {
+        if (lane == 0) prefetch_first_weights(p);
+        prefetched = true;
+      }
     }
     const int status = __shfl_sync(full, lane == 0 ? ld_relaxed(&p.sched->status) : 0, 0);
     if (status != 0) {
@@ -480,6 +510,8 @@ struct moe_layer {
   int release = kReleaseExpert;
   int prefetch = 1;
   int bands = 1;
+  int route_splits = 0;
+  long long l2_pf = 0;  // bytes; -1 = auto
   int trace_cap = 0;
   unsigned long long* trace = nullptr;
   const float* bias = nullptr;
@@ -776,6 +808,14 @@ int moe_layer_set_option(moe_layer_t* h, int key, long long v) {
     case MOE_OPT_BANDS:
       h->bands = v ? 1 : 0;
       break;
+    case MOE_OPT_L2_PREFETCH:
+      if (v < -1) return fail(MOE_E_INVAL, "L2 prefetch must be -1 (auto), 0 (off) or a byte count");
+      h->l2_pf = v;
+      break;
+    case MOE_OPT_ROUTE_SPLITS:
+      if (v < 0 || v > kMaxRouteKs) return fail(MOE_E_INVAL, "router K splits must be 0..8");
+      h->route_splits = (int)v;
+      break;
     case MOE_OPT_ROUTE_TOKENS:
       if (v != 0 && v != kRouteTokens) return fail(MOE_E_INVAL, "router tiles are 128 tokens");
       h->rt_opt = (int)v;
@@ -825,6 +865,7 @@ int moe_layer_forward(moe_layer_t* h, int T, const void* x, const void* router_w
     // two k blocks per split, at most 16 splits)
     const int nkb = h->d / kBK;
     int ks = std::min(kMaxRouteKs, std::min(nkb / 2, std::max(h->num_sms, 1) / p.n_route));
+    if (h->route_splits > 0) ks = std::min(h->route_splits, nkb);
     p.route_ks = std::max(1, ks);
     p.n_route_tasks = p.n_route * p.route_ks;
   }
@@ -856,7 +897,23 @@ int moe_layer_forward(moe_layer_t* h, int T, const void* x, const void* router_w
   p.x = static_cast<const __nv_bfloat16*>(x);
   p.wr = static_cast<const __nv_bfloat16*>(router_w);
   p.bias = h->bias;
+  p.w_gate = static_cast<const __nv_bfloat16*>(w_gate);
+  p.w_up = static_cast<const __nv_bfloat16*>(w_up);
   p.out = static_cast<__nv_bfloat16*>(out);
+  {
+    // L2 prefetch of the first gate/up tiles at launch (persistent mode):
+    // auto when no shared expert keeps HBM busy at the start and the routing
+    // is expected to be balanced (the mean expert load fits half a GEMM
+    // tile), so keeping experts in index order costs no load balance
+    long long pf = h->l2_pf;
+    if (pf < 0) {
+      const bool balanced = h->S == 0 && Tk <= (long long)h->E * (tl.bn / 2);
+      pf = balanced ? (96ll << 20) : 0;
+    }
+    if (h->mode != MOE_MODE_PERSISTENT) pf = 0;
+    p.l2_pf_bytes = pf;
+    p.index_order = pf > 0 ? 1 : 0;
+  }
   char* w = h->ws;
   p.idx = reinterpret_cast<int*>(w + h->o_idx);
   p.wgt = reinterpret_cast<float*>(w + h->o_wgt);

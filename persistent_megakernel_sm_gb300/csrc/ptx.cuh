@@ -236,6 +236,14 @@ namespace moe {
 
 // Global -> shared bulk copy of `bytes` (multiple of 16, both addresses
 // 16-byte aligned), completing `bar` with the byte count.
+// Prefetch `bytes` (a multiple of 16, 16-byte aligned) of global memory into
+// L2; asynchronous, nothing to wait for.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* gsrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(gsrc)),
+               "r"(bytes)
+               : "memory");
+}
+
 __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes,
                                           uint64_t* bar) {
   asm volatile(

@@ -514,8 +514,10 @@ __device__ void plan_task(const Params& p, char* scratch, Ctrl* c, bool push) {
   }
   if (tid == 0) p.offsets[E] = total;
   if (threadIdx.x == 0) c->plan_t[2] = globaltimer();
-  // experts ordered by (count desc, expert asc)
-  if (tid < E) {
+  // experts ordered by (count desc, expert asc), or by index when the first
+  // experts' gate/up weights are being prefetched into L2
+  if (tid < E && p.index_order) order[tid] = tid;
+  if (tid < E && !p.index_order) {
     const int me = cnt[tid];
     int r = 0;
 #pragma unroll 8

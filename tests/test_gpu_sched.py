@@ -61,6 +61,8 @@ def test_every_task_runs_exactly_once(case):
     dict(release=1, claim_ahead=1, grid_ctas=64),
     dict(bands=0),
     dict(bands=0, grid_ctas=5, mover_ctas=2),
+    dict(l2_prefetch=1 << 20),
+    dict(l2_prefetch=1 << 20, grid_ctas=7),
 ])
 def test_schedule_does_not_change_bits(case, opts):
     w, inp, dev, ref = case
