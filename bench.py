@@ -57,7 +57,7 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="decode", choices=list(gen.WORKLOADS))
-    ap.add_argument("--mode", default="persistent", choices=["persistent", "multikernel"])
+    ap.add_argument("--mode", default="persistent", choices=["persistent", "multikernel", "static"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -231,7 +231,7 @@ def run_ours(args):
     layer = pkg.MoELayer(w.d, w.f, w.E, w.k, w.S)
     layer.reserve(w.T)
     layer.set_router_bias(bias)
-    layer.set_option("mode", 0 if args.mode == "persistent" else 1)
+    layer.set_option("mode", {"persistent": 0, "multikernel": 1, "static": 2}[args.mode])
     for kv in args.option:
         name, val = kv.split("=", 1)
         layer.set_option(name, int(val))
@@ -315,8 +315,8 @@ def run_ours(args):
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = traffic
     roof["peak_source"] = f"{peak_src} (burst figure: one launch per step, timed alone)"
-    roof["kernel"] = ("moe_persistent_kernel" if args.mode == "persistent"
-                      else "per-stage kernels (k_route .. k_combine), summed")
+    roof["kernel"] = {"persistent": "moe_persistent_kernel", "static": "moe_static_kernel",
+                      "multikernel": "per-stage kernels (k_route .. k_combine), summed"}[args.mode]
     roof["timed"] = "forward call: one scheduler-reset memset + the kernel(s)"
     roof["algorithmic_bytes"] = alg["bytes"]
     roof["algorithmic_flops"] = alg["flops"]
@@ -326,7 +326,7 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, inp, args.cpu_seconds)
 
-    kernels_per_step = 1 if args.mode == "persistent" else 6
+    kernels_per_step = 6 if args.mode == "multikernel" else 1
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": max(args.warmup, 3), "ms_per_step": ms_max, "higher_is_better": True,

@@ -69,6 +69,9 @@ typedef struct moe_layer moe_layer_t;
 /* execution modes (option MOE_OPT_MODE) */
 #define MOE_MODE_PERSISTENT 0  /* one persistent megakernel, task queue      */
 #define MOE_MODE_MULTIKERNEL 1 /* ablation: one kernel per stage, no queue   */
+#define MOE_MODE_STATIC 2      /* ablation: one cooperative launch, tasks
+                                  assigned round-robin per stage, grid-wide
+                                  barriers between stages, no queue          */
 
 /* option keys for moe_layer_set_option */
 #define MOE_OPT_MODE 1         /* MOE_MODE_*                                   */

@@ -6,6 +6,6 @@ no fallback: importing the binding raises if the library is missing.
 """
 from .binding import (  # noqa: F401
     MOE_OK, MOE_E_INVAL, MOE_E_CUDA, MOE_E_TIMEOUT, MOE_E_DEVICE, MOE_E_NOMEM, MOE_E_STATE,
-    MOE_MODE_PERSISTENT, MOE_MODE_MULTIKERNEL, OPTIONS, STATS, MoEError, MoELayer, lib,
+    MOE_MODE_PERSISTENT, MOE_MODE_MULTIKERNEL, MOE_MODE_STATIC, OPTIONS, STATS, MoEError, MoELayer, lib,
     header_symbols, load_library,
 )

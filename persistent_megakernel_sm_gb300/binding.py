@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(HERE, "_build", "libmoe.so")
 HEADER = os.path.join(os.path.dirname(HERE), "include", "moe.h")
 
 MOE_OK, MOE_E_INVAL, MOE_E_CUDA, MOE_E_TIMEOUT, MOE_E_DEVICE, MOE_E_NOMEM, MOE_E_STATE = range(7)
-MOE_MODE_PERSISTENT, MOE_MODE_MULTIKERNEL = 0, 1
+MOE_MODE_PERSISTENT, MOE_MODE_MULTIKERNEL, MOE_MODE_STATIC = 0, 1, 2
 
 OPTIONS = {
     "mode": 1, "timeout_ns": 2, "mover_ctas": 3, "grid_ctas": 4, "split_k": 5,

@@ -84,7 +84,8 @@ struct Sched {
   int gathers_done;
   int gemm_lo_total_dyn;  // low-priority GEMM tasks (the last d band's down tiles)
   unsigned long long gemm_lo_q[kShards];
-  int pad[10];
+  int bar_count, bar_gen;  // grid barrier of the static mode
+  int pad[8];
 };
 
 struct Params {

@@ -343,6 +343,84 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
   cta_teardown(c, true);
 }
 
+// ------------------------------------------------------------------ static persistent megakernel
+// The static fused baseline: one launch, one CTA per SM, every stage's tasks
+// assigned round-robin to the CTAs (task i of a stage to CTA i mod grid),
+// and a grid-wide barrier between stages -- no queue, no dependency
+// counters, no overlap of stages.  Same tiles as the other two modes, so its
+// gap to the persistent kernel is what the queue, the counters and the
+// cross-stage overlap buy beyond saving launches.  Launched cooperatively, so
+// every CTA is resident and the barrier can wait; each wait is bounded by
+// the deadline.
+
+// Grid-wide barrier: every CTA arrives on a counter; the last one resets it
+// and bumps the generation the others wait for.  False on timeout or abort.
+__device__ bool grid_barrier(const Params& p, Ctrl* c, int& gen, const CtaState& st) {
+  release_writes();
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    const int old = atom_add_acq_rel(&p.sched->bar_count, 1);
+    if (old == (int)gridDim.x - 1) {
+      p.sched->bar_count = 0;
+      st_release(&p.sched->bar_gen, gen + 1);
+    } else {
+      uint32_t backoff = 32;
+      while (ld_acquire(&p.sched->bar_gen) == gen) {
+        if (ld_relaxed(&p.sched->status) != 0) {
+          ok = 0;
+          break;
+        }
+        if (globaltimer() > st.deadline) {
+          set_status(p, MOE_E_TIMEOUT, 40);
+          ok = 0;
+          break;
+        }
+        __nanosleep(backoff);
+        if (backoff < 256) backoff <<= 1;
+      }
+    }
+    c->flag = ok;
+  }
+  cta_sync();
+  ++gen;
+  fence_acq_rel_gpu();
+  return c->flag != 0;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    moe_static_kernel(const __grid_constant__ Params p, const __grid_constant__ Maps maps) {
+  char* smem;
+  Ctrl* c;
+  CtaState st;
+  cta_setup(p, maps, smem, c, st, true);
+  const int G = gridDim.x, b = blockIdx.x;
+  int gen = 0;
+  for (int i = b; i < p.n_route_tasks; i += G)
+    route_task(p, maps, i / p.route_ks, i % p.route_ks, smem, c, st);
+  bool ok = grid_barrier(p, c, gen, st);
+  if (ok && b == 0) plan_task(p, smem, c, false);
+  ok = ok && grid_barrier(p, c, gen, st);
+  const int n_groups = ok ? ld_relaxed(&p.sched->n_groups) : 0;
+  const int n_routed = n_groups - p.n_shared_groups;
+  for (int i = b; ok && i < n_routed * 8; i += G) {  // (routed group, chunk)
+    const int g = p.n_shared_groups + (i >> 3), ch = i & 7;
+    if (ch * kGatherRows < load_group(p, g).nrows) gather_task(p, g, ch, smem, c, st);
+  }
+  ok = ok && grid_barrier(p, c, gen, st);
+  for (int i = b; ok && i < n_groups * p.n_ftiles; i += G)
+    gateup_task(p, maps, task_id(kTaskGateUp, i), smem, c, st);
+  ok = ok && grid_barrier(p, c, gen, st);
+  const int n_down = p.n_dtiles * p.ks;
+  for (int i = b; ok && i < n_groups * n_down; i += G)
+    down_task(p, maps, task_id(kTaskDown, i), smem, c, st);
+  ok = ok && grid_barrier(p, c, gen, st);
+  for (int i = b; ok && i < p.n_comb; i += G) {
+    combine_task(p, i, smem, c, st);
+    cta_sync();
+  }
+  cta_teardown(c, true);
+}
+
 // ------------------------------------------------------------------ ablation: one kernel per stage
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -729,6 +807,7 @@ int moe_layer_reserve(moe_layer_t* h, int T_max, void* stream) {
   const int kernels_smem = kSmemBudget;
   CK(cudaFuncSetAttribute(moe_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                           kernels_smem));
+  CK(cudaFuncSetAttribute(moe_static_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kernels_smem));
   CK(cudaFuncSetAttribute(k_route, cudaFuncAttributeMaxDynamicSharedMemorySize, kernels_smem));
   CK(cudaFuncSetAttribute(k_plan, cudaFuncAttributeMaxDynamicSharedMemorySize, kernels_smem));
   CK(cudaFuncSetAttribute(k_gather, cudaFuncAttributeMaxDynamicSharedMemorySize, kernels_smem));
@@ -750,7 +829,8 @@ int moe_layer_set_option(moe_layer_t* h, int key, long long v) {
   if (!h) return fail(MOE_E_INVAL, "null handle");
   switch (key) {
     case MOE_OPT_MODE:
-      if (v != MOE_MODE_PERSISTENT && v != MOE_MODE_MULTIKERNEL) return fail(MOE_E_INVAL, "bad mode");
+      if (v != MOE_MODE_PERSISTENT && v != MOE_MODE_MULTIKERNEL && v != MOE_MODE_STATIC)
+        return fail(MOE_E_INVAL, "bad mode");
       h->mode = (int)v;
       break;
     case MOE_OPT_TIMEOUT_NS:
@@ -960,6 +1040,12 @@ int moe_layer_forward(moe_layer_t* h, int T, const void* x, const void* router_w
     p.fa_depth = (p.ahead_depth > 0 ? 2 : 1) * grid + 8;
     moe_persistent_kernel<<<grid, kThreads + 32, tl.smem, s>>>(p, m);
     CK(cudaGetLastError());
+  } else if (h->mode == MOE_MODE_STATIC) {
+    const int grid = h->grid_override > 0 ? std::min(h->grid_override, h->num_sms) : h->num_sms;
+    h->last_grid = grid;
+    void* args[] = {&p, &m};
+    CK(cudaLaunchCooperativeKernel((const void*)moe_static_kernel, dim3(grid), dim3(kThreads), args,
+                                   (size_t)tl.smem, s));
   } else {
     h->last_grid = 0;
     k_route<<<p.n_route_tasks, kThreads, tl.smem, s>>>(p, m);
@@ -1120,6 +1206,7 @@ int moe_layer_forward_static(moe_layer_t* h, int T, const void* x, const void* r
       if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
       CK(cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev));
       CK(cudaFuncSetAttribute(moe_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget));
+      CK(cudaFuncSetAttribute(moe_static_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget));
       CK(cudaFuncSetAttribute(k_route, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget));
       CK(cudaFuncSetAttribute(k_plan, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget));
       CK(cudaFuncSetAttribute(k_gather, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget));

@@ -23,7 +23,7 @@ CASES = {
 
 def _full_check(w, inp, mode="persistent", **opts):
     dev = hz.upload(inp)
-    layer = hz.make_layer(w, mode=0 if mode == "persistent" else 1, **opts)
+    layer = hz.make_layer(w, mode={"persistent": 0, "multikernel": 1, "static": 2}[mode], **opts)
     got, routing = hz.run_layer(layer, w, dev)
     hz.check_routing(w, inp, routing)
     ref, _ = oracle.layer(inp["x"], inp["router_w"], inp["bias"], inp["w_gate"], inp["w_up"],
@@ -47,6 +47,18 @@ def test_multikernel_ablation_bit_identical(name):
     a = _full_check(w, inp, "persistent")
     m = _full_check(w, inp, "multikernel")
     assert np.array_equal(a, m), "ablation and megakernel outputs differ"
+
+
+@pytest.mark.parametrize("name", ["tiny", "shared_partial_dtile", "multi_mtile_skew", "top16"])
+def test_static_megakernel_bit_identical(name):
+    # one cooperative launch, round-robin tasks, grid barriers between stages
+    T, d, E, k, f, S, b = CASES[name]
+    w, inp = hz.custom_case(T, d, E, k, f, S, b)
+    a = _full_check(w, inp, "persistent")
+    s = _full_check(w, inp, "static")
+    assert np.array_equal(a, s), "static megakernel and persistent megakernel outputs differ"
+    s7 = _full_check(w, inp, "static", grid_ctas=7)
+    assert np.array_equal(a, s7), "static megakernel depends on its grid size"
 
 
 @pytest.mark.parametrize("split_k", [1, 2, 4])

@@ -46,4 +46,7 @@ def test_workload_parity_and_ablation(workload):
     layer.set_option("mode", 1)
     abl, _ = hz.run_layer(layer, w, dev)
     assert np.array_equal(got, abl), "ablation differs from the megakernel"
+    layer.set_option("mode", 2)
+    sta, _ = hz.run_layer(layer, w, dev)
+    assert np.array_equal(got, sta), "static megakernel differs from the persistent one"
     layer.close()
