@@ -60,8 +60,10 @@ def _L():
         lib.orc_expert_ffn.argtypes = [i32, i32, vp, vp, vp, vp, vp, vp]
         lib.orc_token_out.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
         lib.orc_layer_tokens.argtypes = [i32] * 6 + [vp] * 6 + [i32, vp, vp, vp]
+        lib.orc_residual_rmsnorm.argtypes = [i32, i32, vp, vp, vp, dbl, vp, vp, vp]
         for fn in (lib.orc_bf16_to_f64_array, lib.orc_f64_to_bf16_array, lib.orc_router_logits,
-                   lib.orc_topk, lib.orc_expert_ffn, lib.orc_token_out, lib.orc_layer_tokens):
+                   lib.orc_topk, lib.orc_expert_ffn, lib.orc_token_out, lib.orc_layer_tokens,
+                   lib.orc_residual_rmsnorm):
             fn.restype = None
         _lib = lib
     return _lib
@@ -194,3 +196,25 @@ def layer(x, router_w, bias, w_gate, w_up, w_down, k: int, S: int = 0, tokens=No
     _L().orc_layer_tokens(T, d, f, E, k, S, _p(x), _p(router_w), _p(bias), _p(w_gate), _p(w_up),
                           _p(w_down), n, _p(tok), _p(out), _p(acc))
     return out, acc
+
+
+def residual_rmsnorm(acc, residual, gamma, eps: float):
+    """Residual add and RMSNorm after the combine (xxqk.cn/news/665650
+    section 1 lists both as the megakernel's last steps).
+
+    acc: the combine's rows before rounding, float64 [n, d] (``layer``'s second
+    result); residual: bf16 bits [n, d]; gamma: bf16 bits [d].  Returns
+    (out bf16 bits [n, d], norm_out bf16 bits [n, d], norm before rounding
+    float64 [n, d]) with out = bf16(residual + acc) and
+    norm_out = bf16(out / sqrt(mean(out^2) + eps) * gamma)."""
+    acc = _c(acc, np.float64)
+    residual = _c(residual, np.uint16)
+    gamma = _c(gamma, np.uint16)
+    n, d = acc.shape
+    assert residual.shape == (n, d) and gamma.shape == (d,)
+    out = np.empty((n, d), dtype=np.uint16)
+    norm = np.empty((n, d), dtype=np.uint16)
+    norm64 = np.empty((n, d), dtype=np.float64)
+    _L().orc_residual_rmsnorm(n, d, _p(acc), _p(residual), _p(gamma), float(eps), _p(out),
+                              _p(norm), _p(norm64))
+    return out, norm, norm64

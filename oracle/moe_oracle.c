@@ -29,6 +29,9 @@
  *        y = Wd[e] h                                          (fp64)
  *   8. out[t] = bf16( sum_{j=0..k-1} w_j y_j  +  y_shared )  (shared expert,
  *      index E, weight 1, same h rounding, added after the routed sum)
+ *   9. (optional, orc_residual_rmsnorm) the residual add and the RMSNorm that
+ *      end the megakernel of xxqk.cn/news/665650 section 1:
+ *      out = bf16(residual + the step-8 sum), norm = bf16(out / rms(out) * gamma)
  * Layouts: x [T,d], Wr [E,d], Wg/Wu [E+S,f,d], Wd [E+S,d,f], row-major bf16.
  * Rounding to bf16 is round-to-nearest, ties-to-even, straight from double.
  *
@@ -40,7 +43,9 @@
  * half-way cases; brute-force sorting for top-k; sum of weights = 1 and k = E
  * giving the full softmax; brute-force recount of the permutation; k = E
  * giving the dense mixture; identical experts giving one FFN; a hand-computed
- * layer.  Nothing here is "parity unpinned".
+ * layer; for step 9, a zero residual giving the plain output, a hand-computed
+ * row, unit mean square and scale invariance, a constant row giving the
+ * signed gamma.  Nothing here is "parity unpinned".
  */
 #include <math.h>
 #include <stdint.h>
@@ -275,4 +280,39 @@ void orc_layer_tokens(int T, int d, int f, int E, int k, int S, const uint16_t* 
   free(w);
   free(idx);
   free(L);
+}
+
+/* ---- residual add and RMSNorm after the combine ------------------------------ */
+
+/* The MoE megakernel of xxqk.cn/news/665650 section 1 ends with the residual
+ * add and the normalisation.  The pages give neither form; the reading here is
+ * the pre-norm block of the models they discuss: the layer's output is added
+ * to the residual stream, and the sum, as stored in bf16, is RMS-normalised
+ * for the next sublayer:
+ *   out[c]      = bf16( residual[c] + acc[c] )       acc: the combine's value
+ *                                                     before rounding (fp64)
+ *   ms          = (1/d) sum_c out[c]^2                (out decoded exactly)
+ *   norm_out[c] = bf16( out[c] / sqrt(ms + eps) * gamma[c] )
+ * Rows are [n, d]; norm_f64 (optional) receives the values before rounding. */
+void orc_residual_rmsnorm(int n, int d, const double* acc, const uint16_t* residual,
+                          const uint16_t* gamma, double eps, uint16_t* out, uint16_t* norm_out,
+                          double* norm_f64) {
+  for (int r = 0; r < n; ++r) {
+    const double* a = acc + (size_t)r * d;
+    const uint16_t* res = residual + (size_t)r * d;
+    uint16_t* o = out + (size_t)r * d;
+    double ms = 0.0;
+    for (int c = 0; c < d; ++c) {
+      o[c] = orc_f64_to_bf16(orc_bf16_to_f64(res[c]) + a[c]);
+      const double h = orc_bf16_to_f64(o[c]);
+      ms += h * h;
+    }
+    ms /= (double)d;
+    const double inv = 1.0 / sqrt(ms + eps);
+    for (int c = 0; c < d; ++c) {
+      const double v = orc_bf16_to_f64(o[c]) * inv * orc_bf16_to_f64(gamma[c]);
+      norm_out[(size_t)r * d + c] = orc_f64_to_bf16(v);
+      if (norm_f64) norm_f64[(size_t)r * d + c] = v;
+    }
+  }
 }

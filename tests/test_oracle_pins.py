@@ -311,3 +311,56 @@ def test_token_out_slot_order_and_weights():
     out, acc = oracle.token_out(x, idx, w, wg, wu, wd, E=E, S=0)
     ref = 0.7 * np_ffn(x, wg[3], wu[3], wd[3])[1] + 0.3 * np_ffn(x, wg[1], wu[1], wd[1])[1]
     assert np.allclose(acc, ref, rtol=1e-12, atol=1e-13)
+
+
+# ---- residual add + RMSNorm after the combine ---------------------------------
+
+def test_residual_rmsnorm_zero_residual_is_plain_output():
+    # residual = 0: out is the combine value rounded once, i.e. the layer's output
+    rng = np.random.default_rng(11)
+    acc = rng.standard_normal((3, 64)) * 0.7
+    zero = np.zeros((3, 64), dtype=np.uint16)
+    gamma = as_bf16_bits(np.ones(64))
+    out, _, _ = oracle.residual_rmsnorm(acc, zero, gamma, 1e-6)
+    assert np.array_equal(f64(out), np_round_bf16(acc))
+
+
+def test_residual_rmsnorm_hand_computed():
+    # residual [1, 2, 3, 4] + acc [0.5, -0.5, 0.25, 0] -> out [1.5, 1.5, 3.25, 4]
+    # mean square = (2.25 + 2.25 + 10.5625 + 16) / 4 = 7.765625
+    res = as_bf16_bits([1.0, 2.0, 3.0, 4.0])[None, :]
+    acc = np.array([[0.5, -0.5, 0.25, 0.0]])
+    gamma = as_bf16_bits([1.0, 2.0, 0.5, -1.0])
+    eps = 0.234375
+    out, norm, norm64 = oracle.residual_rmsnorm(acc, res, gamma, eps)
+    assert list(f64(out)[0]) == [1.5, 1.5, 3.25, 4.0]
+    inv = 1.0 / math.sqrt(7.765625 + eps)  # = 1 / sqrt(8) exactly
+    want = np.array([1.5 * inv, 1.5 * inv * 2.0, 3.25 * inv * 0.5, -4.0 * inv])
+    assert np.allclose(norm64[0], want, rtol=0, atol=1e-15)
+    assert np.array_equal(f64(norm)[0], np_round_bf16(want))
+
+
+def test_residual_rmsnorm_unit_rms_and_scale_invariance():
+    # eps = 0, gamma = 1: each row of out / rms has mean square 1, and scaling
+    # the row by a power of two (exact in bf16) leaves the normalised row alone
+    rng = np.random.default_rng(12)
+    res = rand_bf16(rng, (4, 128))
+    acc = np.zeros((4, 128))
+    gamma = as_bf16_bits(np.ones(128))
+    _, norm, norm64 = oracle.residual_rmsnorm(acc, res, gamma, 0.0)
+    assert np.allclose(np.mean(norm64 ** 2, axis=1), 1.0, rtol=0, atol=1e-12)
+    res8 = bits_of(f64(res) * 8.0)
+    _, norm8, norm64_8 = oracle.residual_rmsnorm(acc, res8, gamma, 0.0)
+    assert np.allclose(norm64_8, norm64, rtol=0, atol=1e-14)
+    assert np.array_equal(norm8, norm)
+
+
+def test_residual_rmsnorm_constant_row_gives_signed_gamma():
+    # a row of equal values v normalises to sign(v) * gamma (eps = 0)
+    res = as_bf16_bits(np.full((2, 32), 0.0))
+    acc = np.vstack([np.full(32, 3.0), np.full(32, -0.125)])
+    rng = np.random.default_rng(13)
+    gamma = rand_bf16(rng, (32,))
+    _, norm, _ = oracle.residual_rmsnorm(acc, res, gamma, 0.0)
+    assert np.array_equal(f64(norm)[0], f64(gamma))
+    assert np.array_equal(f64(norm)[1], -f64(gamma))
