@@ -63,6 +63,9 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--residual-norm", action="store_true",
+                    help="time moe_layer_forward_residual_norm (residual add + RMSNorm fused "
+                         "into the combine) instead of moe_layer_forward")
     ap.add_argument("--option", action="append", default=[], metavar="NAME=VALUE",
                     help="a layer option (MoELayer.set_option) for the timed runs")
     return ap.parse_args(argv)
@@ -237,9 +240,20 @@ def run_ours(args):
         layer.set_option(name, int(val))
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
+    if args.residual_norm:  # seeded synthetic residual stream and norm weight
+        g = torch.Generator(device="cpu").manual_seed(7)
+        residual = (torch.randn((w.T, w.d), generator=g) * 0.8).to(torch.bfloat16).cuda()
+        gamma = (1.0 + 0.25 * torch.randn(w.d, generator=g)).to(torch.bfloat16).cuda()
+        norm_out = torch.empty_like(out)
+
+        def fwd():
+            layer.forward_residual_norm(x, wr, wg, wu, wd, residual, gamma, 1e-5, out, norm_out)
+    else:
+        def fwd():
+            layer.forward(x, wr, wg, wu, wd, out)
 
     for _ in range(max(args.warmup, 3)):
-        layer.forward(x, wr, wg, wu, wd, out)
+        fwd()
     layer.check()
     counts = torch.empty(w.E, dtype=torch.int32, device="cuda")
     layer.get_routing(counts=counts)
@@ -263,7 +277,7 @@ def run_ours(args):
     for i in range(K):
         flush.zero_()
         ev[i][0].record(stream)
-        layer.forward(x, wr, wg, wu, wd, out)
+        fwd()
         ev[i][1].record(stream)
     torch.cuda.synchronize()
     if world > 1:
@@ -334,6 +348,7 @@ def run_ours(args):
         "config": {
             "workload": f"{w.name}: {w.describe()}", "T": w.T, "d": w.d, "E": w.E, "k": w.k,
             "f": w.f, "shared_experts": w.S, "mode": args.mode,
+            "residual_rmsnorm": bool(args.residual_norm),
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
             "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MB write, outside the timed events)",
             "inputs": "seeded synthetic (gen module), weights ~N(0,1/fan_in)",

@@ -146,6 +146,24 @@ int moe_layer_forward(moe_layer_t* h, int T, const void* x, const void* router_w
                       const void* w_gate, const void* w_up, const void* w_down, void* out,
                       void* stream);
 
+/* The forward pass with the residual add and the RMSNorm that end the MoE
+ * megakernel (xxqk.cn/news/665650 section 1 lists them after the weighted
+ * merge) fused into the combine.  Per token t, with layer[t] the value
+ * moe_layer_forward rounds to bf16:
+ *   out[t]      = bf16( residual[t] + layer[t] )          (fp32 add)
+ *   norm_out[t] = bf16( out[t] * rsqrt(mean_c out[t,c]^2 + eps) * gamma )
+ * the mean over the d values of out[t] as stored (bf16).  residual [T, d] and
+ * gamma [d] are bf16 device pointers, norm_out [T, d] is overwritten; all
+ * 16-byte aligned; 0 <= eps <= 1.  Everything else (routing, scheduling,
+ * status, asynchrony, no allocation) is that of moe_layer_forward, except
+ * that the combine covers whole rows (MOE_OPT_BANDS does not apply): each
+ * combine task adds the residual rows, bulk-copied with the expert rows, and
+ * then normalises its tile's rows. */
+int moe_layer_forward_residual_norm(moe_layer_t* h, int T, const void* x, const void* router_w,
+                                    const void* w_gate, const void* w_up, const void* w_down,
+                                    const void* residual, const void* gamma, float eps,
+                                    void* out, void* norm_out, void* stream);
+
 /* The same forward pass with x and out in host memory: copies x to the
  * device, runs moe_layer_forward, copies out back and synchronises the
  * stream.  Weights are device pointers as above.  Host buffers may be

@@ -37,6 +37,8 @@ _SIGNATURES = {
     "moe_layer_forward": ([_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp], _i32),
     "moe_layer_forward_host": ([_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp], _i32),
     "moe_layer_forward_static": ([_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp], _i32),
+    "moe_layer_forward_residual_norm": ([_vp, _i32] + [_vp] * 7 + [ctypes.c_float, _vp, _vp, _vp],
+                                        _i32),
     "moe_layer_get_routing": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp], _i32),
     "moe_layer_status": ([_vp, _vp], _i32),
     "moe_layer_set_option": ([_vp, _i32, _i64], _i32),
@@ -127,6 +129,17 @@ class MoELayer:
                                    w_gate.data_ptr(), w_up.data_ptr(), w_down.data_ptr(),
                                    out.data_ptr(), _stream_ptr(stream)))
         return out
+
+    def forward_residual_norm(self, x, router_w, w_gate, w_up, w_down, residual, gamma, eps,
+                              out, norm_out, stream=None):
+        """moe_layer_forward_residual_norm: out = residual + layer(x), norm_out =
+        RMSNorm(out) * gamma, fused into the combine."""
+        T = x.shape[0]
+        _err(lib.moe_layer_forward_residual_norm(
+            self.h, T, x.data_ptr(), router_w.data_ptr(), w_gate.data_ptr(), w_up.data_ptr(),
+            w_down.data_ptr(), residual.data_ptr(), gamma.data_ptr(), float(eps), out.data_ptr(),
+            norm_out.data_ptr(), _stream_ptr(stream)))
+        return out, norm_out
 
     def forward_static(self, x, router_w, w_gate, w_up, w_down, out, stream=None):
         """moe_layer_forward_static: the same pass on the library's fixed scratch."""

@@ -133,6 +133,12 @@ struct Params {
   const __nv_bfloat16* w_gate;  // [E+S, f, d] (the L2 prefetch reads its address)
   const __nv_bfloat16* w_up;
   __nv_bfloat16* out;
+  // optional residual add + RMSNorm fused into the combine (all or none):
+  // out = bf16(residual + layer), norm_out = bf16(out / rms(out) * gamma)
+  const __nv_bfloat16* residual;  // [T, d]
+  const __nv_bfloat16* gamma;     // [d]
+  __nv_bfloat16* norm_out;        // [T, d]
+  float eps;
   // routing workspace
   int* idx;          // [T, k]
   float* wgt;        // [T, k]
@@ -152,6 +158,7 @@ struct Params {
   int* gather_done;  // [max_groups]
   int* gu_done;      // [max_groups]
   int* comb_done;    // [n_comb]
+  int* norm_done;    // [n_comb / n_bands] bands of a combine tile written (fused RMSNorm)
   int* ring_mover;   // [kShards][mover_seg] task id + 1, 0 = not yet pushed
   int* ring_gemm;    // [kShards][gemm_seg]  task id + 1, 0 = not yet pushed
   int* ring_gemm_lo; // [kShards][gemm_seg]  the low-priority GEMM queue

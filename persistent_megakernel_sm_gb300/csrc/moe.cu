@@ -599,7 +599,7 @@ struct moe_layer {
   Bounds B{};
   // offsets into ws
   size_t o_idx, o_wgt, o_rank, o_tile, o_counts, o_offsets, o_perm, o_pos, o_xp, o_h, o_y,
-      o_groups, o_rpart, o_rsd, o_rmask, o_zero, o_gd, o_gu, o_cd, o_sched, o_zero_end, o_ring, o_ring_m, o_ring_g, o_ring_gl,
+      o_groups, o_rpart, o_rsd, o_rmask, o_zero, o_gd, o_gu, o_cd, o_nd, o_sched, o_zero_end, o_ring, o_ring_m, o_ring_g, o_ring_gl,
       o_ring_end;
   // host staging for moe_layer_forward_host
   void* x_dev_stage = nullptr;
@@ -660,6 +660,7 @@ void layout(moe_layer* h, const Bounds& b) {
   h->o_gd = take((size_t)b.max_groups * 4);
   h->o_gu = take((size_t)b.max_groups * 4);
   h->o_cd = take((size_t)b.n_comb * 4);
+  h->o_nd = take((size_t)b.n_comb * 4);
   h->o_zero_end = o;
   h->o_ring = o;
   h->o_ring_m = take((size_t)kShards * (b.mover_cap / kShards * 2 + 64) * 4);
@@ -906,9 +907,18 @@ int moe_layer_set_option(moe_layer_t* h, int key, long long v) {
   return MOE_OK;
 }
 
-int moe_layer_forward(moe_layer_t* h, int T, const void* x, const void* router_w,
-                      const void* w_gate, const void* w_up, const void* w_down, void* out,
-                      void* stream) {
+namespace {
+
+// The residual add + RMSNorm fused into the combine (or none).
+struct Fuse {
+  const void* residual;
+  const void* gamma;
+  float eps;
+  void* norm_out;
+};
+
+int forward_impl(moe_layer_t* h, int T, const void* x, const void* router_w, const void* w_gate,
+                 const void* w_up, const void* w_down, void* out, const Fuse* fz, void* stream) {
   if (!h) return fail(MOE_E_INVAL, "null handle");
   if (!h->ws) return fail(MOE_E_STATE, "moe_layer_reserve was not called");
   if (T < 0 || T > h->T_max) return fail(MOE_E_INVAL, "T out of range (0..T_max)");
@@ -954,7 +964,9 @@ int moe_layer_forward(moe_layer_t* h, int T, const void* x, const void* router_w
   p.ct = tl.ct;
   // d bands: the down tiles of the last quarter of d (at least one tile)
   // have low priority, so the other band's combines overlap them
-  p.n_bands = (h->bands && p.n_dtiles >= 2) ? 2 : 1;
+  // (with the fused residual + RMSNorm a tile's norm waits for its last band,
+  // which runs in the tail: one band measured faster there)
+  p.n_bands = (h->bands && p.n_dtiles >= 2 && !fz) ? 2 : 1;
   p.dt_lo0 = p.n_bands == 2 ? p.n_dtiles - std::max(1, p.n_dtiles / 4) : p.n_dtiles;
   p.n_comb = cdiv(T, tl.ct) * p.n_bands;
   p.n_shared_groups = h->S ? cdiv(T, tl.bn) : 0;
@@ -977,6 +989,12 @@ int moe_layer_forward(moe_layer_t* h, int T, const void* x, const void* router_w
   p.x = static_cast<const __nv_bfloat16*>(x);
   p.wr = static_cast<const __nv_bfloat16*>(router_w);
   p.bias = h->bias;
+  if (fz) {
+    p.residual = static_cast<const __nv_bfloat16*>(fz->residual);
+    p.gamma = static_cast<const __nv_bfloat16*>(fz->gamma);
+    p.norm_out = static_cast<__nv_bfloat16*>(fz->norm_out);
+    p.eps = fz->eps;
+  }
   p.w_gate = static_cast<const __nv_bfloat16*>(w_gate);
   p.w_up = static_cast<const __nv_bfloat16*>(w_up);
   p.out = static_cast<__nv_bfloat16*>(out);
@@ -1011,6 +1029,7 @@ int moe_layer_forward(moe_layer_t* h, int T, const void* x, const void* router_w
   p.gather_done = reinterpret_cast<int*>(w + h->o_gd);
   p.gu_done = reinterpret_cast<int*>(w + h->o_gu);
   p.comb_done = reinterpret_cast<int*>(w + h->o_cd);
+  p.norm_done = reinterpret_cast<int*>(w + h->o_nd);
   p.ring_mover = reinterpret_cast<int*>(w + h->o_ring_m);
   p.ring_gemm = reinterpret_cast<int*>(w + h->o_ring_g);
   p.ring_gemm_lo = reinterpret_cast<int*>(w + h->o_ring_gl);
@@ -1065,6 +1084,26 @@ int moe_layer_forward(moe_layer_t* h, int T, const void* x, const void* router_w
   h->last_valid = false;
   h->last_T = T;
   return MOE_OK;
+}
+
+}  // namespace
+
+int moe_layer_forward(moe_layer_t* h, int T, const void* x, const void* router_w,
+                      const void* w_gate, const void* w_up, const void* w_down, void* out,
+                      void* stream) {
+  return forward_impl(h, T, x, router_w, w_gate, w_up, w_down, out, nullptr, stream);
+}
+
+int moe_layer_forward_residual_norm(moe_layer_t* h, int T, const void* x, const void* router_w,
+                                    const void* w_gate, const void* w_up, const void* w_down,
+                                    const void* residual, const void* gamma, float eps,
+                                    void* out, void* norm_out, void* stream) {
+  if (!residual || !gamma || !norm_out) return fail(MOE_E_INVAL, "null residual/gamma/norm_out");
+  if (!aligned16(residual) || !aligned16(gamma) || !aligned16(norm_out))
+    return fail(MOE_E_INVAL, "residual, gamma and norm_out must be 16-byte aligned");
+  if (!(eps >= 0.f) || eps > 1.f) return fail(MOE_E_INVAL, "eps must be in [0, 1]");
+  const Fuse fz{residual, gamma, eps, norm_out};
+  return forward_impl(h, T, x, router_w, w_gate, w_up, w_down, out, &fz, stream);
 }
 
 int moe_layer_forward_host(moe_layer_t* h, int T, const void* x_host, const void* router_w,

@@ -708,6 +708,14 @@ __device__ void gather_task(const Params& p, int g, int chunk, char* smem, Ctrl*
 }
 
 // ------------------------------------------------------------------ combine (mover)
+// acc += residual[t, 8v .. 8v+7] (the residual add fused into the combine).
+__device__ __forceinline__ void add_residual(const Params& p, int t, int v, float* acc) {
+  float r[8];
+  bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(p.residual) + (size_t)t * (p.d >> 3) + v), r);
+#pragma unroll
+  for (int u = 0; u < 8; ++u) acc[u] += r[u];
+}
+
 // Combine straight from global memory (rows too large for shared memory):
 // columns [c0, c0 + 8 * nvec) of tokens [t0, t0 + nt).
 __device__ void combine_direct(const Params& p, int t0, int nt, int c0, int nvec, Ctrl* c) {
@@ -742,6 +750,7 @@ __device__ void combine_direct(const Params& p, int t0, int nt, int c0, int nvec
 #pragma unroll
       for (int u = 0; u < 8; ++u) acc[u] = fmaf(w, y[u], acc[u]);
     }
+    if (p.residual) add_residual(p, t0 + t, (c0 >> 3) + q, acc);
     out[(size_t)(t0 + t) * dvec + q] = f32x8_to_bf16(acc);
   }
 }
@@ -753,7 +762,7 @@ __device__ void combine_direct(const Params& p, int t0, int nt, int c0, int nvec
 // rows of a few tokens at a time are bulk-copied into one half of the
 // pipeline's shared memory while the other half is being summed (double
 // buffering).
-__device__ void combine_task(const Params& p, int ci, char* smem, Ctrl* c, CtaState& st) {
+__device__ void combine_band(const Params& p, int ci, char* smem, Ctrl* c, CtaState& st) {
   const int ctile = ci / p.n_bands, band = ci - ctile * p.n_bands;
   const int c0 = band_dt0(p, band) * 2 * kBM;
   const int c1 = min(p.d, band_dt1(p, band) * 2 * kBM);
@@ -769,7 +778,10 @@ __device__ void combine_task(const Params& p, int ci, char* smem, Ctrl* c, CtaSt
   const int nsplit = p.y_f32 ? p.ks : 1;
   const int ebytes = p.y_f32 ? 4 : 2;
   const uint32_t row_bytes = (uint32_t)(c1 - c0) * ebytes;  // one source row's band
-  const size_t per_tok = (size_t)nsrc * nsplit * row_bytes;
+  // a token's block: its source rows, then (fused residual) its residual row
+  const uint32_t res_bytes = p.residual ? (uint32_t)(c1 - c0) * 2 : 0u;
+  const size_t src_bytes = (size_t)nsrc * nsplit * row_bytes;
+  const size_t per_tok = src_bytes + res_bytes;
   const size_t mem = (size_t)p.stages * p.stage_bytes;
   if (per_tok > mem) {  // one token's rows do not fit: sum straight from global
     if (threadIdx.x == 0) st_release_cta_shared(&c->mb_late, st.taken);
@@ -793,9 +805,12 @@ __device__ void combine_task(const Params& p, int ci, char* smem, Ctrl* c, CtaSt
       for (int j = 0; j < nsrc; ++j) {
         const int row = j < k ? c->tok[t * k + j] : p.T * k + t0 + t;
         for (int s = 0; s < nsplit; ++s)
-          bulk_load(buf + ((size_t)(tt * nsrc + j) * nsplit + s) * row_bytes,
+          bulk_load(buf + (size_t)tt * per_tok + (size_t)(j * nsplit + s) * row_bytes,
                     Yb + s * part_bytes + (size_t)row * y_row, row_bytes, &c->cbar[b]);
       }
+      if (res_bytes)
+        bulk_load(buf + (size_t)tt * per_tok + src_bytes,
+                  p.residual + (size_t)(t0 + t) * p.d + c0, res_bytes, &c->cbar[b]);
     }
   };
   if (threadIdx.x == 0) {
@@ -824,7 +839,7 @@ __device__ void combine_task(const Params& p, int ci, char* smem, Ctrl* c, CtaSt
       for (int u = 0; u < 8; ++u) acc[u] = 0.f;
       for (int j = 0; j < nsrc; ++j) {
         const float w = j < k ? c->wsum[t * k + j] : 1.f;
-        const char* src = buf + (size_t)(tt * nsrc + j) * nsplit * row_bytes;
+        const char* src = buf + (size_t)tt * per_tok + (size_t)j * nsplit * row_bytes;
         float y[8];
         if (p.y_f32) {
 #pragma unroll
@@ -841,11 +856,68 @@ __device__ void combine_task(const Params& p, int ci, char* smem, Ctrl* c, CtaSt
 #pragma unroll
         for (int u = 0; u < 8; ++u) acc[u] = fmaf(w, y[u], acc[u]);
       }
+      if (res_bytes) {
+        float rv[8];
+        bf16x8_to_f32(reinterpret_cast<const uint4*>(buf + (size_t)tt * per_tok + src_bytes)[q], rv);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) acc[u] += rv[u];
+      }
       out[(size_t)(t0 + t) * dvec + q] = f32x8_to_bf16(acc);
     }
     cta_sync();  // buffer b is free again
     if (threadIdx.x == 0 && r + nbuf < rounds) issue(r + nbuf);
   }
+}
+
+// The RMSNorm of the combine tile's tokens, once every band of the tile has
+// written its columns of out (the residual stream, bf16): per token,
+// norm_out = bf16(out * rsqrt(mean(out^2) + eps) * gamma), the mean over the
+// d stored values.  One warp per token (lanes stride the row, then a fixed
+// butterfly), eight tokens at a time.
+__device__ void norm_tile(const Params& p, int ctile) {
+  const int t0 = ctile * p.ct, nt = min(p.ct, p.T - t0);
+  const int nvec = p.d >> 3, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint4* o4 = reinterpret_cast<const uint4*>(p.out);
+  const uint4* g4 = reinterpret_cast<const uint4*>(p.gamma);
+  uint4* n4 = reinterpret_cast<uint4*>(p.norm_out);
+  for (int tt = warp; tt < nt; tt += kThreads / 32) {
+    const size_t row = (size_t)(t0 + tt) * nvec;
+    float ss = 0.f;
+#pragma unroll 4
+    for (int q = lane; q < nvec; q += 32) {
+      float h[8];
+      bf16x8_to_f32(__ldcg(o4 + row + q), h);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) ss = fmaf(h[u], h[u], ss);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float inv = rsqrtf(ss / (float)p.d + p.eps);
+#pragma unroll 4
+    for (int q = lane; q < nvec; q += 32) {
+      float h[8], g[8], v[8];
+      bf16x8_to_f32(__ldcg(o4 + row + q), h);
+      bf16x8_to_f32(__ldg(g4 + q), g);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = h[u] * inv * g[u];
+      n4[row + q] = f32x8_to_bf16(v);
+    }
+  }
+}
+
+// One combine task: tile ci / n_bands, band ci % n_bands.  With the fused
+// residual + RMSNorm, the task whose band completes the tile (a counter per
+// tile) then runs the tile's norm.
+__device__ void combine_task(const Params& p, int ci, char* smem, Ctrl* c, CtaState& st) {
+  combine_band(p, ci, smem, c, st);
+  if (!p.norm_out) return;
+  const int ctile = ci / p.n_bands;
+  release_writes();
+  if (threadIdx.x == 0) c->flag = atom_add_acq_rel(p.norm_done + ctile, 1) + 1 == p.n_bands;
+  cta_sync();
+  if (!c->flag) return;
+  fence_acq_rel_gpu();
+  norm_tile(p, ctile);
 }
 
 // ------------------------------------------------------------------ GEMM tile (tcgen05)
