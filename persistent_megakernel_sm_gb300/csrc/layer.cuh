@@ -120,7 +120,6 @@ struct Params {
   int ahead_depth;   // claim the next task early when this many wait (0 = never)
   int index_order;   // the plan keeps experts in index order (not by count)
   long long l2_pf_bytes;  // gate/up weight bytes prefetched into L2 at launch (0 = none)
-  int fa_depth;      // claims are fetch-and-adds when this many tasks wait
   unsigned long long timeout_ns;
   // cost model constants
   float beta_move;   // bytes/s one mover CTA sustains

@@ -1,11 +1,12 @@
 // MoE-layer forward for GB300 (sm_103a): the persistent megakernel, the
-// one-kernel-per-stage ablation, and the C ABI declared in include/moe.h.
+// static persistent megakernel and the one-kernel-per-stage ablation, and the
+// C ABI declared in include/moe.h.
 //
 // Persistent mode (Weave abstract, arXiv 2609.21483; xxqk.cn/news/665650
 // sections 2.1-2.3; m.xxqk.cn/news/657744 sections 2.2-2.3): one CTA per SM
 // stays resident and loops { claim a task; run it; publish its writes; bump
 // the dependency counters it feeds; push the tasks that reached zero } until
-// both task queues are drained.  Termination is by task count, never by
+// every task queue is drained.  Termination is by task count, never by
 // seeing an empty queue (m.xxqk.cn/news/657744 section 3.3 describes the
 // early-exit race the other rule invites).  Router tiles and shared-expert
 // tiles are ready at launch; the CTA that finishes the last router tile runs
@@ -1055,8 +1056,6 @@ int forward_impl(moe_layer_t* h, int T, const void* x, const void* router_w, con
     int grid = h->grid_override > 0 ? h->grid_override : h->num_sms;
     h->last_grid = grid;
     p.ahead_depth = h->ahead_opt < 0 ? grid : h->ahead_opt;
-    // fetch-and-add claims when more tasks wait than there are claimers
-    p.fa_depth = (p.ahead_depth > 0 ? 2 : 1) * grid + 8;
     moe_persistent_kernel<<<grid, kThreads + 32, tl.smem, s>>>(p, m);
     CK(cudaGetLastError());
   } else if (h->mode == MOE_MODE_STATIC) {

@@ -1,8 +1,10 @@
 // Device-side tasks of the MoE-layer forward pass and the in-kernel scheduler.
 //
-// Every task is a __device__ function run by a whole CTA (256 threads).  The
-// persistent megakernel (moe.cu) pulls task ids from two queues; the
-// multi-kernel ablation launches the same functions one kernel per stage.
+// Every task is a __device__ function run by the CTA's kThreads compute
+// threads, which synchronise on a named barrier.  The persistent megakernel
+// (moe.cu) pulls task ids from three queues through its scheduler warp; the
+// static megakernel runs them round-robin between grid barriers, and the
+// multi-kernel ablation launches them one kernel per stage.
 #pragma once
 
 #include "layer.cuh"
@@ -578,8 +580,7 @@ __device__ void plan_task(const Params& p, char* scratch, Ctrl* c, bool push) {
     }
   }
   cta_sync();
-  if (threadIdx.x == 0) c->plan_t[4] = globaltimer();
-  if (threadIdx.x == 0) c->plan_t[5] = globaltimer();
+  if (threadIdx.x == 0) c->plan_t[4] = c->plan_t[5] = globaltimer();
   // cost model (spatial split): CTA-seconds of mover work against GEMM work
   const int touched_routed = cta_sync_count(tid < E && cnt[tid] > 0);
   if (tid == 0) {

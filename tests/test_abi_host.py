@@ -67,3 +67,36 @@ def test_options_and_workspace_without_device(lib):
     finally:
         lib.moe_layer_destroy(h)
     lib.moe_layer_destroy(None)
+
+
+def test_new_options_validate_without_device(lib):
+    h = lib.moe_layer_create(2048, 768, 128, 8, 0)
+    try:
+        opt = pkg.OPTIONS
+        assert lib.moe_layer_set_option(h, opt["mode"], pkg.MOE_MODE_STATIC) == 0
+        assert lib.moe_layer_set_option(h, opt["bands"], 0) == 0
+        assert lib.moe_layer_set_option(h, opt["bands"], 1) == 0
+        assert lib.moe_layer_set_option(h, opt["route_splits"], 8) == 0
+        assert lib.moe_layer_set_option(h, opt["route_splits"], 9) == pkg.MOE_E_INVAL
+        assert lib.moe_layer_set_option(h, opt["l2_prefetch"], -1) == 0
+        assert lib.moe_layer_set_option(h, opt["l2_prefetch"], -2) == pkg.MOE_E_INVAL
+        assert lib.moe_layer_set_option(h, opt["release"], 2) == pkg.MOE_E_INVAL
+    finally:
+        lib.moe_layer_destroy(h)
+
+
+def test_residual_norm_entry_validates_without_device(lib):
+    h = lib.moe_layer_create(2048, 768, 128, 8, 0)
+    try:
+        f = lib.moe_layer_forward_residual_norm
+        ptrs = [16] * 5
+        # missing residual / gamma / norm_out
+        assert f(h, 1, *ptrs, None, 16, 1e-5, 16, 16, None) == pkg.MOE_E_INVAL
+        assert f(h, 1, *ptrs, 16, 16, 1e-5, 16, None, None) == pkg.MOE_E_INVAL
+        # misaligned residual, negative eps
+        assert f(h, 1, *ptrs, 8, 16, 1e-5, 16, 16, None) == pkg.MOE_E_INVAL
+        assert f(h, 1, *ptrs, 16, 16, -1.0, 16, 16, None) == pkg.MOE_E_INVAL
+        # well-formed but before reserve: a state error, not a crash
+        assert f(h, 1, *ptrs, 16, 16, 1e-5, 16, 16, None) == pkg.MOE_E_STATE
+    finally:
+        lib.moe_layer_destroy(h)
