@@ -676,7 +676,7 @@ struct Tiling {
   int bn, stages, stage_bytes, smem, ks, rt, ct, y_f32;
 };
 
-int choose_tiling(const moe_layer* h, int T, Tiling* t) {
+int choose_tiling(const moe_layer* h, int T, bool whole_rows, Tiling* t) {
   const long long Tk = (long long)T * h->k;
   int bn = h->bn_opt;
   if (bn <= 0) {
@@ -706,8 +706,11 @@ int choose_tiling(const moe_layer* h, int T, Tiling* t) {
   t->ks = ks;
   t->y_f32 = ks > 1 ? 1 : ((size_t)rows * h->d <= h->B.y_elems ? 1 : 0);
   t->rt = kRouteTokens;
-  // combine tile: ~one per SM, (k+S) rows per token, <= 256 (token, slot) pairs
-  int ct = cdiv(T, 2 * std::max(h->num_sms, 1));
+  // combine tile, <= 256 (token, slot) pairs: one per SM when the combine is
+  // split in two d bands (each task then covers part of a row), two per SM
+  // with one band -- the faster choice of each, measured on GB300
+  const bool two_bands = h->bands && cdiv(h->d, 2 * kBM) >= 2 && !whole_rows;
+  int ct = cdiv(T, (two_bands ? 1 : 2) * std::max(h->num_sms, 1));
   ct = std::max(1, std::min(ct, kThreads / h->k));
   t->ct = ct;
   return MOE_OK;
@@ -931,7 +934,7 @@ int forward_impl(moe_layer_t* h, int T, const void* x, const void* router_w, con
     return fail(MOE_E_INVAL, "tensors must be 16-byte aligned");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Tiling tl;
-  int rc = choose_tiling(h, T, &tl);
+  int rc = choose_tiling(h, T, fz != nullptr, &tl);
   if (rc) return rc;
 
   Params p;
