@@ -106,9 +106,9 @@ typedef struct moe_layer moe_layer_t;
                                   prefetch into L2 once the router is done,
                                   while the plan and gathers run; the plan
                                   then keeps experts in index order.
-                                  0 (default) = off; -1 = 96 MiB when S = 0
-                                  and the mean expert load is at most half a
-                                  GEMM tile, else off                          */
+                                  -1 (default) = 96 MiB when S = 0 and the
+                                  mean expert load is at most half a GEMM
+                                  tile, else off; 0 = off                      */
 
 /* statistics keys for moe_layer_get_stat (values of the last forward;
  * moe_layer_status must have been called after it) */

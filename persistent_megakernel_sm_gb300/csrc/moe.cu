@@ -590,7 +590,7 @@ struct moe_layer {
   int prefetch = 1;
   int bands = 1;
   int route_splits = 0;
-  long long l2_pf = 0;  // bytes; -1 = auto
+  long long l2_pf = -1;  // bytes; -1 = auto
   int trace_cap = 0;
   unsigned long long* trace = nullptr;
   const float* bias = nullptr;
