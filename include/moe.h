@@ -100,7 +100,9 @@ typedef struct moe_layer moe_layer_t;
                                   first band's combine overlaps them; 0: one
                                   band                                         */
 #define MOE_OPT_ROUTE_SPLITS 14 /* K splits of a router tile (1..8; 0 = auto:
-                                  enough to spread the tiles over the SMs)    */
+                                  enough to spread the tiles over the SMs,
+                                  8 k blocks per split at least); capped so
+                                  that tiles x splits <= the SM count          */
 #define MOE_OPT_L2_PREFETCH 15 /* persistent mode: bytes of the first gate/up
                                   weight tiles (experts in index order) to
                                   prefetch into L2 once the router is done,

@@ -680,12 +680,13 @@ int choose_tiling(const moe_layer* h, int T, bool whole_rows, Tiling* t) {
   const long long Tk = (long long)T * h->k;
   int bn = h->bn_opt;
   if (bn <= 0) {
-    // at least 128 tokens (or twice the mean expert load): the MMA's N is the
+    // at least 160 tokens (or twice the mean expert load): the MMA's N is the
     // group's actual rows, so a larger cap wastes nothing and keeps experts
     // whose load varies from being split into sibling groups that re-read
-    // the weights (fine workload: 304 us at 128 against 322 us at 64)
+    // the weights (fine workload: 322, 308, 304, 302, 313 us at 64, 96, 128,
+    // 160, 256; the decode workload is the same at 128 and 160)
     const long long avg = Tk / h->E;
-    long long want = std::max<long long>(128, 2 * avg);
+    long long want = std::max<long long>(160, 2 * avg);
     want = std::min<long long>(want, std::max(T, 1));
     bn = (int)std::min<long long>(256, ((want + 31) / 32) * 32);
   }
@@ -967,11 +968,15 @@ int forward_impl(moe_layer_t* h, int T, const void* x, const void* router_w, con
   p.rt = tl.rt;
   p.n_route = cdiv(T, tl.rt);
   {
-    // K splits of the router: spread few router tiles over the SMs (at least
-    // two k blocks per split, at most 16 splits)
+    // K splits of the router: spread few router tiles over the SMs, with at
+    // least 8 k blocks per split (fine workload: 4 splits, 301 us against
+    // 303 us at 8) and at most kMaxRouteKs.  The partial logits hold one
+    // [128, E] block per SM, so tiles x splits never exceeds the SM count,
+    // the option included.
     const int nkb = h->d / kBK;
-    int ks = std::min(kMaxRouteKs, std::min(nkb / 2, std::max(h->num_sms, 1) / p.n_route));
-    if (h->route_splits > 0) ks = std::min(h->route_splits, nkb);
+    const int cap = std::max(1, std::max(h->num_sms, 1) / p.n_route);
+    int ks = std::min(kMaxRouteKs, std::min(std::max(1, nkb / 8), cap));
+    if (h->route_splits > 0) ks = std::min(std::min(h->route_splits, nkb), cap);
     p.route_ks = std::max(1, ks);
     p.n_route_tasks = p.n_route * p.route_ks;
   }

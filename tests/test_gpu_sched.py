@@ -74,6 +74,20 @@ def test_schedule_does_not_change_bits(case, opts):
     base_layer.close()
 
 
+@pytest.mark.parametrize("splits", [2, 4, 8])
+def test_router_k_split_keeps_routing_and_tolerance(case, splits):
+    # the K split changes the fp32 summation order of the logits, so the
+    # weights may differ in the last bits: same experts, oracle tolerance;
+    # 8 splits of 3 router tiles exceed a 9-CTA grid's partial buffers and
+    # are capped by the host (tiles x splits <= SM count)
+    w, inp, dev, ref = case
+    for opts in (dict(route_splits=splits), dict(route_splits=splits, grid_ctas=9)):
+        layer, out, routing = _run(w, dev, **opts)
+        hz.check_routing(w, inp, routing)
+        hz.check_out(out, ref)
+        layer.close()
+
+
 def test_dropped_notification_times_out_cleanly(case):
     import torch
     w, inp, dev, ref = case
