@@ -105,9 +105,9 @@ typedef struct moe_layer moe_layer_t;
                                   that tiles x splits <= the SM count          */
 #define MOE_OPT_L2_PREFETCH 15 /* persistent mode: bytes of the first gate/up
                                   weight tiles (experts in index order) to
-                                  prefetch into L2 once the router is done,
-                                  while the plan and gathers run; the plan
-                                  then keeps experts in index order.
+                                  prefetch into L2 once the plan is published,
+                                  while the gathers run; the plan keeps
+                                  experts in index order then.
                                   -1 (default) = 96 MiB when S = 0 and the
                                   mean expert load is at most half a GEMM
                                   tile, else off; 0 = off                      */

@@ -116,11 +116,13 @@ __device__ __forceinline__ void trace_record(const Params& p, unsigned long long
   }
 }
 
-// Once the router is done and until the first gate/up tiles start, HBM only
-// carries the plan and the gathers: pull the gate/up weight tiles the first
-// GEMM wave will read into L2 -- tiles (expert, f tile) in index order, the
-// order the plan then keeps (Params::index_order) -- spread over the CTAs,
-// up to l2_pf_bytes.  One lane, asynchronous.
+// Once the plan is published and until the first gate/up tiles start, HBM
+// only carries the gathers: pull the gate/up weight tiles the first GEMM wave
+// will read into L2 -- tiles (expert, f tile) in index order, the order the
+// plan keeps (Params::index_order) -- spread over the CTAs, up to
+// l2_pf_bytes.  One lane, asynchronous.  (Issued earlier, while the plan
+// runs, the prefetch traffic slows the plan's memory accesses: measured
+// 2.5 us slower on the fine and decode workloads.)
 __device__ void prefetch_first_weights(const Params& p) {
   const size_t tile_bytes = (size_t)kBM * p.d * 2;  // one 128-row f tile of w_gate or w_up
   const long long n_tiles =
@@ -265,9 +267,9 @@ __device__ void scheduler_loop(const Params& p, Ctrl* c, CtaState& st) {
       if (lane == 0) st_release_cta_shared(&c->mb_handled, handled);
       progress = true;
     }
-    if (!prefetched) {  // the L2 weight prefetch, once every router tile is done
-      const int rd = __shfl_sync(full, lane == 0 ? ld_relaxed(&p.sched->route_done) : 0, 0);
-      if (rd >= p.n_route) {
+    if (!prefetched) {  // the L2 weight prefetch, once the plan is published
+      const int pd = __shfl_sync(full, lane == 0 ? ld_relaxed(&p.sched->plan_done) : 0, 0);
+      if (pd != 0) {
         if (lane == 0) prefetch_first_weights(p);
         prefetched = true;
       }
