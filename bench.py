@@ -2,7 +2,8 @@
 """Benchmark of the MoE-layer forward megakernel on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode]
-                    [--mode persistent|multikernel] [--impl ours|reference]
+                    [--mode persistent|multikernel|static] [--impl ours|reference]
+                    [--residual-norm] [--option NAME=VALUE ...]
 
 One step = one forward pass of the whole layer (router, top-k, permute,
 gate/up + SiLU, down, combine) over one batch of synthetic tokens.  The default

@@ -55,9 +55,9 @@ struct CtaState {
   int role_mover;       // 1 if this CTA prefers mover work (after the plan)
   uint32_t gather_phase;  // parity of the gather barrier (thread 0)
   uint32_t comb_phase;    // parities of the two combine barriers (bits 0, 1; all threads)
-  int exit_reason;        // why claim_next gave up (trace only): 1 done, 2 abort, 3 deadline
-  unsigned polls;         // claim attempts of thread 0 that found nothing (trace only)
-  bool plan_seen;         // the plan's totals below are cached
+  int exit_reason;        // why the scheduler warp stopped (trace only): 1 done, 2 abort, 3 deadline
+  unsigned polls;         // scheduler warp: claims that found nothing while idle (trace only)
+  bool plan_seen;         // scheduler warp: the plan's totals below are cached
   int n_gather, mover_total, gemm_total, gemm_lo_total;
   int pf_task, pf_count;  // producer: task whose first k blocks are already loading
   int taken;              // compute thread 0: tasks taken from the mailbox
@@ -404,30 +404,6 @@ __device__ int claim_once(const Params& p, CtaState& st, int min_depth) {
   const int bad = lane == 0 ? ld_relaxed(&s->status) : 0;
   if (__shfl_sync(full, bad, 0) != 0) return -3;
   return -1;
-}
-
-// Decide this CTA's next task (one whole warp), waiting with back-off until
-// one is claimable.  Returns a task id or -1 to exit (the same on every lane).
-__device__ int claim_next(const Params& p, CtaState& st) {
-  uint32_t backoff = 32;
-  while (true) {
-    const int r = claim_once(p, st, 1);
-    if (r >= 0) return r;
-    if (r == -4) continue;
-    ++st.polls;
-    if (r == -2 || r == -3) {
-      st.exit_reason = r == -2 ? 1 : 2;
-      return -1;
-    }
-    const int late = (threadIdx.x & 31) == 0 ? globaltimer() > st.deadline : 0;
-    if (__shfl_sync(0xffffffffu, late, 0)) {
-      if ((threadIdx.x & 31) == 0) set_status(p, MOE_E_TIMEOUT, 3);
-      st.exit_reason = 3;
-      return -1;
-    }
-    __nanosleep(backoff);
-    if (backoff < 512) backoff <<= 1;
-  }
 }
 
 // ------------------------------------------------------------------ plan
