@@ -48,6 +48,12 @@ def test_every_task_runs_exactly_once(case):
     t_start = tr["t_start"][real]
     ty = tasks >> 28
     assert t_start[ty == 5].min() >= t_end[ty == 1].max()
+    # the trace summary sees every task type, the whole grid and the plan
+    from persistent_megakernel_sm_gb300.trace_report import summarize
+    s = summarize(tr)
+    assert set(s["types"]) == {"route", "gather", "gateup", "down", "combine"}
+    assert s["grid"] == layer.stat("grid") and len(s["plan_phases_us"]) == 8
+    assert sum(t["n"] for t in s["types"].values()) == layer.stat("tasks")
     layer.close()
 
 
