@@ -122,6 +122,9 @@ typedef struct moe_layer moe_layer_t;
 #define MOE_STAT_STOLEN 6      /* tasks a CTA ran from the other role's queue  */
 #define MOE_STAT_AHEAD 7       /* tasks claimed ahead while another one ran    */
 #define MOE_STAT_TRACE_RECORDS 8 /* task records the last forward produced     */
+#define MOE_STAT_TILE_TOKENS 9 /* max tokens per GEMM tile of the last forward */
+#define MOE_STAT_SPLIT_K 10    /* down-projection K splits of the last forward */
+#define MOE_STAT_BANDS 11      /* d bands of the last forward (1 or 2)         */
 
 /* Create a layer description.  Pure host call (no CUDA call, no allocation on
  * the device).  Returns NULL on invalid dimensions (see moe_last_error). */
@@ -210,6 +213,27 @@ int moe_layer_get_routing(moe_layer_t* h, int32_t* idx, float* w, int32_t* count
  * last forward (MOE_OK, MOE_E_TIMEOUT or MOE_E_DEVICE), or MOE_E_CUDA when a
  * CUDA error is pending. */
 int moe_layer_status(moe_layer_t* h, void* stream);
+
+/* Automatic granularity calibration (the per-workload tuning of task
+ * granularity discussed in xxqk.cn/news/665650 section 4.4 and
+ * m.xxqk.cn/news/657744 section 5.2): times the forward pass on these inputs
+ * for a few candidate settings -- tokens per GEMM tile (auto, 64, 128, 160,
+ * 256), down-projection K splits (auto, 1, 2, 4), one or two d bands -- by
+ * coordinate descent from the current options, `reps` timed passes each
+ * (1..100, after one untimed pass), and keeps the fastest as the handle's
+ * options (MOE_OPT_TOKENS_PER_TILE, MOE_OPT_SPLIT_K, MOE_OPT_BANDS).
+ * Arguments are those of moe_layer_forward (out is overwritten, 1 <= T);
+ * best_us (may be NULL) receives the best mean time in microseconds.  It runs
+ * 10-20 forwards and synchronises the stream after each candidate, so call it
+ * at set-up, not under stream capture; it allocates nothing (two CUDA events).
+ * Candidates that fail (a tile too large, a device timeout) are skipped; the
+ * MOE_STAT_TILE_TOKENS / _SPLIT_K / _BANDS statistics of the next forward
+ * report the chosen tiling.  The expert selection of every candidate is the
+ * same; K splits change the fp32 summation order, so outputs may differ from
+ * the uncalibrated pass in their last bits. */
+int moe_layer_calibrate(moe_layer_t* h, int T, const void* x, const void* router_w,
+                        const void* w_gate, const void* w_up, const void* w_down, void* out,
+                        int reps, float* best_us, void* stream);
 
 /* Set an option (MOE_OPT_*).  Takes effect at the next forward. */
 int moe_layer_set_option(moe_layer_t* h, int key, long long value);

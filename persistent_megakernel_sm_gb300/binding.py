@@ -25,7 +25,7 @@ OPTIONS = {
     "trace": 10, "release": 11, "prefetch": 12, "bands": 13, "route_splits": 14, "l2_prefetch": 15,
 }
 STATS = {"mover_ctas": 1, "tasks": 2, "grid": 3, "gemm_tasks": 4, "mover_tasks": 5, "stolen": 6,
-         "ahead": 7, "trace_records": 8}
+         "ahead": 7, "trace_records": 8, "tile_tokens": 9, "split_k": 10, "bands": 11}
 TASK_TYPES = {1: "route", 2: "gather", 3: "gateup", 4: "down", 5: "combine", 6: "plan"}
 
 _vp, _i32, _i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong
@@ -39,6 +39,7 @@ _SIGNATURES = {
     "moe_layer_forward_static": ([_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp], _i32),
     "moe_layer_forward_residual_norm": ([_vp, _i32] + [_vp] * 7 + [ctypes.c_float, _vp, _vp, _vp],
                                         _i32),
+    "moe_layer_calibrate": ([_vp, _i32] + [_vp] * 6 + [_i32, _vp, _vp], _i32),
     "moe_layer_get_routing": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp], _i32),
     "moe_layer_status": ([_vp, _vp], _i32),
     "moe_layer_set_option": ([_vp, _i32, _i64], _i32),
@@ -140,6 +141,18 @@ class MoELayer:
             w_down.data_ptr(), residual.data_ptr(), gamma.data_ptr(), float(eps), out.data_ptr(),
             norm_out.data_ptr(), _stream_ptr(stream)))
         return out, norm_out
+
+    def calibrate(self, x, router_w, w_gate, w_up, w_down, out, reps: int = 3, stream=None):
+        """moe_layer_calibrate: time candidate tile sizes, K splits and d bands
+        on these inputs and keep the fastest as options; returns the best mean
+        time in microseconds."""
+        T = x.shape[0]
+        best = ctypes.c_float(0.0)
+        _err(lib.moe_layer_calibrate(self.h, T, x.data_ptr(), router_w.data_ptr(),
+                                     w_gate.data_ptr(), w_up.data_ptr(), w_down.data_ptr(),
+                                     out.data_ptr(), int(reps), ctypes.byref(best),
+                                     _stream_ptr(stream)))
+        return best.value
 
     def forward_static(self, x, router_w, w_gate, w_up, w_down, out, stream=None):
         """moe_layer_forward_static: the same pass on the library's fixed scratch."""

@@ -611,6 +611,7 @@ struct moe_layer {
   Sched last{};
   bool last_valid = false;
   int last_grid = 0;
+  int last_bn = 0, last_ks = 0, last_bands = 0;  // tiling of the last forward
   int last_T = 0;
 };
 
@@ -1104,6 +1105,9 @@ int forward_impl(moe_layer_t* h, int T, const void* x, const void* router_w, con
   }
   h->last_valid = false;
   h->last_T = T;
+  h->last_bn = tl.bn;
+  h->last_ks = tl.ks;
+  h->last_bands = p.n_bands;
   return MOE_OK;
 }
 
@@ -1125,6 +1129,80 @@ int moe_layer_forward_residual_norm(moe_layer_t* h, int T, const void* x, const 
   if (!(eps >= 0.f) || eps > 1.f) return fail(MOE_E_INVAL, "eps must be in [0, 1]");
   const Fuse fz{residual, gamma, eps, norm_out};
   return forward_impl(h, T, x, router_w, w_gate, w_up, w_down, out, &fz, stream);
+}
+
+int moe_layer_calibrate(moe_layer_t* h, int T, const void* x, const void* router_w,
+                        const void* w_gate, const void* w_up, const void* w_down, void* out,
+                        int reps, float* best_us, void* stream) {
+  if (!h) return fail(MOE_E_INVAL, "null handle");
+  if (!h->ws) return fail(MOE_E_STATE, "moe_layer_reserve was not called");
+  if (T < 1 || T > h->T_max) return fail(MOE_E_INVAL, "T out of range (1..T_max)");
+  if (reps < 1 || reps > 100) return fail(MOE_E_INVAL, "reps must be 1..100");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  CK(cudaEventCreate(&e0));
+  if (cudaEventCreate(&e1) != cudaSuccess) {
+    cudaEventDestroy(e0);
+    return fail(MOE_E_CUDA, "cudaEventCreate");
+  }
+  // mean time of `reps` forwards after one untimed one; +inf if a forward or
+  // its device status fails (the candidate is then never chosen)
+  auto time_it = [&](float* ms) -> int {
+    *ms = INFINITY;
+    int rc = moe_layer_forward(h, T, x, router_w, w_gate, w_up, w_down, out, stream);
+    if (rc == MOE_OK) rc = moe_layer_status(h, stream);
+    if (rc != MOE_OK) return rc == MOE_E_CUDA ? rc : MOE_OK;
+    if (cudaEventRecord(e0, s) != cudaSuccess) return MOE_E_CUDA;
+    for (int r = 0; r < reps && rc == MOE_OK; ++r)
+      rc = moe_layer_forward(h, T, x, router_w, w_gate, w_up, w_down, out, stream);
+    if (cudaEventRecord(e1, s) != cudaSuccess) return MOE_E_CUDA;
+    const int st = moe_layer_status(h, stream);
+    if (rc != MOE_OK || st != MOE_OK) return (rc == MOE_E_CUDA || st == MOE_E_CUDA) ? MOE_E_CUDA : MOE_OK;
+    float el = 0.f;
+    if (cudaEventElapsedTime(&el, e0, e1) != cudaSuccess) return MOE_E_CUDA;
+    *ms = el / reps;
+    return MOE_OK;
+  };
+  // coordinate descent from the current settings: tile tokens, then the down
+  // K split, then one or two d bands
+  const int bn_c[] = {0, 64, 128, 160, 256};
+  const int ks_c[] = {0, 1, 2, 4};
+  const int bd_c[] = {1, 0};
+  float best = INFINITY;
+  int rc = time_it(&best);
+  for (int i = 0; rc == MOE_OK && i < 5; ++i) {
+    const int keep = h->bn_opt;
+    if (bn_c[i] == keep) continue;
+    h->bn_opt = bn_c[i];
+    float t;
+    rc = time_it(&t);
+    if (t < best) best = t;
+    else h->bn_opt = keep;
+  }
+  for (int i = 0; rc == MOE_OK && i < 4; ++i) {
+    const int keep = h->split_k;
+    if (ks_c[i] == keep) continue;
+    h->split_k = ks_c[i];
+    float t;
+    rc = time_it(&t);
+    if (t < best) best = t;
+    else h->split_k = keep;
+  }
+  for (int i = 0; rc == MOE_OK && i < 2; ++i) {
+    const int keep = h->bands;
+    if (bd_c[i] == keep) continue;
+    h->bands = bd_c[i];
+    float t;
+    rc = time_it(&t);
+    if (t < best) best = t;
+    else h->bands = keep;
+  }
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  if (rc != MOE_OK) return rc;
+  if (!(best < INFINITY)) return fail(MOE_E_DEVICE, "no calibration candidate ran cleanly");
+  if (best_us) *best_us = best * 1e3f;
+  return MOE_OK;
 }
 
 int moe_layer_forward_host(moe_layer_t* h, int T, const void* x_host, const void* router_w,
@@ -1190,7 +1268,11 @@ int moe_layer_status(moe_layer_t* h, void* stream) {
 }
 
 long long moe_layer_get_stat(moe_layer_t* h, int key) {
-  if (!h || !h->last_valid) return -1;
+  if (!h) return -1;
+  if (key == MOE_STAT_TILE_TOKENS) return h->last_T ? h->last_bn : -1;
+  if (key == MOE_STAT_SPLIT_K) return h->last_T ? h->last_ks : -1;
+  if (key == MOE_STAT_BANDS) return h->last_T ? h->last_bands : -1;
+  if (!h->last_valid) return -1;
   switch (key) {
     case MOE_STAT_MOVER_CTAS: return h->last.n_movers;
     case MOE_STAT_TASKS: return h->last.tasks_done;

@@ -100,3 +100,16 @@ def test_residual_norm_entry_validates_without_device(lib):
         assert f(h, 1, *ptrs, 16, 16, 1e-5, 16, 16, None) == pkg.MOE_E_STATE
     finally:
         lib.moe_layer_destroy(h)
+
+
+def test_calibrate_validates_without_device(lib):
+    assert lib.moe_layer_calibrate(None, 8, 16, 16, 16, 16, 16, 16, 3, None, None) == \
+        pkg.MOE_E_INVAL
+    h = lib.moe_layer_create(2048, 768, 128, 8, 0)
+    try:
+        # before reserve: a state error, not a crash
+        assert lib.moe_layer_calibrate(h, 8, 16, 16, 16, 16, 16, 16, 3, None, None) == \
+            pkg.MOE_E_STATE
+        assert lib.moe_layer_get_stat(h, pkg.STATS["tile_tokens"]) == -1
+    finally:
+        lib.moe_layer_destroy(h)
