@@ -83,7 +83,10 @@ typedef struct moe_layer moe_layer_t;
 #define MOE_OPT_FAULT_DROP_TASK 7 /* test only: -1 off; else drop the dependency
                                      notification of the n-th finished GEMM task,
                                      which must end in MOE_E_TIMEOUT            */
-#define MOE_OPT_ROUTE_TOKENS 8 /* tokens per router tile: 0 or 128 (the MMA M) */
+#define MOE_OPT_ROUTE_TOKENS 8 /* tokens per router tile: 64 or 128; 0 (default)
+                                  = 64 when T <= 1024 and E >= 64, else 128.
+                                  A forward with more than 256 router tiles
+                                  fails with MOE_E_INVAL                      */
 #define MOE_OPT_CLAIM_AHEAD 9  /* claim the next task while running one when at
                                   least this many tasks wait; -1 auto, 0 off  */
 #define MOE_OPT_TRACE 10       /* >0: record up to this many task records per

@@ -18,6 +18,9 @@ constexpr int kBBoxRows = 32;       // token rows per activation box
 constexpr int kBBoxBytes = kBBoxRows * kBK * 2;  // 4 KB
 constexpr int kGatherRows = 32;     // permuted rows per gather task
 constexpr int kRouteTokens = 128;   // tokens per router tile (the MMA M)
+constexpr int kRouteTokensSmall = 64;  // router tile of small layers with many experts
+constexpr int kSmallRouteT = 1024;
+constexpr int kSmallRouteMinE = 64;
 constexpr int kMaxRouteKs = 8;      // K splits of a router tile, at most
 constexpr int kShards = 8;          // shards of each task queue
 constexpr int kMaxE = 256;
@@ -99,7 +102,7 @@ struct Params {
   int n_dtiles;      // ceil(d / 256): each down task covers 256 d rows
   int ks;            // split of the down projection's K (= f)
   int kb_down;       // k blocks (of 64) per down split
-  int rt;            // tokens per router tile (kRouteTokens)
+  int rt;            // tokens per router tile (kRouteTokens or kRouteTokensSmall)
   int n_route;       // router tiles
   int route_ks;      // K splits of a router tile
   int n_route_tasks; // n_route * route_ks (implicit slots of the mover queue)

@@ -621,7 +621,7 @@ Bounds make_bounds(const moe_layer* h, int T) {
   Bounds b{};
   b.T = T;
   const long long Tk = (long long)T * h->k;
-  b.n_route = std::max(1, cdiv(T, kRouteTokens));
+  b.n_route = std::max(1, cdiv(T, kRouteTokensSmall));  // at the smallest router tile
   const int shared_groups = h->S ? cdiv(T, 32) : 0;
   b.max_groups = shared_groups + cdiv(Tk, 32) + std::min<long long>(h->E, Tk) + 1;
   b.n_comb = 2 * std::max(T, 1);  // one token per tile, two d bands
@@ -721,7 +721,13 @@ int choose_tiling(const moe_layer* h, int T, bool whole_rows, Tiling* t) {
   if (ks < 1) ks = 1;
   t->ks = ks;
   t->y_f32 = ks > 1 ? 1 : ((size_t)rows * h->d <= h->B.y_elems ? 1 : 0);
-  t->rt = kRouteTokens;
+  // router tile: 64 tokens for small layers with many experts (four threads
+  // per token share the top-k and softmax over E, and twice the tiles spread
+  // over the SMs; with few experts the extra threads have nothing to do and
+  // the extra tiles only add tasks), else 128
+  const bool small_rt = T <= kSmallRouteT && h->E >= kSmallRouteMinE;
+  t->rt = h->rt_opt ? h->rt_opt : (small_rt ? kRouteTokensSmall : kRouteTokens);
+  if (cdiv(T, t->rt) > kMaxE) return fail(MOE_E_INVAL, "too many router tiles: use 128-token tiles");
   // combine tile, <= 256 (token, slot) pairs: one per SM when the combine is
   // split in two d bands (each task then covers part of a row), two per SM
   // with one band -- the faster choice of each, measured on GB300
@@ -918,7 +924,8 @@ int moe_layer_set_option(moe_layer_t* h, int key, long long v) {
       h->route_splits = (int)v;
       break;
     case MOE_OPT_ROUTE_TOKENS:
-      if (v != 0 && v != kRouteTokens) return fail(MOE_E_INVAL, "router tiles are 128 tokens");
+      if (v != 0 && v != kRouteTokens && v != kRouteTokensSmall)
+        return fail(MOE_E_INVAL, "router tiles are 64 or 128 tokens (0: automatic)");
       h->rt_opt = (int)v;
       break;
     default:

@@ -652,7 +652,7 @@ __device__ void gather_task(const Params& p, int g, int chunk, char* smem, Ctrl*
       }
       rank -= pc;
     }
-    const int t = lo * kRouteTokens + bit;
+    const int t = lo * p.rt + bit;
     c->tok[threadIdx.x] = t;
     p.perm[r] = t;
     for (int j = 0; j < p.k; ++j)
@@ -1192,10 +1192,14 @@ __device__ void down_task(const Params& p, const Maps& maps, int task, char* sme
 // (one quarter warp) on distinct banks.
 __device__ __forceinline__ int route_row_stride(int E) { return ((E + 15) / 16) * 16 + 4; }
 
-// Shared-memory bytes the router epilogue needs (logits + exchange area).
+// Shared-memory bytes the router epilogue needs (logits + exchange area), for
+// either tile size (128 tokens, two threads per token; 64 tokens, four).
 __host__ __device__ __forceinline__ size_t route_smem_bytes(int E) {
+  // max [rt] + part sums [parts][rt] + (parts - 1) lists of 2 KL words per token
+  const size_t xch128 = (size_t)(1 + 2 + 1 * 2 * kMaxK) * 128;
+  const size_t xch64 = (size_t)(1 + 4 + 3 * 2 * kMaxK) * 64;
   return (size_t)kRouteTokens * (((E + 15) / 16) * 16 + 4) * 4 +
-         (size_t)(2 + 2 * kMaxK) * kRouteTokens * 4;
+         (xch128 > xch64 ? xch128 : xch64) * 4;
 }
 
 // The top-k order: larger logit first, smaller expert first on equal logits.
@@ -1229,23 +1233,25 @@ __device__ __forceinline__ void topk_merge(float (&tv)[KL], int (&te)[KL], float
   }
 }
 
-// Epilogue of one router tile whose logits (without bias) sit in shared
-// memory, token m's row at lg + m * ls.  Two threads per token: warps 0-3
-// take experts [0, eh) and warps 4-7 [eh, E).  Pass 1 keeps each half's
-// top-KL list, four logits at a time (sorted by a 4-input network, then
-// merged); the upper half hands its list to the lower one, whose merged list
-// starts with the row maximum.  Pass 2 sums exp(L - max) over each half.
-// Then p_j = exp(L_j - max) / sum and w_j = p_j / sum of the kept p.
+// Epilogue of one router tile of rt tokens (p.rt: 128 or 64) whose logits
+// (without bias) sit in shared memory, token m's row at lg + m * ls.  The
+// CTA's threads split each token's experts: thread t takes token t % rt and
+// the (t / rt)-th of kThreads / rt equal expert ranges (multiples of four).
+// Pass 1 keeps each range's top-KL list, four logits at a time (sorted by a
+// 4-input network, then merged); the other parts hand their lists to part 0,
+// which merges them in part order, so its list starts with the row maximum.
+// Pass 2 sums exp(L - max) over each range; part 0 adds the parts' sums in
+// part order.  Then p_j = exp(L_j - max) / sum and w_j = p_j / sum of the
+// kept p.
 template <int KL>
 __device__ __noinline__ void route_epilogue(const Params& p, Ctrl* c, int tile, int nt,
                                             const float* lg, int ls, float* xch) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int E = p.E, k = p.k;
-  const int t0 = tile * kRouteTokens;
-  const int m = (warp & 3) * 32 + lane;
-  const int upper = warp >> 2;
-  const int eh = ((E + 7) / 8) * 4;  // a multiple of 4: float4 aligned
-  const int e0 = upper ? eh : 0, e1 = upper ? E : min(eh, E);
+  const int E = p.E, k = p.k, rt = p.rt;
+  const int parts = kThreads / rt;
+  const int t0 = tile * rt;
+  const int m = threadIdx.x % rt, part = threadIdx.x / rt;
+  const int span = ((E + 4 * parts - 1) / (4 * parts)) * 4;  // a multiple of 4: float4 aligned
+  const int e0 = min(E, part * span), e1 = min(E, e0 + span);
   float tv[KL];
   int te[KL];
 #pragma unroll
@@ -1263,6 +1269,9 @@ __device__ __noinline__ void route_epilogue(const Params& p, Ctrl* c, int tile, 
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       ne[j] = e4 + j;
+      // a NaN logit ranks as -inf (below every real expert's finite logit,
+      // above the empty slots), so the kept k are always real experts
+      nv[j] = nv[j] == nv[j] ? nv[j] : -INFINITY;
       if (e4 + j >= e1) {
         nv[j] = -INFINITY;
         ne[j] = 0x7fffffff;
@@ -1275,28 +1284,35 @@ __device__ __noinline__ void route_epilogue(const Params& p, Ctrl* c, int tile, 
     topk_cx(nv[1], ne[1], nv[2], ne[2]);
     topk_merge<KL, 4>(tv, te, nv, ne);
   }
-  // exchange area: [2 + 2 * KL][128] words, token-minor (conflict-free)
+  // exchange area, token-minor (conflict-free): max [rt], sums [parts][rt],
+  // then the lists of parts 1.. : values [KL][rt] and experts [KL][rt] each
   float* x_max = xch;
-  float* x_sum = xch + kRouteTokens;
-  float* x_v = xch + 2 * kRouteTokens;
-  int* x_e = reinterpret_cast<int*>(xch) + (2 + KL) * kRouteTokens;
-  if (upper) {
+  float* x_sum = xch + rt;
+  float* x_list = xch + (size_t)(1 + parts) * rt;
+  const size_t list_words = (size_t)2 * KL * rt;
+  if (part > 0) {
+    float* v = x_list + (size_t)(part - 1) * list_words;
+    int* ev = reinterpret_cast<int*>(v + (size_t)KL * rt);
 #pragma unroll
     for (int s = 0; s < KL; ++s) {
-      x_v[s * kRouteTokens + m] = tv[s];
-      x_e[s * kRouteTokens + m] = te[s];
+      v[s * rt + m] = tv[s];
+      ev[s * rt + m] = te[s];
     }
   }
   cta_sync();
-  if (!upper) {
-    float bv[KL];
-    int be[KL];
+  if (part == 0) {
+    for (int q = 1; q < parts; ++q) {
+      const float* v = x_list + (size_t)(q - 1) * list_words;
+      const int* ev = reinterpret_cast<const int*>(v + (size_t)KL * rt);
+      float bv[KL];
+      int be[KL];
 #pragma unroll
-    for (int s = 0; s < KL; ++s) {
-      bv[s] = x_v[s * kRouteTokens + m];
-      be[s] = x_e[s * kRouteTokens + m];
+      for (int s = 0; s < KL; ++s) {
+        bv[s] = v[s * rt + m];
+        be[s] = ev[s * rt + m];
+      }
+      topk_merge<KL, KL>(tv, te, bv, be);
     }
-    topk_merge<KL, KL>(tv, te, bv, be);
     x_max[m] = tv[0];
   }
   cta_sync();
@@ -1310,10 +1326,11 @@ __device__ __noinline__ void route_epilogue(const Params& p, Ctrl* c, int tile, 
     for (int j = 0; j < 4; ++j)
       if (e4 + j < e1) sum += __expf(nv[j] - mx);
   }
-  if (upper) x_sum[m] = sum;
+  x_sum[part * rt + m] = sum;
   cta_sync();
-  const bool valid = !upper && m < nt;
-  if (!upper) sum += x_sum[m];
+  const bool valid = part == 0 && m < nt;
+  if (part == 0)
+    for (int q = 1; q < parts; ++q) sum += x_sum[q * rt + m];
   float pk[KL];
   float kept = 0.f;
 #pragma unroll
@@ -1369,8 +1386,9 @@ __device__ __forceinline__ void route_epilogue_k(const Params& p, Ctrl* c, int t
 // runs the epilogue.  Returns true when this call completed the tile.
 __device__ bool route_task(const Params& p, const Maps& maps, int tile, int split, char* smem,
                            Ctrl* c, CtaState& st) {
-  const int t0 = tile * kRouteTokens;
-  const int nt = min(kRouteTokens, p.T - t0);
+  const int rt = p.rt;  // tokens of a router tile: 128, or 64 for small layers
+  const int t0 = tile * rt;
+  const int nt = min(rt, p.T - t0);
   const int ks = p.route_ks;
   const int nkb = p.d / kBK;
   const int epad = ((p.E + 15) / 16) * 16;
@@ -1398,14 +1416,15 @@ __device__ bool route_task(const Params& p, const Maps& maps, int tile, int spli
     const uint32_t lane_addr = c->tmem_base + ((uint32_t)((warp & 3) * 32) << 16);
     const int ls = route_row_stride(p.E);
     float* lg = reinterpret_cast<float*>(smem);  // [128][ls] logits
-    float* xch = lg + (size_t)kRouteTokens * ls;
+    float* xch = lg + (size_t)rt * ls;
     const int nch = epad / 16;
     if (ks == 1) {
-      // TMEM -> shared: warps w and w + 4 share TMEM lanes, each takes half the chunks
+      // TMEM -> shared, the tile's rt rows: warps w and w + 4 share TMEM
+      // lanes, each takes half the chunks (the MMA's rows past rt are unused)
       const int m = (warp & 3) * 32 + (threadIdx.x & 31);
       const int c0 = (warp >> 2) * ((nch + 1) / 2), c1 = (warp >> 2) ? nch : (nch + 1) / 2;
       float4* dst = reinterpret_cast<float4*>(lg + (size_t)m * ls);
-      for (int ch = c0; ch < c1; ++ch) {
+      for (int ch = c0; (warp & 3) * 32 < rt && ch < c1; ++ch) {
         float v[16];
         tmem_ld16(lane_addr + ch * 16, v);
 #pragma unroll
@@ -1417,11 +1436,11 @@ __device__ bool route_task(const Params& p, const Maps& maps, int tile, int spli
       route_epilogue_k(p, c, tile, nt, lg, ls, xch);
       tile_done = true;
     } else {
-      // partial logits of this split: [tile][split][128][epad] fp32
-      if (warp < 4) {
+      // partial logits of this split: [tile][split][rt][epad] fp32
+      if (warp < 4 && warp * 32 < rt) {
         const int m = warp * 32 + (threadIdx.x & 31);
         float4* dst = reinterpret_cast<float4*>(
-            p.rpart + (((size_t)tile * ks + split) * kRouteTokens + m) * epad);
+            p.rpart + (((size_t)tile * ks + split) * rt + m) * epad);
         for (int ch = 0; ch < nch; ++ch) {
           float v[16];
           tmem_ld16(lane_addr + ch * 16, v);
@@ -1439,8 +1458,8 @@ __device__ bool route_task(const Params& p, const Maps& maps, int tile, int spli
         // sum the splits into the shared logits, in split order: each thread
         // owns up to 16 float4 of the tile per round and loads that slice of
         // every split in turn (16 independent loads in flight per thread)
-        const float4* src = reinterpret_cast<const float4*>(p.rpart + (size_t)tile * ks * kRouteTokens * epad);
-        const int r4 = epad / 4, n4 = kRouteTokens * r4;
+        const float4* src = reinterpret_cast<const float4*>(p.rpart + (size_t)tile * ks * rt * epad);
+        const int r4 = epad / 4, n4 = rt * r4;
         constexpr int kPer = 16;
         for (int base = 0; base < n4; base += kPer * kThreads) {
           float4 acc[kPer];

@@ -81,6 +81,9 @@ def test_new_options_validate_without_device(lib):
         assert lib.moe_layer_set_option(h, opt["l2_prefetch"], -1) == 0
         assert lib.moe_layer_set_option(h, opt["l2_prefetch"], -2) == pkg.MOE_E_INVAL
         assert lib.moe_layer_set_option(h, opt["release"], 2) == pkg.MOE_E_INVAL
+        for v in (0, 64, 128):
+            assert lib.moe_layer_set_option(h, opt["route_tokens"], v) == 0
+        assert lib.moe_layer_set_option(h, opt["route_tokens"], 96) == pkg.MOE_E_INVAL
     finally:
         lib.moe_layer_destroy(h)
 

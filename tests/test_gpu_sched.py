@@ -94,6 +94,19 @@ def test_router_k_split_keeps_routing_and_tolerance(case, splits):
         layer.close()
 
 
+@pytest.mark.parametrize("rt", [64, 128])
+def test_router_tile_size_keeps_routing_and_tolerance(case, rt):
+    # 64-token router tiles split each token's experts over four threads
+    # instead of two, so the softmax sum adds its parts in another order:
+    # same experts, oracle tolerance, with and without router K splits
+    w, inp, dev, ref = case
+    for opts in (dict(route_tokens=rt), dict(route_tokens=rt, route_splits=4, grid_ctas=11)):
+        layer, out, routing = _run(w, dev, **opts)
+        hz.check_routing(w, inp, routing)
+        hz.check_out(out, ref)
+        layer.close()
+
+
 def test_dropped_notification_times_out_cleanly(case):
     import torch
     w, inp, dev, ref = case
