@@ -32,6 +32,10 @@
  *   9. (optional, orc_residual_rmsnorm) the residual add and the RMSNorm that
  *      end the megakernel of xxqk.cn/news/665650 section 1:
  *      out = bf16(residual + the step-8 sum), norm = bf16(out / rms(out) * gamma)
+ *  10. (orc_movers) the spatial split of the Weave abstract: once routing is
+ *      known, the CTAs are divided between data movement and the expert GEMMs
+ *      in the ratio of the two sides' work (the formula is this project's
+ *      reading; see orc_movers).
  * Layouts: x [T,d], Wr [E,d], Wg/Wu [E+S,f,d], Wd [E+S,d,f], row-major bf16.
  * Rounding to bf16 is round-to-nearest, ties-to-even, straight from double.
  *
@@ -45,7 +49,9 @@
  * giving the dense mixture; identical experts giving one FFN; a hand-computed
  * layer; for step 9, a zero residual giving the plain output, a hand-computed
  * row, unit mean square and scale invariance, a constant row giving the
- * signed gamma.  Nothing here is "parity unpinned".
+ * signed gamma; for step 10, the byte and FLOP totals recounted copy by copy
+ * and row by row, the split against a brute-force minimiser of the slower
+ * side's time, and its clamps.  Nothing here is "parity unpinned".
  */
 #include <math.h>
 #include <stdint.h>
@@ -315,4 +321,48 @@ void orc_residual_rmsnorm(int n, int d, const double* acc, const uint16_t* resid
       if (norm_f64) norm_f64[(size_t)r * d + c] = v;
     }
   }
+}
+
+/* ---- step 10: the spatial split of the CTAs --------------------------------
+ * Weave abstract: once routing completes, the layer's communication and
+ * computation volumes are known, and a cost model inside the megakernel
+ * divides the SMs into communication and computation workers so that the two
+ * sides' throughputs match.  The page gives no formula; this project reads it
+ * as follows, with the work of each side in worker-seconds:
+ *   a = B_move / beta                      bytes the movers copy, at beta B/s
+ *       B_move = T*k rows gathered (read and write d bf16 values each)
+ *              + T*(k+S) expert-output rows read by the combine, d values of
+ *                ybytes each (4*ks for ks fp32 K-split partials, else 2)
+ *              + T rows written by the combine (d bf16 values each)
+ *   b = max(F / phi, N * G_w / BW)         the GEMM side: its FLOPs at phi
+ *       F   = 6 * d * f per routed or shared row (T*k + T*S rows)   FLOP/s per
+ *       G_w = 3 * f * d bf16 weights per touched expert              worker,
+ *             (routed experts with a token, plus S shared)           or the
+ *                                                  weight stream at BW for N
+ *   M* = clamp(round(N * a / (a + b)), 1, N - 1)   (N * a / (a + b) minimises
+ *        max(a / M, b / (N - M)), the slower side's time, over real M)
+ * M* is an integer decided by floating point, so it is computed in fp32, the
+ * precision the kernel decides in, rounding half to even; *m_cont receives
+ * N * a / (a + b) before rounding. */
+int orc_movers(int T, int d, int f, int k, int S, int touched_routed, int N, int ks, int y_f32,
+               float beta, float phi, float bw, float* m_cont) {
+  const float ybytes = y_f32 ? 4.0f * (float)ks : 2.0f;
+  const float Tk = (float)T * (float)k;
+  const float gather = Tk * (float)d * 2.0f * 2.0f;
+  const float combine_read = ((float)T * (float)(k + S)) * (float)d * ybytes;
+  const float combine_write = (float)T * (float)d * 2.0f;
+  const float b_move = gather + combine_read + combine_write;
+  const float flops = 6.0f * (Tk + (float)T * (float)S) * (float)d * (float)f;
+  const float wbytes = (float)(touched_routed + S) * 3.0f * (float)f * (float)d * 2.0f;
+  const float a = b_move / beta;
+  const float b_flops = flops / phi;
+  const float b_bytes = (float)N * wbytes / bw;
+  const float b = b_flops > b_bytes ? b_flops : b_bytes;
+  const float x = (float)N * a / (a + b);
+  if (m_cont) *m_cont = x;
+  int m = (int)nearbyintf(x);
+  const int hi = N - 1 > 1 ? N - 1 : 1;
+  if (m > hi) m = hi;
+  if (m < 1) m = 1;
+  return m;
 }

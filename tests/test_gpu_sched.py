@@ -107,6 +107,32 @@ def test_router_tile_size_keeps_routing_and_tolerance(case, rt):
         layer.close()
 
 
+@pytest.mark.parametrize("grid", [None, 37])
+def test_spatial_split_matches_oracle(case, grid):
+    # the plan's split of the CTAs into movers and GEMM workers, from the
+    # routed counts, against the oracle's fp32 statement of the same cost
+    # model with the kernel's constants (40 GB/s per mover, 1925 TF/s over
+    # 152 SMs per GEMM worker, 6.79 TB/s of weight stream)
+    w, inp, dev, ref = case
+    layer, out, routing = _run(w, dev, **({} if grid is None else dict(grid_ctas=grid)))
+    hz.check_out(out, ref)
+    counts = oracle.permute(oracle.route(inp["x"], inp["router_w"], inp["bias"], w.k)["idx"],
+                            w.E)[0]
+    N, ks = layer.stat("grid"), layer.stat("split_k")
+    rows = w.T * (w.k + w.S)
+    # the down projection's outputs are fp32 partials with a K split, or when
+    # the workspace reserved for this T holds an fp32 word per output
+    y_f32 = 1 if ks > 1 or rows * w.d * 4 <= (1 << 27) else 0
+    want, x = oracle.movers(w.T, w.d, w.f, w.k, w.S, int(np.count_nonzero(counts)), N, ks, y_f32,
+                            40e9, float(np.float32(1925e12) / np.float32(152)), 6.79e12)
+    got = layer.stat("mover_ctas")
+    if abs(x - np.floor(x) - 0.5) < 1e-3:  # fp32 contraction may tip a near tie
+        assert abs(got - want) <= 1, (got, want, x)
+    else:
+        assert got == want, (got, want, x)
+    layer.close()
+
+
 def test_dropped_notification_times_out_cleanly(case):
     import torch
     w, inp, dev, ref = case
