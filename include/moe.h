@@ -79,7 +79,9 @@ typedef struct moe_layer moe_layer_t;
 #define MOE_OPT_MOVER_CTAS 3   /* >0: fixed number of mover CTAs; 0 = model   */
 #define MOE_OPT_GRID_CTAS 4    /* >0: persistent grid size; 0 = one per SM    */
 #define MOE_OPT_SPLIT_K 5      /* down-projection K splits (1,2,4; 0 = auto)  */
-#define MOE_OPT_TOKENS_PER_TILE 6 /* max tokens per GEMM tile (16..256, %16) */
+#define MOE_OPT_TOKENS_PER_TILE 6 /* max tokens per GEMM tile: 0 = auto, else
+                                     16..256 in steps of 16, used rounded up
+                                     to a multiple of 32                       */
 #define MOE_OPT_FAULT_DROP_TASK 7 /* test only: -1 off; else drop the dependency
                                      notification of the n-th finished GEMM task,
                                      which must end in MOE_E_TIMEOUT            */
@@ -253,7 +255,10 @@ long long moe_layer_get_stat(moe_layer_t* h, int key);
  * number of records copied, or -1 on error. */
 int moe_layer_get_trace(moe_layer_t* h, uint64_t* records, int cap, void* stream);
 
-/* Bytes of device workspace moe_layer_reserve(T_max) allocates (host-only). */
+/* Bytes of device workspace moe_layer_reserve(T_max) allocates (host-only;
+ * -1 for a NULL handle or T_max < 0).  Not monotone in T_max: while four
+ * fp32 K-split partials of the down-projection outputs of T_max tokens fit
+ * in 512 MB the workspace holds them, beyond that only bf16 outputs. */
 long long moe_layer_workspace_bytes(const moe_layer_t* h, int T_max);
 
 /* Free the workspace and the handle.  NULL is ignored. */
