@@ -103,8 +103,32 @@ def _stream_ptr(stream):
     return ctypes.c_void_p(getattr(stream, "cuda_stream", stream))
 
 
+def _check_tensor(name, t, dtype, shape, rows_at_least=False):
+    """Refuse a tensor the kernels would read or write out of its bounds: wrong
+    dtype or shape, not contiguous, or not on a CUDA device.  ``shape`` is the
+    exact shape, except that with ``rows_at_least`` the first dimension may be
+    larger (an output buffer with room for more rows)."""
+    if t.dtype != dtype:
+        raise MoEError(MOE_E_INVAL, f"{name}: dtype {t.dtype}, expected {dtype}")
+    got = tuple(t.shape)
+    ok = (len(got) == len(shape) and got[1:] == tuple(shape[1:]) and
+          (got[0] >= shape[0] if rows_at_least else got[0] == shape[0]))
+    if not ok:
+        want = ("[>=%d, %s]" % (shape[0], ", ".join(map(str, shape[1:])))
+                if rows_at_least else str(list(shape)))
+        raise MoEError(MOE_E_INVAL, f"{name}: shape {list(got)}, expected {want}")
+    if not t.is_contiguous():
+        raise MoEError(MOE_E_INVAL, f"{name}: not contiguous")
+    if not t.is_cuda:
+        raise MoEError(MOE_E_INVAL, f"{name}: not a CUDA tensor")
+
+
 class MoELayer:
-    """One MoE layer handle (d, f, E, k, shared experts)."""
+    """One MoE layer handle (d, f, E, k, shared experts).
+
+    The tensor-taking methods check each tensor's dtype (bf16; the bias fp32),
+    shape, contiguity and device before the C call, so that a mismatched
+    tensor raises ``MoEError`` instead of being read out of bounds."""
 
     def __init__(self, d: int, f: int, E: int, k: int, shared_experts: int = 0):
         h = lib.moe_layer_create(d, f, E, k, shared_experts)
@@ -117,7 +141,23 @@ class MoELayer:
     def reserve(self, T_max: int, stream=None):
         _err(lib.moe_layer_reserve(self.h, T_max, _stream_ptr(stream)))
 
+    def _check_weights(self, router_w, w_gate, w_up, w_down):
+        import torch
+        bf, n = torch.bfloat16, self.E + self.S
+        _check_tensor("router_w", router_w, bf, (self.E, self.d))
+        _check_tensor("w_gate", w_gate, bf, (n, self.f, self.d))
+        _check_tensor("w_up", w_up, bf, (n, self.f, self.d))
+        _check_tensor("w_down", w_down, bf, (n, self.d, self.f))
+
+    def _check_rows(self, T, **rows):
+        import torch
+        for name, t in rows.items():
+            _check_tensor(name, t, torch.bfloat16, (T, self.d), rows_at_least=name != "x")
+
     def set_router_bias(self, bias):
+        if bias is not None:
+            import torch
+            _check_tensor("bias", bias, torch.float32, (self.E,))
         self._bias = bias  # keep the tensor alive while the library holds its pointer
         _err(lib.moe_layer_set_router_bias(self.h, None if bias is None else bias.data_ptr()))
 
@@ -126,6 +166,8 @@ class MoELayer:
 
     def forward(self, x, router_w, w_gate, w_up, w_down, out, stream=None):
         T = x.shape[0]
+        self._check_weights(router_w, w_gate, w_up, w_down)
+        self._check_rows(T, x=x, out=out)
         _err(lib.moe_layer_forward(self.h, T, x.data_ptr(), router_w.data_ptr(),
                                    w_gate.data_ptr(), w_up.data_ptr(), w_down.data_ptr(),
                                    out.data_ptr(), _stream_ptr(stream)))
@@ -135,7 +177,11 @@ class MoELayer:
                               out, norm_out, stream=None):
         """moe_layer_forward_residual_norm: out = residual + layer(x), norm_out =
         RMSNorm(out) * gamma, fused into the combine."""
+        import torch
         T = x.shape[0]
+        self._check_weights(router_w, w_gate, w_up, w_down)
+        self._check_rows(T, x=x, out=out, residual=residual, norm_out=norm_out)
+        _check_tensor("gamma", gamma, torch.bfloat16, (self.d,))
         _err(lib.moe_layer_forward_residual_norm(
             self.h, T, x.data_ptr(), router_w.data_ptr(), w_gate.data_ptr(), w_up.data_ptr(),
             w_down.data_ptr(), residual.data_ptr(), gamma.data_ptr(), float(eps), out.data_ptr(),
@@ -147,6 +193,8 @@ class MoELayer:
         on these inputs and keep the fastest as options; returns the best mean
         time in microseconds."""
         T = x.shape[0]
+        self._check_weights(router_w, w_gate, w_up, w_down)
+        self._check_rows(T, x=x, out=out)
         best = ctypes.c_float(0.0)
         _err(lib.moe_layer_calibrate(self.h, T, x.data_ptr(), router_w.data_ptr(),
                                      w_gate.data_ptr(), w_up.data_ptr(), w_down.data_ptr(),
@@ -157,6 +205,8 @@ class MoELayer:
     def forward_static(self, x, router_w, w_gate, w_up, w_down, out, stream=None):
         """moe_layer_forward_static: the same pass on the library's fixed scratch."""
         T = x.shape[0]
+        self._check_weights(router_w, w_gate, w_up, w_down)
+        self._check_rows(T, x=x, out=out)
         _err(lib.moe_layer_forward_static(self.h, T, x.data_ptr(), router_w.data_ptr(),
                                           w_gate.data_ptr(), w_up.data_ptr(), w_down.data_ptr(),
                                           out.data_ptr(), _stream_ptr(stream)))
@@ -164,6 +214,9 @@ class MoELayer:
 
     def forward_host(self, T, x_host_ptr, router_w, w_gate, w_up, w_down, out_host_ptr,
                      stream=None):
+        """moe_layer_forward_host: x and out are host addresses of T x d bf16
+        values each (pinned memory for asynchronous copies)."""
+        self._check_weights(router_w, w_gate, w_up, w_down)
         _err(lib.moe_layer_forward_host(self.h, T, x_host_ptr, router_w.data_ptr(),
                                         w_gate.data_ptr(), w_up.data_ptr(), w_down.data_ptr(),
                                         out_host_ptr, _stream_ptr(stream)))
