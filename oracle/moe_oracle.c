@@ -58,6 +58,14 @@
 #include <stdlib.h>
 #include <string.h>
 
+/* Scratch allocation: the oracle stops (abort) rather than compute on a NULL
+ * buffer when the host is out of memory. */
+static void* orc_alloc(size_t n, int zero) {
+  void* q = zero ? calloc(n ? n : 1, 1) : malloc(n ? n : 1);
+  if (!q) abort();
+  return q;
+}
+
 /* ---- bf16 <-> double ------------------------------------------------------ */
 
 double orc_bf16_to_f64(uint16_t b) {
@@ -125,8 +133,8 @@ void orc_router_logits(int T, int d, int E, const uint16_t* x, const uint16_t* w
  * largest logits (1e300 when k == E). */
 void orc_topk(int T, int E, int k, const double* L, int32_t* idx, double* w, double* p_full,
               double* gap) {
-  double* p = (double*)malloc(sizeof(double) * (size_t)E);
-  char* taken = (char*)malloc((size_t)E);
+  double* p = (double*)orc_alloc(sizeof(double) * (size_t)E, 0);
+  char* taken = (char*)orc_alloc((size_t)E, 0);
   for (int t = 0; t < T; ++t) {
     const double* l = L + (size_t)t * E;
     double mx = l[0];
@@ -209,8 +217,8 @@ int orc_permute(int T, int E, int k, const int32_t* idx, int32_t* counts, int32_
  * expert's [f, d] block, wd at its [d, f] block.  h_out (optional) gets h. */
 void orc_expert_ffn(int d, int f, const uint16_t* x_row, const uint16_t* wg, const uint16_t* wu,
                     const uint16_t* wd, double* h_out, double* y) {
-  double* h = (double*)malloc(sizeof(double) * (size_t)f);
-  double* xd = (double*)malloc(sizeof(double) * (size_t)d);
+  double* h = (double*)orc_alloc(sizeof(double) * (size_t)f, 0);
+  double* xd = (double*)orc_alloc(sizeof(double) * (size_t)d, 0);
   for (int i = 0; i < d; ++i) xd[i] = orc_bf16_to_f64(x_row[i]);
   for (int r = 0; r < f; ++r) {
     const uint16_t* gr = wg + (size_t)r * d;
@@ -241,8 +249,8 @@ void orc_expert_ffn(int d, int f, const uint16_t* x_row, const uint16_t* wg, con
 void orc_token_out(int d, int f, int E, int k, int S, const uint16_t* x_row, const int32_t* idx_row,
                    const double* w_row, const uint16_t* wg, const uint16_t* wu, const uint16_t* wd,
                    double* acc_out, uint16_t* out_row) {
-  double* acc = (double*)calloc((size_t)d, sizeof(double));
-  double* y = (double*)malloc(sizeof(double) * (size_t)d);
+  double* acc = (double*)orc_alloc(sizeof(double) * (size_t)d, 1);
+  double* y = (double*)orc_alloc(sizeof(double) * (size_t)d, 0);
   size_t fd = (size_t)f * (size_t)d;
   for (int j = 0; j < k; ++j) {
     int e = idx_row[j];
@@ -271,9 +279,9 @@ void orc_layer_tokens(int T, int d, int f, int E, int k, int S, const uint16_t* 
                       const uint16_t* wr, const float* bias, const uint16_t* wg,
                       const uint16_t* wu, const uint16_t* wd, int n_tok, const int32_t* tokens,
                       uint16_t* out_rows, double* acc_rows) {
-  double* L = (double*)malloc(sizeof(double) * (size_t)E);
-  int32_t* idx = (int32_t*)malloc(sizeof(int32_t) * (size_t)k);
-  double* w = (double*)malloc(sizeof(double) * (size_t)k);
+  double* L = (double*)orc_alloc(sizeof(double) * (size_t)E, 0);
+  int32_t* idx = (int32_t*)orc_alloc(sizeof(int32_t) * (size_t)k, 0);
+  double* w = (double*)orc_alloc(sizeof(double) * (size_t)k, 0);
   for (int n = 0; n < n_tok; ++n) {
     int t = tokens ? tokens[n] : n;
     if (t < 0 || t >= T) continue;
