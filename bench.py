@@ -114,6 +114,18 @@ def traffic_from_profiles(workload: str, mode: str):
     return float(ent["dram_bytes_per_launch"])
 
 
+def smi_device(dev: int) -> str:
+    """nvidia-smi's id of CUDA device `dev` of this process: with
+    CUDA_VISIBLE_DEVICES set, the entry it maps `dev` to (a physical index or a
+    GPU UUID, both accepted by nvidia-smi -i); otherwise `dev` itself."""
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        if 0 <= dev < len(ids):
+            return ids[dev]
+    return str(dev)
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle samples every 200 ms while running."""
 
@@ -130,7 +142,7 @@ class ClockSampler:
     def start(self):
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                ["nvidia-smi", "-i", smi_device(self.gpu), f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "200"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             threading.Thread(target=self._read, daemon=True).start()

@@ -46,3 +46,16 @@ def test_single_process_identity():
     import bench
     assert bench.reduce_max(3.5, "cpu") == 3.5
     assert bench.job_throughput(256, 1.0, 1) == pytest.approx(256000.0)
+
+
+def test_clock_sampler_follows_visible_devices(monkeypatch):
+    # the sampler must query the physical GPU the process runs on
+    import bench
+    monkeypatch.delenv("CUDA_VISIBLE_DEVICES", raising=False)
+    assert bench.smi_device(0) == "0"
+    monkeypatch.setenv("CUDA_VISIBLE_DEVICES", "5")
+    assert bench.smi_device(0) == "5"
+    monkeypatch.setenv("CUDA_VISIBLE_DEVICES", "3, 6")
+    assert bench.smi_device(1) == "6"
+    monkeypatch.setenv("CUDA_VISIBLE_DEVICES", "GPU-1234abcd-0000-1111-2222-333344445555")
+    assert bench.smi_device(0).startswith("GPU-1234abcd")
