@@ -1,14 +1,16 @@
 #!/usr/bin/env python
 """Benchmark of the MoE-layer forward megakernel on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload prefill]
                     [--mode persistent|multikernel|static] [--impl ours|reference]
                     [--residual-norm] [--option NAME=VALUE ...]
 
 One step = one forward pass of the whole layer (router, top-k, permute,
 gate/up + SiLU, down, combine) over one batch of synthetic tokens.  The default
-workload is the decode-sized 8-expert layer (T=256, d=4096, E=8, k=2,
-f=14336), the configuration the headline metric is quoted on.
+workload is the large prefill layer (T=8192, d=7168, E=256 routed experts plus
+one shared expert, k=8, f=2048): the largest of the five layer shapes, and the
+one a per-layer throughput figure with no named configuration is read on.
+The other shapes (tiny, decode, fine, skew) are selected with --workload.
 
 Prints ONE JSON line (rank 0):
   value      tokens/s over all ranks, inputs resident in HBM, device-timed with
@@ -57,7 +59,7 @@ def parse_args(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="decode", choices=list(gen.WORKLOADS))
+    ap.add_argument("--workload", default="prefill", choices=list(gen.WORKLOADS))
     ap.add_argument("--mode", default="persistent", choices=["persistent", "multikernel", "static"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=200)

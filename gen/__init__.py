@@ -18,7 +18,8 @@ skew      4096   4096   64   6   1408   0  fitted so counts follow Zipf(1.2)
 prefill   8192   7168   256  8   2048   1  b_e ~ N(0, 0.3^2)
 ========  =====  =====  ===  ==  =====  =  ==================================
 
-(``decode_small``: decode with f = 2048, a small case for profiler captures.)
+(``decode_small``: decode with f = 2048, and ``prefill_small``: prefill's
+expert shape with E = 32 and T = 1024, small cases for profiler captures.)
 
 Distributions: x ~ N(0, 1); router_w ~ N(0, 1/d); w_gate, w_up ~ N(0, 1/d);
 w_down ~ N(0, 1/f) ("N(0, 1/fan_in)" read as a variance).  Every workload uses
@@ -93,6 +94,10 @@ WORKLOADS = {
     # decode's shape with a narrower expert (f = 2048): 403 MB of weights, above
     # the L2 size, for profiling captures that must stay small
     "decode_small": Workload("decode_small", 256, 4096, 8, 2, 2048, 0, ()),
+    # prefill's expert shape (d = 7168, f = 2048, top-8, one shared expert) with
+    # 32 experts and 1024 tokens, so each expert still receives ~256 rows:
+    # 2.9 GB of weights, for profiling captures that must stay small
+    "prefill_small": Workload("prefill_small", 1024, 7168, 32, 8, 2048, 1, ("normal", 0.3)),
 }
 
 

@@ -43,8 +43,8 @@
  *     message of the last failure on the calling thread is moe_last_error();
  *   - a handle serves one stream at a time; calls on one handle are not
  *     thread-safe.
- * Limits: d % 128 == 0, f % 128 == 0, 1 <= k <= E <= 256, k <= 16, S <= 1,
- * 0 <= T <= T_max given to moe_layer_reserve, T_max <= 32768.
+ * Limits: d % 128 == 0, d <= 32768, f % 128 == 0, 1 <= k <= E <= 256,
+ * k <= 16, S <= 1, 0 <= T <= T_max given to moe_layer_reserve, T_max <= 32768.
  */
 #ifndef MOE_H_
 #define MOE_H_
@@ -130,9 +130,14 @@ typedef struct moe_layer moe_layer_t;
 #define MOE_STAT_TILE_TOKENS 9 /* max tokens per GEMM tile of the last forward */
 #define MOE_STAT_SPLIT_K 10    /* down-projection K splits of the last forward */
 #define MOE_STAT_BANDS 11      /* d bands of the last forward (1 or 2)         */
+#define MOE_STAT_Y_BYTES 12    /* bytes the combine read per down-projection
+                                  output value in the last forward: 2 (bf16
+                                  outputs) or 4 * split_k (fp32 partials)     */
 
 /* Create a layer description.  Pure host call (no CUDA call, no allocation on
- * the device).  Returns NULL on invalid dimensions (see moe_last_error). */
+ * the device).  Returns NULL on invalid dimensions (see moe_last_error),
+ * among them d > 32768: a gather copies whole bf16 token rows through the
+ * pipeline's shared memory, which holds a 64 KB row under every tiling. */
 moe_layer_t* moe_layer_create(int d, int f, int E, int k, int shared_experts);
 
 /* Allocate the device workspace for up to T_max tokens on the current device

@@ -62,7 +62,7 @@ def _L():
         lib.orc_layer_tokens.argtypes = [i32] * 6 + [vp] * 6 + [i32, vp, vp, vp]
         lib.orc_residual_rmsnorm.argtypes = [i32, i32, vp, vp, vp, dbl, vp, vp, vp]
         flt = ctypes.c_float
-        lib.orc_movers.argtypes = [i32] * 9 + [flt, flt, flt, ctypes.POINTER(flt)]
+        lib.orc_movers.argtypes = [i32] * 7 + [flt, flt, flt, flt, ctypes.POINTER(flt)]
         lib.orc_movers.restype = i32
         for fn in (lib.orc_bf16_to_f64_array, lib.orc_f64_to_bf16_array, lib.orc_router_logits,
                    lib.orc_topk, lib.orc_expert_ffn, lib.orc_token_out, lib.orc_layer_tokens,
@@ -223,20 +223,20 @@ def residual_rmsnorm(acc, residual, gamma, eps: float):
     return out, norm, norm64
 
 
-def movers(T: int, d: int, f: int, k: int, S: int, touched_routed: int, N: int, ks: int,
-           y_f32: int, beta: float, phi: float, bw: float):
+def movers(T: int, d: int, f: int, k: int, S: int, touched_routed: int, N: int,
+           ybytes: float, beta: float, phi: float, bw: float):
     """The spatial split of the Weave abstract (CTAs for data movement against
     CTAs for the expert GEMMs, in the ratio of the two sides' work once
     routing is known), as ``moe_oracle.c: orc_movers`` defines it.
 
-    touched_routed: routed experts with at least one token; N: CTAs; ks, y_f32:
-    the K splits of the down projection and whether its outputs are stored as
-    fp32 partials (they set the bytes the combine reads); beta (B/s per mover),
-    phi (FLOP/s per GEMM worker), bw (B/s): the cost model's constants, each
-    rounded to fp32 like the rest of the arithmetic.  Returns (M*, the value
-    N*a/(a+b) before rounding)."""
+    touched_routed: routed experts with at least one token; N: CTAs; ybytes:
+    bytes the combine reads per expert-output value (2 for bf16 outputs, 4 * ks
+    for ks fp32 partial sums); beta (B/s per mover), phi (FLOP/s per GEMM
+    worker), bw (B/s): the cost model's constants, each rounded to fp32 like
+    the rest of the arithmetic.  Returns (M*, the value N*a/(a+b) before
+    rounding)."""
     m_cont = ctypes.c_float(0.0)
     m = _L().orc_movers(int(T), int(d), int(f), int(k), int(S), int(touched_routed), int(N),
-                        int(ks), int(y_f32), float(np.float32(beta)), float(np.float32(phi)),
-                        float(np.float32(bw)), ctypes.byref(m_cont))
+                        float(np.float32(ybytes)), float(np.float32(beta)),
+                        float(np.float32(phi)), float(np.float32(bw)), ctypes.byref(m_cont))
     return int(m), float(m_cont.value)

@@ -338,10 +338,10 @@ void orc_residual_rmsnorm(int n, int d, const double* acc, const uint16_t* resid
  * sides' throughputs match.  The page gives no formula; this project reads it
  * as follows, with the work of each side in worker-seconds:
  *   a = B_move / beta                      bytes the movers copy, at beta B/s
- *       B_move = T*k rows gathered (read and write d bf16 values each)
- *              + T*(k+S) expert-output rows read by the combine, d values of
- *                ybytes each (4*ks for ks fp32 K-split partials, else 2)
- *              + T rows written by the combine (d bf16 values each)
+ *       B_move = T*k rows gathered          (each read and written: 2 * d * 2 B)
+ *              + T*(k+S) expert-output rows read by the combine (d * ybytes B
+ *                each: every routed slot and the shared expert's row)
+ *              + T rows written by the combine (d * 2 B each)
  *   b = max(F / phi, N * G_w / BW)         the GEMM side: its FLOPs at phi
  *       F   = 6 * d * f per routed or shared row (T*k + T*S rows)   FLOP/s per
  *       G_w = 3 * f * d bf16 weights per touched expert              worker,
@@ -349,12 +349,15 @@ void orc_residual_rmsnorm(int n, int d, const double* acc, const uint16_t* resid
  *                                                  weight stream at BW for N
  *   M* = clamp(round(N * a / (a + b)), 1, N - 1)   (N * a / (a + b) minimises
  *        max(a / M, b / (N - M)), the slower side's time, over real M)
+ * ybytes is the size in bytes of one stored expert-output value, summed over
+ * the pieces the combine reads for it: 2 when the outputs are kept as bf16,
+ * 4 * ks when they are kept as ks fp32 partial sums of a K-split down
+ * projection (the caller passes the size of the layout in use).
  * M* is an integer decided by floating point, so it is computed in fp32, the
  * precision the kernel decides in, rounding half to even; *m_cont receives
  * N * a / (a + b) before rounding. */
-int orc_movers(int T, int d, int f, int k, int S, int touched_routed, int N, int ks, int y_f32,
+int orc_movers(int T, int d, int f, int k, int S, int touched_routed, int N, float ybytes,
                float beta, float phi, float bw, float* m_cont) {
-  const float ybytes = y_f32 ? 4.0f * (float)ks : 2.0f;
   const float Tk = (float)T * (float)k;
   const float gather = Tk * (float)d * 2.0f * 2.0f;
   const float combine_read = ((float)T * (float)(k + S)) * (float)d * ybytes;

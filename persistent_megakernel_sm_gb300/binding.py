@@ -25,7 +25,7 @@ OPTIONS = {
     "trace": 10, "release": 11, "prefetch": 12, "bands": 13, "route_splits": 14, "l2_prefetch": 15,
 }
 STATS = {"mover_ctas": 1, "tasks": 2, "grid": 3, "gemm_tasks": 4, "mover_tasks": 5, "stolen": 6,
-         "ahead": 7, "trace_records": 8, "tile_tokens": 9, "split_k": 10, "bands": 11}
+         "ahead": 7, "trace_records": 8, "tile_tokens": 9, "split_k": 10, "bands": 11, "y_bytes": 12}
 TASK_TYPES = {1: "route", 2: "gather", 3: "gateup", 4: "down", 5: "combine", 6: "plan"}
 
 _vp, _i32, _i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong

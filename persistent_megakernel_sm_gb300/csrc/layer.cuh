@@ -25,6 +25,7 @@ constexpr int kMaxRouteKs = 8;      // K splits of a router tile, at most
 constexpr int kShards = 8;          // shards of each task queue
 constexpr int kMaxE = 256;
 constexpr int kMaxK = 16;
+constexpr int kMaxD = 32768;        // model dim limit: one bf16 row (64 KB) fits a gather round
 constexpr int kTmemCols = 512;
 constexpr int kAcc1Col = 256;       // second accumulator's first TMEM column
 

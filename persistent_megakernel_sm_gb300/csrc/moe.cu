@@ -612,6 +612,7 @@ struct moe_layer {
   bool last_valid = false;
   int last_grid = 0;
   int last_bn = 0, last_ks = 0, last_bands = 0;  // tiling of the last forward
+  int last_ybytes = 0;  // bytes the combine reads per expert-output value
   int last_T = 0;
 };
 
@@ -761,6 +762,12 @@ const char* moe_last_error(void) { return g_err.c_str(); }
 moe_layer_t* moe_layer_create(int d, int f, int E, int k, int shared_experts) {
   if (d <= 0 || d % 128 != 0) {
     g_err = "d must be a positive multiple of 128";
+    return nullptr;
+  }
+  if (d > kMaxD) {
+    // a gather task stages whole bf16 token rows in the pipeline's shared
+    // memory (at least ~145 KB under every tiling): rows of up to 64 KB fit
+    g_err = "d must be at most 32768";
     return nullptr;
   }
   if (f <= 0 || f % 128 != 0) {
@@ -1115,6 +1122,7 @@ int forward_impl(moe_layer_t* h, int T, const void* x, const void* router_w, con
   h->last_bn = tl.bn;
   h->last_ks = tl.ks;
   h->last_bands = p.n_bands;
+  h->last_ybytes = p.y_f32 ? 4 * p.ks : 2;
   return MOE_OK;
 }
 
@@ -1279,6 +1287,7 @@ long long moe_layer_get_stat(moe_layer_t* h, int key) {
   if (key == MOE_STAT_TILE_TOKENS) return h->last_T ? h->last_bn : -1;
   if (key == MOE_STAT_SPLIT_K) return h->last_T ? h->last_ks : -1;
   if (key == MOE_STAT_BANDS) return h->last_T ? h->last_bands : -1;
+  if (key == MOE_STAT_Y_BYTES) return h->last_T ? h->last_ybytes : -1;
   if (!h->last_valid) return -1;
   switch (key) {
     case MOE_STAT_MOVER_CTAS: return h->last.n_movers;

@@ -36,6 +36,8 @@ def test_library_exports_every_declared_symbol(lib):
     ((256, 512, 300, 2, 0), False),   # E > 256
     ((256, 512, 64, 17, 0), False),   # k > 16
     ((256, 512, 8, 2, 2), False),     # two shared experts
+    ((32768, 512, 8, 2, 0), True),    # the largest d: a 64 KB row fits a gather round
+    ((32896, 512, 8, 2, 0), False),   # d > 32768: a row could overrun the gather's stages
 ])
 def test_create_validates(lib, args, ok):
     h = lib.moe_layer_create(*args)

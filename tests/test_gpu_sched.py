@@ -118,12 +118,12 @@ def test_spatial_split_matches_oracle(case, grid):
     hz.check_out(out, ref)
     counts = oracle.permute(oracle.route(inp["x"], inp["router_w"], inp["bias"], w.k)["idx"],
                             w.E)[0]
-    N, ks = layer.stat("grid"), layer.stat("split_k")
-    rows = w.T * (w.k + w.S)
-    # the down projection's outputs are fp32 partials with a K split, or when
-    # the workspace reserved for this T holds an fp32 word per output
-    y_f32 = 1 if ks > 1 or rows * w.d * 4 <= (1 << 27) else 0
-    want, x = oracle.movers(w.T, w.d, w.f, w.k, w.S, int(np.count_nonzero(counts)), N, ks, y_f32,
+    N = layer.stat("grid")
+    # the combine reads each expert output as stored: bf16 (2 bytes) or ks
+    # fp32 partial sums (4 ks bytes), whichever layout this forward used
+    ybytes = layer.stat("y_bytes")
+    assert ybytes in (2, 4, 8, 16)
+    want, x = oracle.movers(w.T, w.d, w.f, w.k, w.S, int(np.count_nonzero(counts)), N, ybytes,
                             40e9, float(np.float32(1925e12) / np.float32(152)), 6.79e12)
     got = layer.stat("mover_ctas")
     if abs(x - np.floor(x) - 0.5) < 1e-3:  # fp32 contraction may tip a near tie

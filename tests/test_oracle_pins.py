@@ -371,10 +371,11 @@ def test_residual_rmsnorm_constant_row_gives_signed_gamma():
 PHI32 = float(np.float32(1925e12) / np.float32(152))
 
 
-def _work_by_enumeration(T, d, f, k, S, touched, ks, y_f32):
+def _work_by_enumeration(T, d, f, k, S, touched, ybytes):
     """Mover bytes, GEMM FLOPs and weight bytes of a layer, counted copy by
-    copy, row by row and matrix by matrix (exact integers)."""
-    ybytes = 4 * ks if y_f32 else 2
+    copy, row by row and matrix by matrix (exact integers); ybytes is the size
+    of one stored expert-output value the combine reads (2: bf16; 4 * ks: ks
+    fp32 partial sums)."""
     moved = 0
     for _ in range(T * k):          # gather: a token row read, a permuted row written
         moved += d * 2 + d * 2
@@ -399,8 +400,8 @@ def _random_layers(n, seed):
         yield dict(T=int(rng.integers(1, 48)), d=64 * int(rng.integers(1, 65)),
                    f=64 * int(rng.integers(1, 65)), k=int(rng.integers(1, min(E, 16) + 1)),
                    S=int(rng.integers(0, 2)), touched=int(rng.integers(1, E + 1)),
-                   N=int(rng.integers(1, 300)), ks=int(rng.choice([1, 2, 4])),
-                   y_f32=int(rng.integers(0, 2)), beta=float(10.0 ** rng.uniform(8, 12)),
+                   N=int(rng.integers(1, 300)), ybytes=int(rng.choice([2, 4, 8, 16])),
+                   beta=float(10.0 ** rng.uniform(8, 12)),
                    phi=float(10.0 ** rng.uniform(10, 14)), bw=float(10.0 ** rng.uniform(11, 13)))
 
 
@@ -411,12 +412,12 @@ def test_movers_minimise_the_slower_side(seed):
     # the slower side's time max(a / M, b / (N - M)) over M = 1 .. N - 1
     for c in _random_layers(150, seed):
         moved, flops, wbytes = _work_by_enumeration(c["T"], c["d"], c["f"], c["k"], c["S"],
-                                                    c["touched"], c["ks"], c["y_f32"])
+                                                    c["touched"], c["ybytes"])
         beta, phi, bw = (float(np.float32(c[key])) for key in ("beta", "phi", "bw"))
         a = moved / beta
         b = max(flops / phi, c["N"] * wbytes / bw)
         m, x = oracle.movers(c["T"], c["d"], c["f"], c["k"], c["S"], c["touched"], c["N"],
-                             c["ks"], c["y_f32"], c["beta"], c["phi"], c["bw"])
+                             c["ybytes"], c["beta"], c["phi"], c["bw"])
         assert abs(x - c["N"] * a / (a + b)) <= 1e-5 * c["N"], c
         N = c["N"]
         if N == 1:
@@ -430,47 +431,47 @@ def test_movers_minimise_the_slower_side(seed):
 def test_movers_follow_a_three_to_one_ratio():
     # movers' work three times the GEMM side's: three quarters of the CTAs
     # move data (a swap of the two sides would give one quarter)
-    T, d, f, k, S, touched, ks, y_f32, N = 32, 512, 256, 4, 1, 6, 2, 1, 16
-    moved, flops, wbytes = _work_by_enumeration(T, d, f, k, S, touched, ks, y_f32)
+    T, d, f, k, S, touched, ybytes, N = 32, 512, 256, 4, 1, 6, 8, 16
+    moved, flops, wbytes = _work_by_enumeration(T, d, f, k, S, touched, ybytes)
     bw = 6.79e12
     b = max(flops / PHI32, N * wbytes / float(np.float32(bw)))
     beta = moved / (3.0 * b)
-    m, x = oracle.movers(T, d, f, k, S, touched, N, ks, y_f32, beta, PHI32, bw)
+    m, x = oracle.movers(T, d, f, k, S, touched, N, ybytes, beta, PHI32, bw)
     assert abs(x - 12.0) < 1e-4 and m == 12
-    m, x = oracle.movers(T, d, f, k, S, touched, N, ks, y_f32, moved / (b / 3.0), PHI32, bw)
+    m, x = oracle.movers(T, d, f, k, S, touched, N, ybytes, moved / (b / 3.0), PHI32, bw)
     assert abs(x - 4.0) < 1e-4 and m == 4
 
 
 def test_movers_round_to_the_nearest_split():
     # with a / b = 0.27 / 0.73 the real split of 10 CTAs is 2.7 movers, which
     # rounds to 3; with 0.23 / 0.77 it is 2.3, which rounds to 2
-    T, d, f, k, S, touched, ks, y_f32, N = 16, 256, 512, 2, 0, 3, 1, 0, 10
-    moved, flops, wbytes = _work_by_enumeration(T, d, f, k, S, touched, ks, y_f32)
+    T, d, f, k, S, touched, ybytes, N = 16, 256, 512, 2, 0, 3, 2, 10
+    moved, flops, wbytes = _work_by_enumeration(T, d, f, k, S, touched, ybytes)
     bw = 6.79e12
     b = max(flops / PHI32, N * wbytes / float(np.float32(bw)))
     for frac, want in ((0.27, 3), (0.23, 2)):
         beta = moved / (frac / (1.0 - frac) * b)
-        m, x = oracle.movers(T, d, f, k, S, touched, N, ks, y_f32, beta, PHI32, bw)
+        m, x = oracle.movers(T, d, f, k, S, touched, N, ybytes, beta, PHI32, bw)
         assert abs(x - 10 * frac) < 1e-4 and m == want
 
 
 def test_movers_clamps():
     args = (64, 256, 256, 2, 0, 4)
     # data movement dwarfs the GEMMs: all CTAs but one move data
-    assert oracle.movers(*args, 16, 1, 1, 1e3, PHI32, 6.79e12)[0] == 15
+    assert oracle.movers(*args, 16, 4, 1e3, PHI32, 6.79e12)[0] == 15
     # the GEMMs dwarf data movement: one mover is kept
-    assert oracle.movers(*args, 16, 1, 1, 1e30, PHI32, 6.79e12)[0] == 1
+    assert oracle.movers(*args, 16, 4, 1e30, PHI32, 6.79e12)[0] == 1
     # one or two CTAs: a single mover (the other side shares it or the last CTA)
     for beta in (1e3, 1e30):
-        assert oracle.movers(*args, 1, 1, 1, beta, PHI32, 6.79e12)[0] == 1
-        assert oracle.movers(*args, 2, 1, 1, beta, PHI32, 6.79e12)[0] == 1
+        assert oracle.movers(*args, 1, 4, beta, PHI32, 6.79e12)[0] == 1
+        assert oracle.movers(*args, 2, 4, beta, PHI32, 6.79e12)[0] == 1
 
 
 def test_movers_fall_as_more_experts_are_touched():
     # more touched experts means more weight bytes on the GEMM side
     prev = None
     for touched in range(1, 129, 8):
-        m, _ = oracle.movers(512, 2048, 768, 8, 0, touched, 152, 1, 1, 40e9, PHI32, 6.79e12)
+        m, _ = oracle.movers(512, 2048, 768, 8, 0, touched, 152, 4, 40e9, PHI32, 6.79e12)
         assert prev is None or m <= prev
         prev = m
-    assert prev < oracle.movers(512, 2048, 768, 8, 0, 1, 152, 1, 1, 40e9, PHI32, 6.79e12)[0]
+    assert prev < oracle.movers(512, 2048, 768, 8, 0, 1, 152, 4, 40e9, PHI32, 6.79e12)[0]
