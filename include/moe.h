@@ -133,6 +133,8 @@ typedef struct moe_layer moe_layer_t;
 #define MOE_STAT_Y_BYTES 12    /* bytes the combine read per down-projection
                                   output value in the last forward: 2 (bf16
                                   outputs) or 4 * split_k (fp32 partials)     */
+#define MOE_STAT_COMBINE_TOKENS 13 /* tokens per combine tile of the last
+                                      forward                                  */
 
 /* Create a layer description.  Pure host call (no CUDA call, no allocation on
  * the device).  Returns NULL on invalid dimensions (see moe_last_error),
@@ -189,27 +191,34 @@ int moe_layer_forward_host(moe_layer_t* h, int T, const void* x_host, const void
                            void* out_host, void* stream);
 
 /* The same forward pass without any allocation, for callers that cannot call
- * cudaMalloc: code that runs while a stream is being captured into a CUDA
- * graph, hosts whose device memory is owned by another allocator, and
- * embedded runtimes that forbid allocation after start-up.  (The pages have
- * no counterpart: this is an interface convenience, not part of the method.)
- * Needs only moe_layer_create (host memory); no moe_layer_reserve.  Its
- * scratch is a fixed 32 MiB array inside this library's device code, which
- * every GPU that loads the library holds until the process exits.  Layers
- * whose workspace for T tokens exceeds it are rejected with MOE_E_INVAL and
- * a message naming the size needed (the decode-sized layer, T=256 d=4096
- * E=8 k=2 f=14336, fits).  The first call on a device looks up the scratch
- * array's device address and sets kernel attributes (no allocation); make
- * that first call before any stream capture.  Every call on a device shares
- * the one array and the array keeps the last call's contents: the scheduler
- * state is cleared at each call, but calls that overlap on the GPU (two
- * streams, two threads) race on it.  Inputs, outputs, layouts, options and
- * the asynchronous behaviour are those of moe_layer_forward; device-side
- * status of these calls is not reported by moe_layer_status, and
- * moe_layer_get_routing / moe_layer_get_trace do not cover them. */
-int moe_layer_forward_static(moe_layer_t* h, int T, const void* x, const void* router_w,
-                             const void* w_gate, const void* w_up, const void* w_down, void* out,
-                             void* stream);
+ * cudaMalloc: processes whose device memory is owned by another allocator (a
+ * framework's caching allocator that must account for every byte), and
+ * runtimes that forbid allocation after start-up (fixed memory budgets,
+ * real-time or certified deployments).  (The pages have no counterpart: this
+ * is an interface convenience, not part of the method.)  Needs only
+ * moe_layer_create (host memory); no moe_layer_reserve.  Its scratch is a
+ * fixed 32 MiB array inside this library's device code, which every GPU that
+ * loads the library holds until the process exits.  Layers whose workspace
+ * for T tokens exceeds it are rejected with MOE_E_INVAL and a message naming
+ * the size needed (the decode-sized layer, T=256 d=4096 E=8 k=2 f=14336,
+ * fits).  The first call on a device looks up the scratch array's device
+ * address and sets kernel attributes (no allocation); make that first call
+ * before any stream capture.  Later calls look the address up again and
+ * redo that set-up if it changed (after a device reset).  Every call on a
+ * device shares the one array and the array keeps the last call's contents:
+ * the scheduler state is cleared at each call, but calls that overlap on the
+ * GPU (two streams, two threads, two handles) race on it.  Inputs, outputs,
+ * layouts, options and the asynchronous behaviour are those of
+ * moe_layer_forward.  When the fp32 K-split partials of the down projection
+ * do not fit the scratch, it keeps them in bf16 with one K split, so its
+ * results may differ from moe_layer_forward's in the last bits (both stay
+ * within the oracle's tolerance).  After a call, moe_layer_status and
+ * moe_layer_get_routing on the same handle report this call (read from the
+ * shared array: call them before another no-allocation forward runs on the
+ * device); moe_layer_get_trace does not cover these calls. */
+int moe_layer_forward_noalloc(moe_layer_t* h, int T, const void* x, const void* router_w,
+                              const void* w_gate, const void* w_up, const void* w_down, void* out,
+                              void* stream);
 
 /* Copy the routing of the last forward into caller device buffers (any may be
  * NULL): idx int32 [T,k], w fp32 [T,k] (renormalised weights, slot order),

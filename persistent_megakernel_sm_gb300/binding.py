@@ -25,7 +25,8 @@ OPTIONS = {
     "trace": 10, "release": 11, "prefetch": 12, "bands": 13, "route_splits": 14, "l2_prefetch": 15,
 }
 STATS = {"mover_ctas": 1, "tasks": 2, "grid": 3, "gemm_tasks": 4, "mover_tasks": 5, "stolen": 6,
-         "ahead": 7, "trace_records": 8, "tile_tokens": 9, "split_k": 10, "bands": 11, "y_bytes": 12}
+         "ahead": 7, "trace_records": 8, "tile_tokens": 9, "split_k": 10, "bands": 11, "y_bytes": 12,
+         "combine_tokens": 13}
 TASK_TYPES = {1: "route", 2: "gather", 3: "gateup", 4: "down", 5: "combine", 6: "plan"}
 
 _vp, _i32, _i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong
@@ -36,7 +37,7 @@ _SIGNATURES = {
     "moe_layer_set_router_bias": ([_vp, _vp], _i32),
     "moe_layer_forward": ([_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp], _i32),
     "moe_layer_forward_host": ([_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp], _i32),
-    "moe_layer_forward_static": ([_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp], _i32),
+    "moe_layer_forward_noalloc": ([_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp], _i32),
     "moe_layer_forward_residual_norm": ([_vp, _i32] + [_vp] * 7 + [ctypes.c_float, _vp, _vp, _vp],
                                         _i32),
     "moe_layer_calibrate": ([_vp, _i32] + [_vp] * 6 + [_i32, _vp, _vp], _i32),
@@ -202,12 +203,13 @@ class MoELayer:
                                      _stream_ptr(stream)))
         return best.value
 
-    def forward_static(self, x, router_w, w_gate, w_up, w_down, out, stream=None):
-        """moe_layer_forward_static: the same pass on the library's fixed scratch."""
+    def forward_noalloc(self, x, router_w, w_gate, w_up, w_down, out, stream=None):
+        """moe_layer_forward_noalloc: the same pass on the library's fixed scratch,
+        allocating nothing (for callers that cannot allocate device memory)."""
         T = x.shape[0]
         self._check_weights(router_w, w_gate, w_up, w_down)
         self._check_rows(T, x=x, out=out)
-        _err(lib.moe_layer_forward_static(self.h, T, x.data_ptr(), router_w.data_ptr(),
+        _err(lib.moe_layer_forward_noalloc(self.h, T, x.data_ptr(), router_w.data_ptr(),
                                           w_gate.data_ptr(), w_up.data_ptr(), w_down.data_ptr(),
                                           out.data_ptr(), _stream_ptr(stream)))
         return out

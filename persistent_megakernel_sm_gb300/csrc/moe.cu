@@ -498,11 +498,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 using namespace moe;
 
-// Scratch of moe_layer_forward_static: a file-scope device array, so that
+// Scratch of moe_layer_forward_noalloc: a file-scope device array, so that
 // entry point needs no allocation call.  Every GPU that loads this library
 // holds it until the process exits.
-constexpr size_t kStaticScratchBytes = 32u << 20;
-static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+constexpr size_t kNoallocScratchBytes = 32u << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
 namespace {
 
@@ -604,6 +604,12 @@ struct moe_layer {
   size_t o_idx, o_wgt, o_rank, o_tile, o_counts, o_offsets, o_perm, o_pos, o_xp, o_h, o_y,
       o_groups, o_rpart, o_rsd, o_rmask, o_zero, o_gd, o_gu, o_cd, o_nd, o_sched, o_zero_end, o_ring, o_ring_m, o_ring_g, o_ring_gl,
       o_ring_end;
+  // where the last forward's routing and scheduler state live: the reserved
+  // workspace, or the no-allocation entry point's scratch array
+  struct View {
+    char* ws = nullptr;
+    size_t o_idx = 0, o_wgt = 0, o_counts = 0, o_offsets = 0, o_perm = 0, o_pos = 0, o_sched = 0;
+  } view;
   // host staging for moe_layer_forward_host
   void* x_dev_stage = nullptr;
   void* out_dev_stage = nullptr;
@@ -613,6 +619,7 @@ struct moe_layer {
   int last_grid = 0;
   int last_bn = 0, last_ks = 0, last_bands = 0;  // tiling of the last forward
   int last_ybytes = 0;  // bytes the combine reads per expert-output value
+  int last_ct = 0;      // tokens per combine tile
   int last_T = 0;
 };
 
@@ -1117,12 +1124,21 @@ int forward_impl(moe_layer_t* h, int T, const void* x, const void* router_w, con
     k_combine<<<p.n_comb, kThreads, tl.smem, s>>>(p, m);
     CK(cudaGetLastError());
   }
+  h->view.ws = h->ws;
+  h->view.o_idx = h->o_idx;
+  h->view.o_wgt = h->o_wgt;
+  h->view.o_counts = h->o_counts;
+  h->view.o_offsets = h->o_offsets;
+  h->view.o_perm = h->o_perm;
+  h->view.o_pos = h->o_pos;
+  h->view.o_sched = h->o_sched;
   h->last_valid = false;
   h->last_T = T;
   h->last_bn = tl.bn;
   h->last_ks = tl.ks;
   h->last_bands = p.n_bands;
   h->last_ybytes = p.y_f32 ? 4 * p.ks : 2;
+  h->last_ct = p.ct;
   return MOE_OK;
 }
 
@@ -1248,21 +1264,22 @@ int moe_layer_forward_host(moe_layer_t* h, int T, const void* x_host, const void
 
 int moe_layer_get_routing(moe_layer_t* h, int32_t* idx, float* w, int32_t* counts,
                           int32_t* offsets, int32_t* perm, int32_t* pos, void* stream) {
-  if (!h || !h->ws) return fail(MOE_E_STATE, "no workspace");
+  if (!h || !h->view.ws) return fail(MOE_E_STATE, "no forward has run on this handle");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // sizes of the last forward are not kept on the host; copy T_max-sized
   // regions would overrun small caller buffers, so the caller passes buffers
   // sized for the T of the last forward and we copy exactly that much.
   const int T = h->last_T;
   const size_t Tk = (size_t)T * h->k;
-  char* ws = h->ws;
-  if (idx) CK(cudaMemcpyAsync(idx, ws + h->o_idx, Tk * 4, cudaMemcpyDeviceToDevice, s));
-  if (w) CK(cudaMemcpyAsync(w, ws + h->o_wgt, Tk * 4, cudaMemcpyDeviceToDevice, s));
-  if (counts) CK(cudaMemcpyAsync(counts, ws + h->o_counts, h->E * 4, cudaMemcpyDeviceToDevice, s));
+  const auto& v = h->view;
+  char* ws = v.ws;
+  if (idx) CK(cudaMemcpyAsync(idx, ws + v.o_idx, Tk * 4, cudaMemcpyDeviceToDevice, s));
+  if (w) CK(cudaMemcpyAsync(w, ws + v.o_wgt, Tk * 4, cudaMemcpyDeviceToDevice, s));
+  if (counts) CK(cudaMemcpyAsync(counts, ws + v.o_counts, h->E * 4, cudaMemcpyDeviceToDevice, s));
   if (offsets)
-    CK(cudaMemcpyAsync(offsets, ws + h->o_offsets, (h->E + 1) * 4, cudaMemcpyDeviceToDevice, s));
-  if (perm) CK(cudaMemcpyAsync(perm, ws + h->o_perm, Tk * 4, cudaMemcpyDeviceToDevice, s));
-  if (pos) CK(cudaMemcpyAsync(pos, ws + h->o_pos, Tk * 4, cudaMemcpyDeviceToDevice, s));
+    CK(cudaMemcpyAsync(offsets, ws + v.o_offsets, (h->E + 1) * 4, cudaMemcpyDeviceToDevice, s));
+  if (perm) CK(cudaMemcpyAsync(perm, ws + v.o_perm, Tk * 4, cudaMemcpyDeviceToDevice, s));
+  if (pos) CK(cudaMemcpyAsync(pos, ws + v.o_pos, Tk * 4, cudaMemcpyDeviceToDevice, s));
   return MOE_OK;
 }
 
@@ -1271,13 +1288,14 @@ int moe_layer_status(moe_layer_t* h, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-  if (!h->ws) return MOE_OK;
-  CK(cudaMemcpy(&h->last, h->ws + h->o_sched, sizeof(Sched), cudaMemcpyDeviceToHost));
+  char* sched = h->view.ws ? h->view.ws + h->view.o_sched : nullptr;
+  if (!sched) return MOE_OK;
+  CK(cudaMemcpy(&h->last, sched, sizeof(Sched), cudaMemcpyDeviceToHost));
   h->last_valid = true;
   const int rc = set_error_from_sched(h->last);
   if (rc) {
     int zero = 0;
-    CK(cudaMemcpy(h->ws + h->o_sched, &zero, sizeof(int), cudaMemcpyHostToDevice));
+    CK(cudaMemcpy(sched, &zero, sizeof(int), cudaMemcpyHostToDevice));
   }
   return rc;
 }
@@ -1288,6 +1306,7 @@ long long moe_layer_get_stat(moe_layer_t* h, int key) {
   if (key == MOE_STAT_SPLIT_K) return h->last_T ? h->last_ks : -1;
   if (key == MOE_STAT_BANDS) return h->last_T ? h->last_bands : -1;
   if (key == MOE_STAT_Y_BYTES) return h->last_T ? h->last_ybytes : -1;
+  if (key == MOE_STAT_COMBINE_TOKENS) return h->last_T ? h->last_ct : -1;
   if (!h->last_valid) return -1;
   switch (key) {
     case MOE_STAT_MOVER_CTAS: return h->last.n_movers;
@@ -1328,17 +1347,22 @@ int moe_layer_get_trace(moe_layer_t* h, uint64_t* records, int cap, void* stream
 }
 
 /* See include/moe.h.  Runs the unchanged moe_layer_forward on a copy of the
- * handle whose workspace is the file-scope scratch array above. */
-int moe_layer_forward_static(moe_layer_t* h, int T, const void* x, const void* router_w,
-                             const void* w_gate, const void* w_up, const void* w_down, void* out,
-                             void* stream) {
+ * handle whose workspace is the file-scope scratch array above, then points
+ * the caller's handle at that copy's routing and scheduler state, so that
+ * moe_layer_status and moe_layer_get_routing report this call. */
+int moe_layer_forward_noalloc(moe_layer_t* h, int T, const void* x, const void* router_w,
+                              const void* w_gate, const void* w_up, const void* w_down, void* out,
+                              void* stream) {
   if (!h) return fail(MOE_E_INVAL, "null handle");
   if (T < 0) return fail(MOE_E_INVAL, "T must be >= 0");
   if (T == 0) return MOE_OK;
   if (T > kMaxE * kRouteTokens) return fail(MOE_E_INVAL, "T out of range (1..32768)");
-  // One-time set-up per device, with that device current: the scratch
-  // array's device address (the host-side symbol is only a stand-in), the
-  // device's SM count and the kernels' shared-memory limit.  No allocation.
+  // Set-up per device, with that device current: the scratch array's device
+  // address (the host-side symbol is only a stand-in), the device's SM count
+  // and the kernels' shared-memory limit.  No allocation.  The address is
+  // looked up again at every call (a lookup, no allocation); when it differs
+  // from the cached one (the device was reset and the module reloaded) the
+  // set-up is redone.
   struct DeviceSetup {
     bool done = false;
     void* scratch = nullptr;
@@ -1349,19 +1373,23 @@ int moe_layer_forward_static(moe_layer_t* h, int T, const void* x, const void* r
   int dev = 0;
   CK(cudaGetDevice(&dev));
   if (dev < 0 || dev >= 64) return fail(MOE_E_INVAL, "device ordinal out of range");
+  void* scratch_now = nullptr;
+  {
+    cudaError_t e = cudaGetSymbolAddress(&scratch_now, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+  }
+  DeviceSetup su;
   {
     std::lock_guard<std::mutex> lock(setup_mutex);
     DeviceSetup& s = setups[dev];
-    if (!s.done) {
+    if (!s.done || s.scratch != scratch_now) {
+      s.done = false;
       int cc_major = 0, cc_minor = 0;
       CK(cudaDeviceGetAttribute(&cc_major, cudaDevAttrComputeCapabilityMajor, dev));
       CK(cudaDeviceGetAttribute(&cc_minor, cudaDevAttrComputeCapabilityMinor, dev));
       if (cc_major != 10 || cc_minor != 3)
         return fail(MOE_E_INVAL, "this library is built for sm_103a (GB300) only");
       if (!encode_fn()) return fail(MOE_E_CUDA, "cuTensorMapEncodeTiled is not available");
-      void* ptr = nullptr;
-      cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_scratch);
-      if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
       CK(cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev));
       CK(cudaFuncSetAttribute(moe_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget));
       CK(cudaFuncSetAttribute(moe_static_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget));
@@ -1371,34 +1399,49 @@ int moe_layer_forward_static(moe_layer_t* h, int T, const void* x, const void* r
       CK(cudaFuncSetAttribute(k_gateup, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget));
       CK(cudaFuncSetAttribute(k_down, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget));
       CK(cudaFuncSetAttribute(k_combine, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget));
-      s.scratch = ptr;
+      s.scratch = scratch_now;
       s.done = true;
     }
+    su = s;
   }
-  const DeviceSetup& s = setups[dev];
   // A workspace laid out for exactly T tokens inside the scratch array; when
-  // the fp32 split-K partials do not fit, the down projection keeps Y in bf16.
+  // the fp32 split-K partials do not fit, the down projection keeps Y in bf16
+  // (so the tiling, and the last bits of out, may differ from
+  // moe_layer_forward's for the same layer: both are within the oracle's
+  // tolerance).
   moe_layer tmp = *h;
   tmp.device = dev;
-  tmp.num_sms = s.num_sms;
+  tmp.num_sms = su.num_sms;
   tmp.x_dev_stage = tmp.out_dev_stage = nullptr;
   tmp.trace = nullptr;  // the trace counters live in the caller's own workspace
   tmp.trace_cap = 0;
   Bounds b = make_bounds(&tmp, T);
   layout(&tmp, b);
-  if (tmp.ws_bytes > kStaticScratchBytes) {
+  if (tmp.ws_bytes > kNoallocScratchBytes) {
     const long long rows = (long long)T * h->k + (long long)T * h->S;
     b.y_elems = (size_t)((rows * h->d + 1) / 2);
     layout(&tmp, b);
   }
-  if (tmp.ws_bytes > kStaticScratchBytes)
-    return fail(MOE_E_INVAL, "layer too large for the " + std::to_string(kStaticScratchBytes >> 20) +
-                                 " MiB scratch of moe_layer_forward_static (needs " +
+  if (tmp.ws_bytes > kNoallocScratchBytes)
+    return fail(MOE_E_INVAL, "layer too large for the " + std::to_string(kNoallocScratchBytes >> 20) +
+                                 " MiB scratch of moe_layer_forward_noalloc (needs " +
                                  std::to_string(tmp.ws_bytes >> 20) + " MiB); use moe_layer_reserve");
   tmp.B = b;
-  tmp.ws = static_cast<char*>(s.scratch);
+  tmp.ws = static_cast<char*>(su.scratch);
   tmp.T_max = T;
-  return moe_layer_forward(&tmp, T, x, router_w, w_gate, w_up, w_down, out, stream);
+  const int rc = moe_layer_forward(&tmp, T, x, router_w, w_gate, w_up, w_down, out, stream);
+  if (rc == MOE_OK) {
+    h->view = tmp.view;
+    h->last_valid = false;
+    h->last_T = tmp.last_T;
+    h->last_grid = tmp.last_grid;
+    h->last_bn = tmp.last_bn;
+    h->last_ks = tmp.last_ks;
+    h->last_bands = tmp.last_bands;
+    h->last_ybytes = tmp.last_ybytes;
+    h->last_ct = tmp.last_ct;
+  }
+  return rc;
 }
 
 void moe_layer_destroy(moe_layer_t* h) {

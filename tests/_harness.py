@@ -192,3 +192,47 @@ def check_routing_full(w, inp, got, ref=None):
     assert np.all(np.abs(gw - rw) <= 1e-5 + 1e-5 * np.abs(rw)), "weights differ"
     assert np.all(ref["gap"] > MARGIN), "input violates the routing margin"
     return ref
+
+
+# ---- which tokens a sampled full-size comparison checks ---------------------------
+
+def expert_groups(rows: np.ndarray, bn: int):
+    """The plan's row groups of one expert: its tokens (ascending) split into
+    ceil(n / bn) balanced groups of a multiple of 16 rows."""
+    n = len(rows)
+    if n == 0:
+        return []
+    nmt = -(-n // bn)
+    per = ((-(-n // nmt)) + 15) // 16 * 16
+    return [rows[m * per:(m + 1) * per] for m in range(nmt) if m * per < n]
+
+
+def coverage_tokens(T, E, k, S, idx, bn, ct, n, seed=0):
+    """At least `n` distinct tokens such that every GEMM row group of the
+    shared expert (bn consecutive tokens each) and of the three experts with
+    the most tokens, and every combine tile (ct consecutive tokens, both d
+    bands: a compared token's whole row is compared), holds one of them; the
+    rest are drawn at random.  Sorted."""
+    rng = np.random.default_rng(seed)
+    pick = set()
+
+    def one_of(cands):
+        cands = np.asarray(cands)
+        if cands.size and not pick.intersection(cands.tolist()):
+            pick.add(int(rng.choice(cands)))
+
+    for c0 in range(0, T, ct):
+        one_of(np.arange(c0, min(T, c0 + ct)))
+    if S:
+        for g0 in range(0, T, bn):
+            one_of(np.arange(g0, min(T, g0 + bn)))
+    counts = np.bincount(np.asarray(idx).ravel(), minlength=E)
+    for e in np.argsort(-counts, kind="stable")[:3]:
+        rows = np.nonzero((np.asarray(idx) == e).any(axis=1))[0]
+        for grp in expert_groups(rows, bn):
+            one_of(grp)
+    rest = np.setdiff1d(np.arange(T), np.fromiter(pick, dtype=np.int64))
+    extra = max(0, min(n, T) - len(pick))
+    if extra:
+        pick.update(int(t) for t in rng.choice(rest, size=extra, replace=False))
+    return np.array(sorted(pick), dtype=np.int64)

@@ -99,7 +99,7 @@ int main(void) {
   CHECK(moe_layer_forward(h, 1, buf, buf, buf, buf, buf, buf, NULL) == MOE_E_STATE);
   CHECK(moe_layer_forward(NULL, 1, buf, buf, buf, buf, buf, buf, NULL) == MOE_E_INVAL);
   CHECK(moe_layer_forward_host(h, 1, buf, buf, buf, buf, buf, buf, NULL) == MOE_E_STATE);
-  CHECK(moe_layer_forward_static(NULL, 1, buf, buf, buf, buf, buf, buf, NULL) == MOE_E_INVAL);
+  CHECK(moe_layer_forward_noalloc(NULL, 1, buf, buf, buf, buf, buf, buf, NULL) == MOE_E_INVAL);
   CHECK(moe_layer_forward_residual_norm(h, 1, buf, buf, buf, buf, buf, NULL, buf, 1e-6f, buf,
                                         buf, NULL) == MOE_E_INVAL);
   CHECK(moe_layer_forward_residual_norm(h, 1, buf, buf, buf, buf, buf, buf, buf, -1.0f, buf,

@@ -70,11 +70,11 @@ def test_every_caller_shape_passes(rec, case):
     layer.forward_residual_norm(dev["x"], *wts, _out(w.T, w.d), gamma, 1e-5, _out(w.T, w.d),
                                 _out(w.T, w.d), stream=0)
     layer.calibrate(dev["x"], *wts, _out(w.T, w.d), reps=2, stream=0)
-    layer.forward_static(dev["x"], *wts, _out(w.T, w.d), stream=0)
+    layer.forward_noalloc(dev["x"], *wts, _out(w.T, w.d), stream=0)
     layer.forward_host(w.T, 4096, *wts, 8192, stream=0)
     assert rec.calls.count("moe_layer_forward") == 3
     for name in ("moe_layer_set_router_bias", "moe_layer_forward_residual_norm",
-                 "moe_layer_calibrate", "moe_layer_forward_static", "moe_layer_forward_host"):
+                 "moe_layer_calibrate", "moe_layer_forward_noalloc", "moe_layer_forward_host"):
         assert name in rec.calls, name
 
 
