@@ -76,8 +76,12 @@ typedef struct moe_layer moe_layer_t;
 /* option keys for moe_layer_set_option */
 #define MOE_OPT_MODE 1         /* MOE_MODE_*                                   */
 #define MOE_OPT_TIMEOUT_NS 2   /* device wait budget in ns (default 2e9)      */
-#define MOE_OPT_MOVER_CTAS 3   /* >0: fixed number of mover CTAs; 0 = model   */
-#define MOE_OPT_GRID_CTAS 4    /* >0: persistent grid size; 0 = one per SM    */
+#define MOE_OPT_MOVER_CTAS 3   /* >0: fixed number of mover workers (CTA
+                                  pairs); 0 = the cost model                  */
+#define MOE_OPT_GRID_CTAS 4    /* >0: CTAs of the persistent (and static)
+                                  grid, used rounded down to pairs (at least
+                                  one pair); 0 = every SM pair the device
+                                  keeps resident                              */
 #define MOE_OPT_SPLIT_K 5      /* down-projection K splits (1,2,4; 0 = auto)  */
 #define MOE_OPT_TOKENS_PER_TILE 6 /* max tokens per GEMM tile: 0 = auto, else
                                      16..256 in steps of 16, used rounded up
@@ -119,9 +123,10 @@ typedef struct moe_layer moe_layer_t;
 
 /* statistics keys for moe_layer_get_stat (values of the last forward;
  * moe_layer_status must have been called after it) */
-#define MOE_STAT_MOVER_CTAS 1  /* mover CTAs chosen by the cost model          */
+#define MOE_STAT_MOVER_CTAS 1  /* mover workers (CTA pairs) the cost model chose */
 #define MOE_STAT_TASKS 2       /* tasks executed (all types)                   */
-#define MOE_STAT_GRID 3        /* CTAs launched for the persistent kernel      */
+#define MOE_STAT_GRID 3        /* CTAs launched for the persistent kernel (two
+                                  per worker: clusters of a CTA pair)         */
 #define MOE_STAT_GEMM_TASKS 4  /* expert GEMM tasks executed                   */
 #define MOE_STAT_MOVER_TASKS 5 /* gather + combine tasks executed              */
 #define MOE_STAT_STOLEN 6      /* tasks a CTA ran from the other role's queue  */

@@ -30,9 +30,12 @@ __device__ __forceinline__ char* align1024(char* p) {
   return reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-// CTA set-up shared by every kernel: barriers, TMEM, per-thread state.
+// CTA set-up shared by every kernel: barriers, TMEM, per-thread state.  The
+// kernels with tensor-core tasks (`pair`) run as clusters of two CTAs: their
+// TMEM is allocated for the pair (one warp in each CTA) and a cluster barrier
+// makes both CTAs' barriers visible before any traffic between them.
 __device__ __forceinline__ void cta_setup(const Params& p, const Maps& maps, char*& smem,
-                                          Ctrl*& c, CtaState& st, bool with_tmem) {
+                                          Ctrl*& c, CtaState& st, bool pair) {
   extern __shared__ __align__(1024) char smem_raw[];
   smem = align1024(smem_raw);
   c = reinterpret_cast<Ctrl*>(smem + (size_t)p.stages * p.stage_bytes);
@@ -43,15 +46,16 @@ __device__ __forceinline__ void cta_setup(const Params& p, const Maps& maps, cha
       mbar_init(&c->empty_bar[s], 1);
     }
     mbar_init(&c->acc_bar, 1);
+    mbar_init(&c->tmem_empty, 1);
     mbar_init(&c->gbar, 1);
     mbar_init(&c->cbar[0], 1);
     mbar_init(&c->cbar[1], 1);
     fence_mbar_init();
     c->deadline = globaltimer() + p.timeout_ns;
-    c->mb_posted = c->mb_taken = c->mb_done = c->mb_handled = 0;
+    c->mb_posted = c->mb_taken = c->mb_done = c->mb_handled = c->mb_done_peer = 0;
     c->mb_late = -1;
   }
-  if (with_tmem && warp == 1) {
+  if (pair && warp == 1) {
     tmem_alloc(&c->tmem_base, kTmemCols);
     tmem_relinquish();
   }
@@ -67,7 +71,11 @@ __device__ __forceinline__ void cta_setup(const Params& p, const Maps& maps, cha
   }
   tc_fence_before();
   __syncthreads();
+  if (pair) cluster_sync();
   tc_fence_after();
+  st.rank = pair ? (int)cluster_rank() : 0;
+  st.worker = pair ? (int)(blockIdx.x / kPair) : (int)blockIdx.x;
+  st.lead_ctrl = pair ? mapa_shared(smem_u32(c), 0) : smem_u32(c);
   st.pipe_it = 0;
   st.gemm_count = 0;
   st.deadline = c->deadline;
@@ -83,10 +91,14 @@ __device__ __forceinline__ void cta_setup(const Params& p, const Maps& maps, cha
   st.taken = 0;
 }
 
-__device__ __forceinline__ void cta_teardown(Ctrl* c, bool with_tmem) {
+// Both CTAs of a pair pass a cluster barrier before either exits or frees the
+// pair's TMEM: neither may leave while the other can still signal its
+// barriers or read its shared memory.
+__device__ __forceinline__ void cta_teardown(Ctrl* c, bool pair) {
   tc_fence_before();
   __syncthreads();
-  if (with_tmem && (threadIdx.x >> 5) == 1) {
+  if (pair) cluster_sync();
+  if (pair && (threadIdx.x >> 5) == 1) {
     tc_fence_after();
     tmem_dealloc(c->tmem_base, kTmemCols);
   }
@@ -119,41 +131,51 @@ __device__ __forceinline__ void trace_record(const Params& p, unsigned long long
 // Once the plan is published and until the first gate/up tiles start, HBM
 // only carries the gathers: pull the gate/up weight tiles the first GEMM wave
 // will read into L2 -- tiles (expert, f tile) in index order, the order the
-// plan keeps (Params::index_order) -- spread over the CTAs, up to
-// l2_pf_bytes.  One lane, asynchronous.  (Issued earlier, while the plan
-// runs, the prefetch traffic slows the plan's memory accesses: measured
-// 2.5 us slower on the fine and decode workloads.)
-__device__ void prefetch_first_weights(const Params& p) {
-  const size_t tile_bytes = (size_t)kBM * p.d * 2;  // one 128-row f tile of w_gate or w_up
+// plan keeps (Params::index_order) -- spread over the CTA pairs, up to
+// l2_pf_bytes.  One lane of each pair's leader, asynchronous.  (Issued
+// earlier, while the plan runs, the prefetch traffic slows the plan's memory
+// accesses: measured 2.5 us slower on the fine and decode workloads.)
+__device__ void prefetch_first_weights(const Params& p, const CtaState& st) {
+  const size_t tile_bytes = (size_t)kFTile * p.d * 2;  // one 256-row f tile of w_gate or w_up
   const long long n_tiles =
       min((long long)p.E * p.n_ftiles, p.l2_pf_bytes / (long long)(2 * tile_bytes));
+  const int workers = (int)gridDim.x / kPair;
   constexpr uint32_t kChunk = 128u << 10;
-  for (long long i = blockIdx.x; i < n_tiles; i += gridDim.x) {
+  for (long long i = st.worker; i < n_tiles; i += workers) {
     const int e = (int)(i / p.n_ftiles), ft = (int)(i - (long long)e * p.n_ftiles);
-    const size_t row0 = (size_t)e * p.f + (size_t)ft * kBM;
+    const int rows = min(kFTile, p.f - ft * kFTile);
+    const size_t row0 = (size_t)e * p.f + (size_t)ft * kFTile;
     const char* g = reinterpret_cast<const char*>(p.w_gate + row0 * p.d);
     const char* u = reinterpret_cast<const char*>(p.w_up + row0 * p.d);
-    for (size_t o = 0; o < tile_bytes; o += kChunk) {
-      const uint32_t n = (uint32_t)min((size_t)kChunk, tile_bytes - o);
+    const size_t bytes = (size_t)rows * p.d * 2;
+    for (size_t o = 0; o < bytes; o += kChunk) {
+      const uint32_t n = (uint32_t)min((size_t)kChunk, bytes - o);
       bulk_prefetch_l2(g + o, n);
       bulk_prefetch_l2(u + o, n);
     }
   }
 }
 
+// The compute warps of either CTA of a pair: take the tasks the leader's
+// scheduler warp posts to this CTA's mailbox (the same tasks, in the same
+// order, in both CTAs), run this CTA's part of each, and report it finished:
+// the leader's own to its scheduler warp through its mailbox, the peer's to
+// the leader as a count of finished tasks.
 __device__ void compute_loop(const Params& p, const Maps& maps, char* smem, Ctrl* c,
                              CtaState& st) {
   int executed = 0, gemm_tasks = 0, mover_tasks = 0, done = 0;
+  const bool lead = st.rank == 0;
   while (true) {
     if (threadIdx.x == 0) {  // take the next posted task, or the exit token
       uint32_t backoff = 32;
       int t = -1;
       while (true) {
-        if (ld_acquire_cta_shared(&c->mb_posted) > st.taken) {
+        if (mailbox_posted(c, st) > st.taken) {
           t = c->mb_task[st.taken & 1];
           c->t_claim = c->mb_tclaim[st.taken & 1];
           ++st.taken;
-          st_release_cta_shared(&c->mb_taken, st.taken);
+          if (lead) st_release_cta_shared(&c->mb_taken, st.taken);
+          else st_release_cluster(smem_u32(&c->mb_taken), st.taken);
           break;
         }
         if (ld_relaxed(&p.sched->status) != 0) break;
@@ -173,8 +195,8 @@ __device__ void compute_loop(const Params& p, const Maps& maps, char* smem, Ctrl
     ++executed;
     const int type = task_type(task), pl = task_payload(task);
     if (type == kTaskRoute) {
-      const int tile = pl / p.route_ks, split = pl - tile * p.route_ks;
-      if (route_task(p, maps, tile, split, smem, c, st)) {
+      const int pt = pl / p.route_ks, split = pl - pt * p.route_ks;
+      if (route_task(p, maps, pt, split, smem, c, st)) {
         release_writes();
         if (threadIdx.x == 0) {
           const int old = atom_add_acq_rel(&p.sched->route_done, 1);
@@ -196,7 +218,7 @@ __device__ void compute_loop(const Params& p, const Maps& maps, char* smem, Ctrl
       }
     } else if (type == kTaskGather) {
       ++mover_tasks;
-      gather_task(p, pl >> 3, pl & 7, smem, c, st);
+      gather_task(p, pl >> 3, pl & 7, st.rank, kPair, smem, c, st);
     } else if (type == kTaskGateUp) {
       ++gemm_tasks;
       gateup_task(p, maps, task, smem, c, st);
@@ -205,42 +227,57 @@ __device__ void compute_loop(const Params& p, const Maps& maps, char* smem, Ctrl
       down_task(p, maps, task, smem, c, st);
     } else if (type == kTaskCombine) {
       ++mover_tasks;
-      combine_task(p, pl, smem, c, st);
+      combine_task(p, pl, st.rank, kPair, smem, c, st);
     } else {
       if (threadIdx.x == 0) set_status(p, MOE_E_DEVICE, 6);
       break;
     }
-    // hand the finished task to the scheduler warp: every compute thread's
-    // writes (async proxy included) come before thread 0's CTA-scope release
+    // hand the finished task over: every compute thread's writes (async
+    // proxy included) come before thread 0's release
     fence_proxy_async_global();
     cta_sync();
     if (threadIdx.x == 0) {
-      if (p.trace)
-        trace_record(p, ((unsigned long long)blockIdx.x << 32) | (unsigned)task, c->t_claim,
-                     c->t_start, globaltimer());
-      while (done - ld_acquire_cta_shared(&c->mb_handled) >= 2) {  // ring of two
-        if (ld_relaxed(&p.sched->status) != 0) break;
-        if (globaltimer() > st.deadline) {
-          set_status(p, MOE_E_TIMEOUT, 31);
-          break;
-        }
-        __nanosleep(64);
-      }
-      c->mb_done_task[done & 1] = task;
       ++done;
-      st_release_cta_shared(&c->mb_done, done);
+      if (lead) {
+        if (p.trace)
+          trace_record(p, ((unsigned long long)blockIdx.x << 32) | (unsigned)task, c->t_claim,
+                       c->t_start, globaltimer());
+        while (done - 1 - ld_acquire_cta_shared(&c->mb_handled) >= 2) {  // ring of two
+          if (ld_relaxed(&p.sched->status) != 0) break;
+          if (globaltimer() > st.deadline) {
+            set_status(p, MOE_E_TIMEOUT, 31);
+            break;
+          }
+          __nanosleep(64);
+        }
+        c->mb_done_task[(done - 1) & 1] = task;
+        st_release_cta_shared(&c->mb_done, done);
+      } else {
+        // the peer's writes (ordered before this store by the CTA barrier)
+        // reach the leader's scheduler warp, which fences at GPU scope before
+        // it notifies
+        st_release_cluster(st.lead_ctrl + (uint32_t)offsetof(Ctrl, mb_done_peer), done);
+      }
     }
   }
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0 && lead) {
     atomicAdd(&p.sched->tasks_done, executed);
     atomicAdd(&p.sched->stat_gemm, gemm_tasks);
     atomicAdd(&p.sched->stat_mover, mover_tasks);
   }
 }
 
+// The leader's scheduler warp (the peer's has nothing to do): claims each
+// task for the pair, posts it to both CTAs' mailboxes, and runs a finished
+// task's notifications once both CTAs have finished it.
 __device__ void scheduler_loop(const Params& p, Ctrl* c, CtaState& st) {
+  if (st.rank != 0) return;
   const int lane = threadIdx.x & 31;
   const unsigned full = 0xffffffffu;
+  const uint32_t peer = mapa_shared(smem_u32(c), 1);  // the peer's Ctrl
+  const uint32_t off_posted = (uint32_t)offsetof(Ctrl, mb_posted);
+  const uint32_t off_taken = (uint32_t)offsetof(Ctrl, mb_taken);
+  const uint32_t off_task = (uint32_t)offsetof(Ctrl, mb_task);
   int posted = 0, handled = 0, ahead = 0, polled_seq = -1;
   bool exit_posted = false, prefetched = p.l2_pf_bytes <= 0;
   uint32_t backoff = 32;
@@ -248,15 +285,27 @@ __device__ void scheduler_loop(const Params& p, Ctrl* c, CtaState& st) {
     if (lane == 0) {
       c->mb_task[posted & 1] = t;
       c->mb_tclaim[posted & 1] = globaltimer();
+      st_cluster(peer + off_task + 4u * (posted & 1), t);
     }
     ++posted;
     __syncwarp();
-    if (lane == 0) st_release_cta_shared(&c->mb_posted, posted);
+    if (lane == 0) {
+      st_release_cta_shared(&c->mb_posted, posted);
+      st_release_cluster(peer + off_posted, posted);
+    }
   };
   while (true) {
     bool progress = false;
-    // notifications of the finished tasks
-    const int done = __shfl_sync(full, ld_acquire_cta_shared(&c->mb_done), 0);
+    // notifications of the tasks both CTAs have finished
+    int done = 0, taken = 0, late_seq = 0;
+    if (lane == 0) {
+      done = min(ld_acquire_cta_shared(&c->mb_done), ld_acquire_cluster(smem_u32(&c->mb_done_peer)));
+      taken = min(ld_acquire_cta_shared(&c->mb_taken), ld_acquire_cluster(peer + off_taken));
+      late_seq = ld_acquire_cta_shared(&c->mb_late);
+    }
+    done = __shfl_sync(full, done, 0);
+    taken = __shfl_sync(full, taken, 0);
+    late_seq = __shfl_sync(full, late_seq, 0);
     if (handled < done) {
       fence_acq_rel_gpu();  // the compute warps' writes, acquired above, before our releases
       while (handled < done) {
@@ -270,7 +319,7 @@ __device__ void scheduler_loop(const Params& p, Ctrl* c, CtaState& st) {
     if (!prefetched) {  // the L2 weight prefetch, once the plan is published
       const int pd = __shfl_sync(full, lane == 0 ? ld_relaxed(&p.sched->plan_done) : 0, 0);
       if (pd != 0) {
-        if (lane == 0) prefetch_first_weights(p);
+        if (lane == 0) prefetch_first_weights(p, st);
         prefetched = true;
       }
     }
@@ -281,39 +330,36 @@ __device__ void scheduler_loop(const Params& p, Ctrl* c, CtaState& st) {
     }
     if (exit_posted) {
       if (handled >= posted - 1) break;  // every real task finished and notified
-    } else {
-      const int taken = __shfl_sync(full, ld_acquire_cta_shared(&c->mb_taken), 0);
-      if (posted == taken) {  // nothing waiting in the mailbox
-        const bool idle = taken == done;
-        const bool late = __shfl_sync(full, ld_acquire_cta_shared(&c->mb_late), 0) == taken;
-        int min_depth = 0;
-        if (idle || late) {
-          min_depth = 1;
-        } else if (p.ahead_depth > 0 && polled_seq != taken) {
-          min_depth = p.ahead_depth;  // early claim: once per task, deep queue only
-          polled_seq = taken;
-        }
-        if (min_depth > 0) {
-          const int r = claim_once(p, st, min_depth);
-          if (r >= 0) {
-            post(r);
-            if (!idle) ++ahead;
-            progress = true;
-          } else if (r == -4) {
-            progress = true;  // lost a CAS: retry at once
-          } else if (r == -2 || r == -3) {
-            st.exit_reason = r == -2 ? 1 : 2;
-            post(-1);
-            exit_posted = true;
-            progress = true;
-          } else if (idle) {
-            ++st.polls;
-            const int late_t = __shfl_sync(full, lane == 0 ? (globaltimer() > st.deadline) : 0, 0);
-            if (late_t) {
-              if (lane == 0) set_status(p, MOE_E_TIMEOUT, 3);
-              st.exit_reason = 3;
-              break;
-            }
+    } else if (posted == taken) {  // nothing waiting in either mailbox
+      const bool idle = taken == done;
+      const bool late = late_seq == taken;
+      int min_depth = 0;
+      if (idle || late) {
+        min_depth = 1;
+      } else if (p.ahead_depth > 0 && polled_seq != taken) {
+        min_depth = p.ahead_depth;  // early claim: once per task, deep queue only
+        polled_seq = taken;
+      }
+      if (min_depth > 0) {
+        const int r = claim_once(p, st, min_depth);
+        if (r >= 0) {
+          post(r);
+          if (!idle) ++ahead;
+          progress = true;
+        } else if (r == -4) {
+          progress = true;  // lost a CAS: retry at once
+        } else if (r == -2 || r == -3) {
+          st.exit_reason = r == -2 ? 1 : 2;
+          post(-1);
+          exit_posted = true;
+          progress = true;
+        } else if (idle) {
+          ++st.polls;
+          const int late_t = __shfl_sync(full, lane == 0 ? (globaltimer() > st.deadline) : 0, 0);
+          if (late_t) {
+            if (lane == 0) set_status(p, MOE_E_TIMEOUT, 3);
+            st.exit_reason = 3;
+            break;
           }
         }
       }
@@ -347,9 +393,9 @@ __global__ void __launch_bounds__(kThreads + 32, 1)
 }
 
 // ------------------------------------------------------------------ static persistent megakernel
-// The static fused baseline: one launch, one CTA per SM, every stage's tasks
-// assigned round-robin to the CTAs (task i of a stage to CTA i mod grid),
-// and a grid-wide barrier between stages -- no queue, no dependency
+// The static fused baseline: one launch, one CTA per SM (in pairs), every
+// stage's tasks assigned round-robin to the CTA pairs (task i of a stage to
+// pair i mod pairs), and a grid-wide barrier between stages -- no queue, no dependency
 // counters, no overlap of stages.  Same tiles as the other two modes, so its
 // gap to the persistent kernel is what the queue, the counters and the
 // cross-stage overlap buy beyond saving launches.  Launched cooperatively, so
@@ -396,35 +442,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   Ctrl* c;
   CtaState st;
   cta_setup(p, maps, smem, c, st, true);
-  const int G = gridDim.x, b = blockIdx.x;
+  // tasks go round-robin to the CTA pairs; both CTAs of a pair run each one
+  const int W = (int)gridDim.x / kPair, w = st.worker;
   int gen = 0;
-  for (int i = b; i < p.n_route_tasks; i += G)
+  for (int i = w; i < p.n_route_tasks; i += W)
     route_task(p, maps, i / p.route_ks, i % p.route_ks, smem, c, st);
   bool ok = grid_barrier(p, c, gen, st);
-  if (ok && b == 0) plan_task(p, smem, c, false);
+  if (ok && blockIdx.x == 0) plan_task(p, smem, c, false);
   ok = ok && grid_barrier(p, c, gen, st);
   const int n_groups = ok ? ld_relaxed(&p.sched->n_groups) : 0;
   const int n_routed = n_groups - p.n_shared_groups;
-  for (int i = b; ok && i < n_routed * 8; i += G) {  // (routed group, chunk)
+  for (int i = w; ok && i < n_routed * 8; i += W) {  // (routed group, chunk)
     const int g = p.n_shared_groups + (i >> 3), ch = i & 7;
-    if (ch * kGatherRows < load_group(p, g).nrows) gather_task(p, g, ch, smem, c, st);
+    if (ch * kGatherRows < load_group(p, g).nrows) gather_task(p, g, ch, st.rank, kPair, smem, c, st);
   }
   ok = ok && grid_barrier(p, c, gen, st);
-  for (int i = b; ok && i < n_groups * p.n_ftiles; i += G)
+  for (int i = w; ok && i < n_groups * p.n_ftiles; i += W)
     gateup_task(p, maps, task_id(kTaskGateUp, i), smem, c, st);
   ok = ok && grid_barrier(p, c, gen, st);
   const int n_down = p.n_dtiles * p.ks;
-  for (int i = b; ok && i < n_groups * n_down; i += G)
+  for (int i = w; ok && i < n_groups * n_down; i += W)
     down_task(p, maps, task_id(kTaskDown, i), smem, c, st);
   ok = ok && grid_barrier(p, c, gen, st);
-  for (int i = b; ok && i < p.n_comb; i += G) {
-    combine_task(p, i, smem, c, st);
+  for (int i = w; ok && i < p.n_comb; i += W) {
+    combine_task(p, i, st.rank, kPair, smem, c, st);
     cta_sync();
   }
   cta_teardown(c, true);
 }
 
 // ------------------------------------------------------------------ ablation: one kernel per stage
+// The tensor-core stages (router, gate/up, down) launch one cluster of two
+// CTAs per task; the others one CTA per task.
 
 __global__ void __launch_bounds__(kThreads, 1)
     k_route(const __grid_constant__ Params p, const __grid_constant__ Maps maps) {
@@ -432,7 +481,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   Ctrl* c;
   CtaState st;
   cta_setup(p, maps, smem, c, st, true);
-  route_task(p, maps, blockIdx.x / p.route_ks, blockIdx.x % p.route_ks, smem, c, st);
+  const int i = (int)blockIdx.x / kPair;
+  route_task(p, maps, i / p.route_ks, i % p.route_ks, smem, c, st);
   cta_teardown(c, true);
 }
 
@@ -455,31 +505,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   Ctrl* c;
   CtaState st;
   cta_setup(p, maps, smem, c, st, false);
-  gather_task(p, g, ch, smem, c, st);
+  gather_task(p, g, ch, 0, 1, smem, c, st);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
     k_gateup(const __grid_constant__ Params p, const __grid_constant__ Maps maps) {
-  const int g = blockIdx.x / p.n_ftiles;
+  const int i = (int)blockIdx.x / kPair;  // the same for both CTAs of the cluster
+  const int g = i / p.n_ftiles;
   if (g >= p.sched->n_groups) return;
   char* smem;
   Ctrl* c;
   CtaState st;
   cta_setup(p, maps, smem, c, st, true);
-  gateup_task(p, maps, task_id(kTaskGateUp, blockIdx.x), smem, c, st);
+  gateup_task(p, maps, task_id(kTaskGateUp, i), smem, c, st);
   cta_teardown(c, true);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
     k_down(const __grid_constant__ Params p, const __grid_constant__ Maps maps) {
   const int n_down = p.n_dtiles * p.ks;
-  const int g = blockIdx.x / n_down;
+  const int i = (int)blockIdx.x / kPair;  // the same for both CTAs of the cluster
+  const int g = i / n_down;
   if (g >= p.sched->n_groups) return;
   char* smem;
   Ctrl* c;
   CtaState st;
   cta_setup(p, maps, smem, c, st, true);
-  down_task(p, maps, task_id(kTaskDown, blockIdx.x), smem, c, st);
+  down_task(p, maps, task_id(kTaskDown, i), smem, c, st);
   cta_teardown(c, true);
 }
 
@@ -489,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   Ctrl* c;
   CtaState st;
   cta_setup(p, maps, smem, c, st, false);
-  combine_task(p, blockIdx.x, smem, c, st);
+  combine_task(p, blockIdx.x, 0, 1, smem, c, st);
 }
 
 }  // namespace moe
@@ -578,6 +630,7 @@ struct moe_layer {
   int T_max = 0;
   int device = -1;
   int num_sms = 0;
+  int max_pairs = 0;  // clusters of two CTAs the persistent kernel can keep resident
   // options
   int mode = MOE_MODE_PERSISTENT;
   unsigned long long timeout_ns = 2000000000ull;
@@ -703,9 +756,12 @@ int choose_tiling(const moe_layer* h, int T, bool whole_rows, Tiling* t) {
   }
   bn = std::max(32, std::min(256, ((bn + 31) / 32) * 32));
   t->bn = bn;
-  t->stage_bytes = 2 * kABoxBytes + cdiv(bn, kBBoxRows) * kBBoxBytes;
-  // the router's tile keeps x (16 KB) then Wr (E rows) in one stage
-  t->stage_bytes = std::max(t->stage_bytes, kABoxBytes + cdiv(h->E, kBBoxRows) * kBBoxBytes);
+  // a stage holds this CTA's 128 rows of each weight operand and half of the
+  // tile's token rows (the pair's other CTA holds the other half)
+  t->stage_bytes = 2 * kABoxBytes + cdiv(bn / kPair, kBBoxRows) * kBBoxBytes;
+  // the router's tile keeps x (16 KB) then half of Wr's E rows (padded to 32)
+  t->stage_bytes =
+      std::max(t->stage_bytes, kABoxBytes + cdiv(((h->E + 31) / 32) * 16, kBBoxRows) * kBBoxBytes);
   const int ctrl = (int)align_up(sizeof(Ctrl), 1024);
   t->stages = std::min(8, (kSmemBudget - 1024 - ctrl) / t->stage_bytes);
   if (t->stages < 2) return fail(MOE_E_INVAL, "tile too large for shared memory");
@@ -717,13 +773,12 @@ int choose_tiling(const moe_layer* h, int T, bool whole_rows, Tiling* t) {
   const long long rows = Tk + (long long)T * h->S;
   int ks = h->split_k;
   if (ks <= 0) {
-    // the smallest split that gives about 1.5 grids of down tasks, counting
-    // one row group per expert that can be touched (decode: 2 -- 518 us
-    // against 521 us at 4 and 529 us at 1)
+    // the smallest split that gives about 1.5 waves of down tasks over the
+    // CTA pairs, counting one row group per expert that can be touched
     const long long groups = std::min<long long>(h->E, Tk) + h->S;
-    const long long want = 3ll * std::max(h->num_sms, 1) / 2;
+    const long long want = 3ll * std::max(h->num_sms / kPair, 1) / 2;
     ks = 1;
-    while (ks < 4 && groups * cdiv(h->d, 2 * kBM) * ks < want) ks <<= 1;
+    while (ks < 4 && groups * cdiv(h->d, kDTile) * ks < want) ks <<= 1;
   }
   while (ks > 1 && (kblocks % ks != 0 || (size_t)rows * h->d * ks > h->B.y_elems)) ks >>= 1;
   if (ks < 1) ks = 1;
@@ -736,11 +791,11 @@ int choose_tiling(const moe_layer* h, int T, bool whole_rows, Tiling* t) {
   const bool small_rt = T <= kSmallRouteT && h->E >= kSmallRouteMinE;
   t->rt = h->rt_opt ? h->rt_opt : (small_rt ? kRouteTokensSmall : kRouteTokens);
   if (cdiv(T, t->rt) > kMaxE) return fail(MOE_E_INVAL, "too many router tiles: use 128-token tiles");
-  // combine tile, <= 256 (token, slot) pairs: one per SM when the combine is
-  // split in two d bands (each task then covers part of a row), two per SM
-  // with one band -- the faster choice of each, measured on GB300
-  const bool two_bands = h->bands && cdiv(h->d, 2 * kBM) >= 2 && !whole_rows;
-  int ct = cdiv(T, (two_bands ? 1 : 2) * std::max(h->num_sms, 1));
+  // combine tile, <= 256 (token, slot) pairs: one per CTA pair when the
+  // combine is split in two d bands (each task then covers part of a row),
+  // two per pair with one band; the pair's CTAs split a tile's tokens
+  const bool two_bands = h->bands && cdiv(h->d, kDTile) >= 2 && !whole_rows;
+  int ct = cdiv(T, (two_bands ? 1 : 2) * std::max(h->num_sms / kPair, 1));
   ct = std::max(1, std::min(ct, kThreads / h->k));
   t->ct = ct;
   return MOE_OK;
@@ -759,6 +814,56 @@ int set_error_from_sched(const Sched& s) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// Launch one of the kernels: `pair` as clusters of two CTAs (the kernels with
+// tensor-core tasks), `coop` cooperatively.
+cudaError_t launch_kernel(void (*kern)(Params, Maps), int grid, int threads, int smem,
+                          cudaStream_t s, bool pair, bool coop, const Params& p, const Maps& m) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)threads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[2];
+  int n = 0;
+  if (pair) {
+    at[n].id = cudaLaunchAttributeClusterDimension;
+    at[n].val.clusterDim.x = kPair;
+    at[n].val.clusterDim.y = 1;
+    at[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  if (coop) {
+    at[n].id = cudaLaunchAttributeCooperative;
+    at[n].val.cooperative = 1;
+    ++n;
+  }
+  cfg.attrs = at;
+  cfg.numAttrs = (unsigned)n;
+  return cudaLaunchKernelEx(&cfg, kern, p, m);
+}
+
+// Clusters of two CTAs of the persistent kernel (one CTA per SM at its shared
+// memory size) the device keeps resident at once; 0 if the query fails.
+int query_max_pairs(int num_sms) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)std::max(kPair, num_sms / kPair * kPair));
+  cfg.blockDim = dim3(kThreads + 32);
+  cfg.dynamicSmemBytes = kSmemBudget;
+  cudaLaunchAttribute at;
+  at.id = cudaLaunchAttributeClusterDimension;
+  at.val.clusterDim.x = kPair;
+  at.val.clusterDim.y = 1;
+  at.val.clusterDim.z = 1;
+  cfg.attrs = &at;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, (const void*)moe_persistent_kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
 
 }  // namespace
 
@@ -855,6 +960,7 @@ int moe_layer_reserve(moe_layer_t* h, int T_max, void* stream) {
   CK(cudaFuncSetAttribute(k_gateup, cudaFuncAttributeMaxDynamicSharedMemorySize, kernels_smem));
   CK(cudaFuncSetAttribute(k_down, cudaFuncAttributeMaxDynamicSharedMemorySize, kernels_smem));
   CK(cudaFuncSetAttribute(k_combine, cudaFuncAttributeMaxDynamicSharedMemorySize, kernels_smem));
+  h->max_pairs = query_max_pairs(h->num_sms);
   g_err.clear();
   return MOE_OK;
 }
@@ -985,8 +1091,8 @@ int forward_impl(moe_layer_t* h, int T, const void* x, const void* router_w, con
   p.bn_max = tl.bn;
   p.stages = tl.stages;
   p.stage_bytes = tl.stage_bytes;
-  p.n_ftiles = h->f / kBM;
-  p.n_dtiles = cdiv(h->d, 2 * kBM);
+  p.n_ftiles = cdiv(h->f, kFTile);
+  p.n_dtiles = cdiv(h->d, kDTile);
   p.ks = tl.ks;
   p.kb_down = (h->f / kBK) / tl.ks;
   p.rt = tl.rt;
@@ -1002,7 +1108,7 @@ int forward_impl(moe_layer_t* h, int T, const void* x, const void* router_w, con
     int ks = std::min(kMaxRouteKs, std::min(std::max(1, nkb / 8), cap));
     if (h->route_splits > 0) ks = std::min(std::min(h->route_splits, nkb), cap);
     p.route_ks = std::max(1, ks);
-    p.n_route_tasks = p.n_route * p.route_ks;
+    p.n_route_tasks = cdiv(p.n_route, kPair) * p.route_ks;
   }
   p.release = h->release;
   p.prefetch = h->prefetch;
@@ -1028,8 +1134,10 @@ int forward_impl(moe_layer_t* h, int T, const void* x, const void* router_w, con
   p.trace = h->trace;
   p.trace_cap = h->trace_cap;
   p.timeout_ns = h->timeout_ns;
-  p.beta_move = 40e9f;
-  p.phi_gemm = 1925e12f / 152.f;
+  // cost-model constants per worker (a CTA pair): 2 x 40 GB/s of bulk copies,
+  // two SMs' share of 1925 TF/s
+  p.beta_move = 80e9f;
+  p.phi_gemm = 1925e12f / 76.f;
   p.hbm_bw = 6.79e12f;
   p.x = static_cast<const __nv_bfloat16*>(x);
   p.wr = static_cast<const __nv_bfloat16*>(router_w);
@@ -1096,33 +1204,35 @@ int forward_impl(moe_layer_t* h, int T, const void* x, const void* router_w, con
 
   // scheduler counters and task rings are contiguous: one memset resets them
   CK(cudaMemsetAsync(w + h->o_zero, 0, h->o_ring_end - h->o_zero, s));
+  const int sms_pairs = std::max(1, h->num_sms / kPair);
+  const int cap_pairs = h->max_pairs > 0 ? std::min(h->max_pairs, sms_pairs) : sms_pairs;
+  const int pairs = h->grid_override > 0 ? std::max(1, std::min(h->grid_override / kPair, cap_pairs))
+                                         : cap_pairs;
+  p.n_workers = pairs;
   if (h->mode == MOE_MODE_PERSISTENT) {
-    int grid = h->grid_override > 0 ? h->grid_override : h->num_sms;
-    h->last_grid = grid;
-    p.ahead_depth = h->ahead_opt < 0 ? grid : h->ahead_opt;
-    moe_persistent_kernel<<<grid, kThreads + 32, tl.smem, s>>>(p, m);
-    CK(cudaGetLastError());
+    h->last_grid = pairs * kPair;
+    p.ahead_depth = h->ahead_opt < 0 ? pairs : h->ahead_opt;
+    CK(launch_kernel(moe_persistent_kernel, pairs * kPair, kThreads + 32, tl.smem, s, true, false, p, m));
   } else if (h->mode == MOE_MODE_STATIC) {
-    const int grid = h->grid_override > 0 ? std::min(h->grid_override, h->num_sms) : h->num_sms;
-    h->last_grid = grid;
-    void* args[] = {&p, &m};
-    CK(cudaLaunchCooperativeKernel((const void*)moe_static_kernel, dim3(grid), dim3(kThreads), args,
-                                   (size_t)tl.smem, s));
+    h->last_grid = pairs * kPair;
+    // cooperative, so that every CTA is resident for the grid barrier; where a
+    // cooperative cluster launch is refused, a plain one (the grid is within
+    // the resident-cluster count, and every barrier wait is bounded)
+    cudaError_t e = launch_kernel(moe_static_kernel, pairs * kPair, kThreads, tl.smem, s, true, true, p, m);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      CK(launch_kernel(moe_static_kernel, pairs * kPair, kThreads, tl.smem, s, true, false, p, m));
+    }
   } else {
     h->last_grid = 0;
-    k_route<<<p.n_route_tasks, kThreads, tl.smem, s>>>(p, m);
-    CK(cudaGetLastError());
-    k_plan<<<1, kThreads, tl.smem, s>>>(p, m);
-    CK(cudaGetLastError());
+    CK(launch_kernel(k_route, p.n_route_tasks * kPair, kThreads, tl.smem, s, true, false, p, m));
+    CK(launch_kernel(k_plan, 1, kThreads, tl.smem, s, false, false, p, m));
     const int routed_max = p.max_groups - p.n_shared_groups;
-    k_gather<<<routed_max * 8, kThreads, tl.smem, s>>>(p, m);
-    CK(cudaGetLastError());
-    k_gateup<<<p.max_groups * p.n_ftiles, kThreads, tl.smem, s>>>(p, m);
-    CK(cudaGetLastError());
-    k_down<<<p.max_groups * p.n_dtiles * p.ks, kThreads, tl.smem, s>>>(p, m);
-    CK(cudaGetLastError());
-    k_combine<<<p.n_comb, kThreads, tl.smem, s>>>(p, m);
-    CK(cudaGetLastError());
+    CK(launch_kernel(k_gather, routed_max * 8, kThreads, tl.smem, s, false, false, p, m));
+    CK(launch_kernel(k_gateup, p.max_groups * p.n_ftiles * kPair, kThreads, tl.smem, s, true, false, p, m));
+    CK(launch_kernel(k_down, p.max_groups * p.n_dtiles * p.ks * kPair, kThreads, tl.smem, s, true,
+                     false, p, m));
+    CK(launch_kernel(k_combine, p.n_comb, kThreads, tl.smem, s, false, false, p, m));
   }
   h->view.ws = h->ws;
   h->view.o_idx = h->o_idx;
@@ -1367,6 +1477,7 @@ int moe_layer_forward_noalloc(moe_layer_t* h, int T, const void* x, const void* 
     bool done = false;
     void* scratch = nullptr;
     int num_sms = 0;
+    int max_pairs = 0;
   };
   static DeviceSetup setups[64];
   static std::mutex setup_mutex;
@@ -1399,6 +1510,7 @@ int moe_layer_forward_noalloc(moe_layer_t* h, int T, const void* x, const void* 
       CK(cudaFuncSetAttribute(k_gateup, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget));
       CK(cudaFuncSetAttribute(k_down, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget));
       CK(cudaFuncSetAttribute(k_combine, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget));
+      s.max_pairs = query_max_pairs(s.num_sms);
       s.scratch = scratch_now;
       s.done = true;
     }
@@ -1412,6 +1524,7 @@ int moe_layer_forward_noalloc(moe_layer_t* h, int T, const void* x, const void* 
   moe_layer tmp = *h;
   tmp.device = dev;
   tmp.num_sms = su.num_sms;
+  tmp.max_pairs = su.max_pairs;
   tmp.x_dev_stage = tmp.out_dev_stage = nullptr;
   tmp.trace = nullptr;  // the trace counters live in the caller's own workspace
   tmp.trace_cap = 0;

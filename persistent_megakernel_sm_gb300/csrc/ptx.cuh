@@ -134,23 +134,90 @@ __device__ __forceinline__ int atom_cas_acq_rel(int* p, int cmp, int v) {
   return old;
 }
 
-// ---------------------------------------------------------------- tcgen05
+// ---------------------------------------------------------------- clusters
+// Every tensor-core kernel here runs as clusters of two CTAs on a pair of
+// SMs (tcgen05 .cta_group::2): cluster rank 0 is the pair's leader.
 
-// Allocate `ncols` TMEM columns (power of two >= 32); whole warp; the TMEM
-// address is written to shared memory at `dst`.
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Address, in the cluster's shared window, of the variable at CTA-local
+// shared address `addr` in the CTA of cluster rank `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+// Barrier of every thread of both CTAs (release / acquire at cluster scope).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_release_cluster(uint32_t cl_addr, int v) {
+  asm volatile("st.release.cluster.shared::cluster.b32 [%0], %1;" ::"r"(cl_addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_cluster(uint32_t cl_addr, int v) {
+  asm volatile("st.shared::cluster.b32 [%0], %1;" ::"r"(cl_addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int ld_acquire_cluster(uint32_t cl_addr) {
+  int v;
+  asm volatile("ld.acquire.cluster.shared::cluster.b32 %0, [%1];" : "=r"(v) : "r"(cl_addr) : "memory");
+  return v;
+}
+
+// Arrive once on the mbarrier at cluster address `cl_addr` (either CTA).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cl_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cl_addr)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// 2-D tiled load into this CTA's shared memory whose completion (the box's
+// byte count) is signalled on the mbarrier at cluster address `cl_bar`,
+// which may be in the pair's other CTA (.cta_group::2).
+__device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorMap* map,
+                                                 uint32_t cl_bar, int c0, int c1, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(cl_bar), "r"(c0), "r"(c1), "l"(policy)
+      : "memory");
+}
+
+// ---------------------------------------------------------------- tcgen05 (CTA pairs)
+
+// Allocate `ncols` TMEM columns in both CTAs of the pair (power of two >= 32).
+// One warp of EACH CTA executes it; the address is written to `dst` in each.
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                    smem_u32(dst)),
                "r"(ncols)
                : "memory");
 }
 
 __device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
                : "memory");
 }
 
@@ -162,22 +229,28 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (bf16 inputs, fp32 accumulate).
+// D[tmem] (+)= A[smem] * B[smem]^T over the CTA pair, kind::f16 (bf16 inputs,
+// fp32 accumulate), issued by the leader: M = 256 rows of A, 128 in each CTA's
+// shared memory at the descriptor's address; the N rows of B (K-major), the
+// first N/2 in the leader's shared memory and the rest in the peer's; each
+// CTA's TMEM receives its 128 rows of D for all N columns.
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                          uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
-// Arrive once on `bar` when every previously issued MMA of this thread is done.
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+// Arrive once on the mbarrier at CTA-local address `bar` in both CTAs of the
+// pair when every MMA this thread issued before is done.
+__device__ __forceinline__ void mma_commit_both(uint64_t* bar) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_u32(bar))
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+      "[%0], %1;" ::"r"(smem_u32(bar)),
+      "h"((uint16_t)3)
       : "memory");
 }
 

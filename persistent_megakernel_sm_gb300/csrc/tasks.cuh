@@ -14,9 +14,10 @@ namespace moe {
 
 // Per-CTA control block, placed after the pipeline stages in shared memory.
 struct Ctrl {
-  uint64_t full_bar[8];
-  uint64_t empty_bar[8];
-  uint64_t acc_bar;
+  uint64_t full_bar[8];   // (leader's are used) stage s loaded in both CTAs
+  uint64_t empty_bar[8];  // stage s free again (the leader's MMAs commit to both CTAs')
+  uint64_t acc_bar;       // the tile's accumulators are complete (committed to both CTAs')
+  uint64_t tmem_empty;    // (leader's is used) the peer finished reading its TMEM, once per GEMM task
   unsigned long long deadline;
   unsigned long long t_claim, t_start;
   uint32_t tmem_base;
@@ -32,6 +33,7 @@ struct Ctrl {
   int mb_posted, mb_taken, mb_late;
   int mb_done_task[2];
   int mb_done, mb_handled;
+  int mb_done_peer;       // (leader) tasks the peer CTA has finished
   int ival[8];
   int qbase[kShards];
   unsigned long long plan_t[8];  // plan phase timestamps (trace only)
@@ -49,6 +51,9 @@ struct Ctrl {
 
 // Per-thread state that lives across tasks.
 struct CtaState {
+  int rank;             // cluster rank: 0 = the pair's leader (issues the MMAs), 1 = its peer
+  int worker;           // pair index (blockIdx.x / kPair)
+  uint32_t lead_ctrl;   // the leader's Ctrl in the cluster's shared window
   uint32_t pipe_it;     // k blocks issued / consumed so far (producer & MMA thread)
   uint32_t gemm_count;  // GEMM tasks done (all threads)
   uint64_t deadline;    // globaltimer value after which waits give up
@@ -333,7 +338,7 @@ __device__ int claim_once(const Params& p, CtaState& st, int min_depth) {
     }
     if (__shfl_sync(full, seen, 0)) {
       st.plan_seen = true;
-      st.role_mover = (int)blockIdx.x < __shfl_sync(full, nm, 0);
+      st.role_mover = st.worker < __shfl_sync(full, nm, 0);
       st.n_gather = __shfl_sync(full, ng, 0);
       st.mover_total = __shfl_sync(full, mt, 0);
       st.gemm_total = __shfl_sync(full, gt, 0);
@@ -366,7 +371,7 @@ __device__ int claim_once(const Params& p, CtaState& st, int min_depth) {
   // order, a GEMM CTA GEMM, low-priority GEMM, mover work.
   const bool mover_first = !st.plan_seen || gathers_left || st.role_mover;
   const int npass = min_depth > 1 ? 1 : 3;
-  const int home = (int)blockIdx.x & (kShards - 1);
+  const int home = st.worker & (kShards - 1);
   for (int pass = 0; pass < npass; ++pass) {
     const int qq = mover_first ? pass : (pass == 2 ? 0 : pass + 1);
     const int depth = qq == 0 ? depth_m : qq == 1 ? depth_g : depth_l;
@@ -570,7 +575,7 @@ __device__ void plan_task(const Params& p, char* scratch, Ctrl* c, bool push) {
     s->mover_total_dyn = n_gather + p.n_comb;
     s->n_gather = n_gather;
     int movers;
-    const int N = gridDim.x;
+    const int N = p.n_workers;
     if (p.mover_override > 0) {
       movers = min(p.mover_override, max(N - 1, 1));
     } else {
@@ -608,19 +613,23 @@ __device__ void plan_task(const Params& p, char* scratch, Ctrl* c, bool push) {
 }
 
 // ------------------------------------------------------------------ gather (mover)
-// Xp[row, :] = x[perm[row], :] for up to 32 rows of one group.  One thread
-// moves whole rows with bulk copies through shared memory (global -> shared
-// on an mbarrier, then shared -> global), as many rows per round as the
-// pipeline stages hold, so hundreds of KB are in flight per SM.
-__device__ void gather_task(const Params& p, int g, int chunk, char* smem, Ctrl* c,
-                            CtaState& st) {
+// Xp[row, :] = x[perm[row], :] for up to 64 rows of one group, of which this
+// CTA takes part `half` of `nhalf` (the two CTAs of a pair split the rows).
+// One thread moves whole rows with bulk copies through shared memory (global
+// -> shared on an mbarrier, then shared -> global), as many rows per round as
+// the pipeline stages hold, so hundreds of KB are in flight per SM.
+__device__ void gather_task(const Params& p, int g, int chunk, int half, int nhalf, char* smem,
+                            Ctrl* c, CtaState& st) {
   const Group G = load_group(p, g);
   if (!group_ok(p, G) || chunk * kGatherRows >= G.nrows) {
     if (threadIdx.x == 0) set_status(p, MOE_E_DEVICE, 20);
     return;
   }
-  const int r0 = G.row0 + chunk * kGatherRows;
-  const int nr = min(kGatherRows, G.nrows - chunk * kGatherRows);
+  const int nr_chunk = min(kGatherRows, G.nrows - chunk * kGatherRows);
+  const int per = ceil_div(nr_chunk, nhalf);
+  const int row_lo = min(nr_chunk, half * per);
+  const int r0 = G.row0 + chunk * kGatherRows + row_lo;
+  const int nr = min(nr_chunk, row_lo + per) - row_lo;
   // Permuted row r of expert e is the (r - off_e)-th token of e in router-tile
   // order: the tile tau with base[tau][e] <= r - off_e < base[tau+1][e], and
   // inside it the token of the (r - off_e - base[tau][e])-th set bit of the
@@ -659,7 +668,8 @@ __device__ void gather_task(const Params& p, int g, int chunk, char* smem, Ctrl*
       if (__ldcg(p.idx + (size_t)t * p.k + j) == G.e) p.pos[(size_t)t * p.k + j] = r;
   }
   cta_sync();
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0 && nr <= 0) st_release_cta_shared(&c->mb_late, st.taken);
+  if (threadIdx.x == 0 && nr > 0) {
     const uint32_t row_bytes = (uint32_t)p.d * 2;
     const int cap = max(1, (int)(((size_t)p.stages * p.stage_bytes) / row_bytes));
     fence_proxy_async_shared();
@@ -738,14 +748,24 @@ __device__ void combine_direct(const Params& p, int t0, int nt, int c0, int nvec
 // tokens and one d band (the columns of the band's down tiles).  The source
 // rows of a few tokens at a time are bulk-copied into one half of the
 // pipeline's shared memory while the other half is being summed (double
-// buffering).
-__device__ void combine_band(const Params& p, int ci, char* smem, Ctrl* c, CtaState& st) {
+// buffering).  This CTA takes part `part` of `nparts` of the tile's tokens
+// (the two CTAs of a pair split them).
+__device__ void combine_band(const Params& p, int ci, int part, int nparts, char* smem, Ctrl* c,
+                             CtaState& st) {
   const int ctile = ci / p.n_bands, band = ci - ctile * p.n_bands;
-  const int c0 = band_dt0(p, band) * 2 * kBM;
-  const int c1 = min(p.d, band_dt1(p, band) * 2 * kBM);
-  const int t0 = ctile * p.ct;
-  const int nt = min(p.ct, p.T - t0);
+  const int c0 = band_dt0(p, band) * kDTile;
+  const int c1 = min(p.d, band_dt1(p, band) * kDTile);
+  const int tt0 = ctile * p.ct;
+  const int nt_tile = min(p.ct, p.T - tt0);
+  const int per = ceil_div(nt_tile, nparts);
+  const int tok_lo = min(nt_tile, part * per);
+  const int t0 = tt0 + tok_lo;
+  const int nt = min(nt_tile, tok_lo + per) - tok_lo;
   const int k = p.k;
+  if (nt <= 0) {
+    if (threadIdx.x == 0) st_release_cta_shared(&c->mb_late, st.taken);
+    return;
+  }
   for (int i = threadIdx.x; i < nt * k; i += kThreads) {
     c->tok[i] = __ldcg(p.pos + (size_t)t0 * k + i);
     c->wsum[i] = __ldcg(p.wgt + (size_t)t0 * k + i);
@@ -882,39 +902,49 @@ __device__ void norm_tile(const Params& p, int ctile) {
   }
 }
 
-// One combine task: tile ci / n_bands, band ci % n_bands.  With the fused
-// residual + RMSNorm, the task whose band completes the tile (a counter per
-// tile) then runs the tile's norm.
-__device__ void combine_task(const Params& p, int ci, char* smem, Ctrl* c, CtaState& st) {
-  combine_band(p, ci, smem, c, st);
+// One combine task: tile ci / n_bands, band ci % n_bands, this CTA's part
+// `half` of `nhalf` of its tokens.  With the fused residual + RMSNorm, the CTA
+// whose part completes the tile (a counter per tile: every band, every part)
+// then runs the norm of the whole tile.
+__device__ void combine_task(const Params& p, int ci, int half, int nhalf, char* smem, Ctrl* c,
+                             CtaState& st) {
+  combine_band(p, ci, half, nhalf, smem, c, st);
   if (!p.norm_out) return;
   const int ctile = ci / p.n_bands;
   release_writes();
-  if (threadIdx.x == 0) c->flag = atom_add_acq_rel(p.norm_done + ctile, 1) + 1 == p.n_bands;
+  if (threadIdx.x == 0)
+    c->flag = atom_add_acq_rel(p.norm_done + ctile, 1) + 1 == p.n_bands * nhalf;
   cta_sync();
   if (!c->flag) return;
   fence_acq_rel_gpu();
   norm_tile(p, ctile);
 }
 
-// ------------------------------------------------------------------ GEMM tile (tcgen05)
-// Swap-AB tile: the weights are the M = 128 operand, the tokens the N operand,
-// so a handful of tokens still fills the tensor core's M dimension.
-//   gate/up (g, ft):  acc0 = Wg[e][ft*128 .. +128, :] * B^T,  acc1 = Wu[...] * B^T
-//   down (g, dt, s):  acc0 = Wd[e][dt*256 .. +128, Ks] * H^T, acc1 = rows +128 .. +256
-// B = the group's rows of Xp (or x for the shared expert) / of H, K-major.
-// Pipeline: warp 0 lane 0 issues TMA loads into a ring of `stages` stages,
-// warp 1 lane 0 issues tcgen05.mma into two TMEM accumulators, all 8 warps
-// run the epilogue from TMEM.
+// ------------------------------------------------------------------ GEMM tile (tcgen05, CTA pair)
+// Swap-AB tile on a pair of SMs: the weights are the MMA's M = 256 operand
+// (128 rows in each CTA's shared memory), the tokens its N operand (the first
+// N/2 rows in the leader's shared memory, the rest in the peer's), so a
+// handful of tokens still fills the tensor core's M dimension and each CTA
+// stages only half of the token rows.
+//   gate/up (g, ft):  acc0 = Wg[e][ft*256 .. +256, :] * B^T,  acc1 = Wu[...] * B^T
+//   down (g, dt, s):  acc0 = Wd[e][dt*512 .. +256, Ks] * H^T, acc1 = rows +256 .. +512
+// CTA r holds rows 128 r .. 128 r + 127 of each accumulator (its TMEM lanes)
+// for all N tokens.  B = the group's rows of Xp (or x for the shared
+// expert) / of H, K-major.
+// Pipeline: in each CTA warp 0 lane 0 issues the TMA loads of its halves into
+// a ring of `stages` stages and signals the leader's full barrier; the
+// leader's warp 1 lane 0 issues tcgen05.mma.cta_group::2 into both CTAs' TMEM
+// and commits each stage to both CTAs' empty barriers; all 8 warps of each CTA
+// run the epilogue from their own TMEM.
 
 struct GemmJob {
   const CUtensorMap* a0;
   const CUtensorMap* a1;  // null: one accumulator only
   const CUtensorMap* b;
-  int a_row0, a1_row0;    // A rows of the two accumulators
-  int b_row0;             // first B row
-  int b_rows;             // B rows to load (boxes of 32 rows)
-  int n_mma;              // MMA N (multiple of 16, <= 256)
+  int a_row0, a1_row0;    // this CTA's first A rows of the two accumulators
+  int b_row0;             // this CTA's first B row
+  int b_rows;             // B rows this CTA loads (n_mma / 2, in boxes of 32 rows)
+  int n_mma;              // MMA N over the pair (multiple of 32, <= 256)
   int b_off;              // byte offset of the B tile inside a stage (1024-aligned)
   int kb0, nkb;           // first k block and number of k blocks
   bool a_stream;          // A is read by this task only (L2 evict-first); else kept (evict-last)
@@ -922,30 +952,41 @@ struct GemmJob {
 };
 
 // Returns false on a timeout (status already set).
-__device__ bool make_gemm_job(const Params& p, const Maps& maps, int task, GemmJob& job);
+__device__ bool make_gemm_job(const Params& p, const Maps& maps, int task, int rank, GemmJob& job);
 
-// Producer: TMA loads of k blocks [kb_from, kb_to) of `job` into the stages
-// starting at pipeline index it0.  Returns the number of k blocks issued
-// (fewer on a timeout).
+// Tasks posted to this CTA's mailbox by the leader's scheduler warp: in the
+// same CTA for the leader (CTA scope), from the other CTA for the peer
+// (cluster scope).
+__device__ __forceinline__ int mailbox_posted(Ctrl* c, const CtaState& st) {
+  return st.rank == 0 ? ld_acquire_cta_shared(&c->mb_posted)
+                      : ld_acquire_cluster(smem_u32(&c->mb_posted));
+}
+
+// Producer: TMA loads of this CTA's halves of k blocks [kb_from, kb_to) of
+// `job` into the stages starting at pipeline index it0.  Both CTAs load the
+// same number of bytes per stage; the leader's full barrier expects the
+// pair's total.  Returns the number of k blocks issued (fewer on a timeout).
 __device__ int issue_loads(const Params& p, const GemmJob& job, char* smem, Ctrl* c,
                            const CtaState& st, uint32_t it0, int kb_from, int kb_to,
                            uint64_t pol_a, uint64_t pol_b) {
   const int nbox = ceil_div(job.b_rows, kBBoxRows);
   const bool two = job.a1 != nullptr;
   const uint32_t bytes = (two ? 2u : 1u) * kABoxBytes + (uint32_t)nbox * kBBoxBytes;
+  const uint32_t full0 = st.lead_ctrl + (uint32_t)offsetof(Ctrl, full_bar);
   uint32_t it = it0;
   int kb = kb_from;
   for (; kb < kb_to; ++kb, ++it) {
     const uint32_t s = it % p.stages, ph = (it / p.stages) & 1u;
     if (!mbar_wait(&c->empty_bar[s], ph ^ 1u, st.deadline)) break;
     char* stage = smem + (size_t)s * p.stage_bytes;
-    mbar_arrive_expect_tx(&c->full_bar[s], bytes);
+    if (st.rank == 0) mbar_arrive_expect_tx(&c->full_bar[s], (uint32_t)kPair * bytes);
+    const uint32_t fb = full0 + 8u * s;
     const int kc = (job.kb0 + kb) * kBK;
-    tma_load_2d(stage, job.a0, &c->full_bar[s], kc, job.a_row0, pol_a);
-    if (two) tma_load_2d(stage + kABoxBytes, job.a1, &c->full_bar[s], kc, job.a1_row0, pol_a);
+    tma_load_2d_pair(stage, job.a0, fb, kc, job.a_row0, pol_a);
+    if (two) tma_load_2d_pair(stage + kABoxBytes, job.a1, fb, kc, job.a1_row0, pol_a);
     for (int bx = 0; bx < nbox; ++bx)
-      tma_load_2d(stage + job.b_off + bx * kBBoxBytes, job.b, &c->full_bar[s], kc,
-                  job.b_row0 + bx * kBBoxRows, pol_b);
+      tma_load_2d_pair(stage + job.b_off + bx * kBBoxBytes, job.b, fb, kc,
+                       job.b_row0 + bx * kBBoxRows, pol_b);
   }
   return kb - kb_from;
 }
@@ -973,13 +1014,14 @@ __device__ bool gemm_mainloop(const Params& p, const Maps& maps, const GemmJob& 
     // so its late phase begins (the scheduler warp may claim the next task
     // now).  Until this tile's MMAs complete, wait for that task; when it is
     // a GEMM tile too, start its first stages now -- they fill as this tile's
-    // last MMAs release the stages.
+    // last MMAs release the stages.  (Both CTAs of the pair receive the same
+    // tasks in the same order, so their producers stay in step.)
     int nxt = -1;
     if (ok && job.task >= 0) {
       st_release_cta_shared(&c->mb_late, st.taken);
       const uint32_t acc_parity = st.gemm_count & 1u;
       while (true) {
-        if (ld_acquire_cta_shared(&c->mb_posted) > st.taken) {
+        if (mailbox_posted(c, st) > st.taken) {
           nxt = c->mb_task[st.taken & 1];
           break;
         }
@@ -991,7 +1033,7 @@ __device__ bool gemm_mainloop(const Params& p, const Maps& maps, const GemmJob& 
     }
     if (ok && p.prefetch && job.task >= 0 && nxt >= 0) {
       GemmJob nj;
-      if (make_gemm_job(p, maps, nxt, nj)) {
+      if (make_gemm_job(p, maps, nxt, st.rank, nj)) {
         fence_acq_rel_gpu();
         fence_proxy_async_global();
         const int n = min(p.stages, nj.nkb);
@@ -1007,35 +1049,50 @@ __device__ bool gemm_mainloop(const Params& p, const Maps& maps, const GemmJob& 
         }
       }
     }
-  } else if (warp == 1 && lane == 0) {
-    const uint32_t idesc = idesc_bf16(kBM, (uint32_t)job.n_mma);
-    const uint32_t t0 = c->tmem_base, t1 = c->tmem_base + kAcc1Col;
-    uint32_t it = st.pipe_it;
-    for (int kb = 0; kb < job.nkb; ++kb, ++it) {
-      const uint32_t s = it % p.stages, ph = (it / p.stages) & 1u;
-      if (!mbar_wait(&c->full_bar[s], ph, st.deadline)) {
-        set_status(p, MOE_E_TIMEOUT, 11);
+  } else if (warp == 1 && lane == 0 && st.rank == 0) {
+    // the leader issues the pair's MMAs, once the peer's epilogue of the
+    // previous GEMM task has finished reading the peer's TMEM
+    if (st.gemm_count > 0) {
+      const uint32_t par = (st.gemm_count - 1u) & 1u;
+      bool got;
+      while (!(got = mbar_try_wait_cluster(&c->tmem_empty, par)))
+        if (globaltimer() > st.deadline) break;
+      if (!got) {
+        set_status(p, MOE_E_TIMEOUT, 14);
         ok = false;
-        break;
       }
-      tc_fence_after();
-      const uint32_t base = smem_u32(smem + (size_t)s * p.stage_bytes);
-      const uint64_t da0 = sw128_desc(base), da1 = sw128_desc(base + kABoxBytes);
-      const uint64_t db = sw128_desc(base + job.b_off);
-#pragma unroll
-      for (int kk = 0; kk < kBK / 16; ++kk) {
-        const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
-        // advancing 16 bf16 (32 B) inside the 128-B swizzle row: +2 in the
-        // 16-byte-granular start-address field
-        mma_bf16(t0, da0 + 2 * kk, db + 2 * kk, idesc, acc);
-        if (two) mma_bf16(t1, da1 + 2 * kk, db + 2 * kk, idesc, acc);
-      }
-      mma_commit(&c->empty_bar[s]);
     }
-    mma_commit(&c->acc_bar);
+    if (ok) {
+      const uint32_t idesc = idesc_bf16(kPair * kBM, (uint32_t)job.n_mma);
+      const uint32_t t0 = c->tmem_base, t1 = c->tmem_base + kAcc1Col;
+      uint32_t it = st.pipe_it;
+      for (int kb = 0; kb < job.nkb; ++kb, ++it) {
+        const uint32_t s = it % p.stages, ph = (it / p.stages) & 1u;
+        if (!mbar_wait(&c->full_bar[s], ph, st.deadline)) {
+          set_status(p, MOE_E_TIMEOUT, 11);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t base = smem_u32(smem + (size_t)s * p.stage_bytes);
+        const uint64_t da0 = sw128_desc(base), da1 = sw128_desc(base + kABoxBytes);
+        const uint64_t db = sw128_desc(base + job.b_off);
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk) {
+          const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+          // advancing 16 bf16 (32 B) inside the 128-B swizzle row: +2 in the
+          // 16-byte-granular start-address field
+          mma_bf16(t0, da0 + 2 * kk, db + 2 * kk, idesc, acc);
+          if (two) mma_bf16(t1, da1 + 2 * kk, db + 2 * kk, idesc, acc);
+        }
+        mma_commit_both(&c->empty_bar[s]);
+      }
+    }
+    // (also after a failure, so that both CTAs' epilogue warps stop waiting)
+    mma_commit_both(&c->acc_bar);
   }
   st.pipe_it += job.nkb;
-  // everyone waits for the accumulators
+  // everyone waits for the accumulators (the leader's commit reaches both CTAs)
   __syncwarp();
   const int ok_all = cta_sync_and(ok ? 1 : 0);
   if (!ok_all) return false;
@@ -1046,24 +1103,36 @@ __device__ bool gemm_mainloop(const Params& p, const Maps& maps, const GemmJob& 
   return true;
 }
 
+// The end of every GEMM task (router, gate/up, down), in both CTAs, whether
+// it succeeded or not: this CTA's TMEM reads are complete; the peer tells the
+// leader, whose next MMAs overwrite the peer's accumulators.
+__device__ __forceinline__ void gemm_task_end(Ctrl* c, CtaState& st) {
+  tc_fence_before();
+  st.gemm_count++;
+  if (st.rank != 0) {
+    cta_sync();
+    if (threadIdx.x == 0) mbar_arrive_cluster(st.lead_ctrl + (uint32_t)offsetof(Ctrl, tmem_empty));
+  }
+}
+
 __device__ __forceinline__ float silu_f(float z) { return z / (1.f + __expf(-z)); }
 
-// The GEMM job of a gate/up or down task id (false for other task types or
-// an inconsistent group).
-__device__ bool make_gemm_job(const Params& p, const Maps& maps, int task, GemmJob& job) {
+// The GEMM job of a gate/up or down task id for the CTA of cluster rank
+// `rank` (false for other task types or an inconsistent group).
+__device__ bool make_gemm_job(const Params& p, const Maps& maps, int task, int rank, GemmJob& job) {
   const int type = task_type(task), pl = task_payload(task);
   if (type == kTaskGateUp) {
     const int g = pl / p.n_ftiles, ft = pl - g * p.n_ftiles;
     const Group G = load_group(p, g);
     if (!group_ok(p, G) || ft < 0 || ft >= p.n_ftiles) return false;
+    job.n_mma = ((G.nrows + 31) / 32) * 32;
     job.a0 = &maps.wg;
     job.a1 = &maps.wu;
     job.b = G.e < p.E ? &maps.xp : &maps.x;
-    job.a_row0 = G.e * p.f + ft * kBM;
+    job.a_row0 = G.e * p.f + ft * kFTile + rank * kBM;
     job.a1_row0 = job.a_row0;
-    job.b_row0 = G.src_row0;
-    job.b_rows = G.nrows;
-    job.n_mma = ((G.nrows + 15) / 16) * 16;
+    job.b_row0 = G.src_row0 + rank * (job.n_mma / 2);
+    job.b_rows = job.n_mma / 2;
     job.b_off = 2 * kABoxBytes;
     job.kb0 = 0;
     job.nkb = p.d / kBK;
@@ -1077,14 +1146,14 @@ __device__ bool make_gemm_job(const Params& p, const Maps& maps, int task, GemmJ
     const int dt = r / p.ks, ksplit = r - dt * p.ks;
     const Group G = load_group(p, g);
     if (!group_ok(p, G) || dt >= p.n_dtiles) return false;
+    job.n_mma = ((G.nrows + 31) / 32) * 32;
     job.a0 = &maps.wd;
     job.a1 = &maps.wd;
     job.b = &maps.h;
-    job.a_row0 = G.e * p.d + dt * 2 * kBM;
-    job.a1_row0 = job.a_row0 + kBM;
-    job.b_row0 = G.row0;
-    job.b_rows = G.nrows;
-    job.n_mma = ((G.nrows + 15) / 16) * 16;
+    job.a_row0 = G.e * p.d + dt * kDTile + rank * kBM;
+    job.a1_row0 = job.a_row0 + kPair * kBM;
+    job.b_row0 = G.row0 + rank * (job.n_mma / 2);
+    job.b_rows = job.n_mma / 2;
     job.b_off = 2 * kABoxBytes;
     job.kb0 = ksplit * p.kb_down;
     job.nkb = p.kb_down;
@@ -1101,29 +1170,31 @@ __device__ void gateup_task(const Params& p, const Maps& maps, int task, char* s
   const int g = pl / p.n_ftiles, ft = pl - g * p.n_ftiles;
   const Group G = load_group(p, g);
   GemmJob job;
-  if (!make_gemm_job(p, maps, task, job)) {
+  if (!make_gemm_job(p, maps, task, st.rank, job)) {
     if (threadIdx.x == 0) set_status(p, MOE_E_DEVICE, 21);
+    gemm_task_end(c, st);
     return;
   }
   const bool ok = gemm_mainloop(p, maps, job, smem, c, st);
   if (ok) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q = warp & 3, half = warp >> 2;
-    const int m = q * 32 + lane;  // f row inside the tile
+    // this thread's f row: row m of this CTA's 128 rows of the 256-row tile
+    const int frow = ft * kFTile + st.rank * kBM + q * 32 + lane;
+    const bool in_f = frow < p.f;  // the last tile of an f that is an odd multiple of 128
     const uint32_t lane_addr = c->tmem_base + ((uint32_t)(q * 32) << 16);
-    __nv_bfloat16* hcol = p.H + (size_t)G.row0 * p.f + ft * kBM + m;
+    __nv_bfloat16* hcol = p.H + (size_t)G.row0 * p.f + frow;
     for (int ch = half; ch * 16 < G.nrows; ch += 2) {
       float gv[16], uv[16];
       tmem_ld2x16(lane_addr + ch * 16, lane_addr + kAcc1Col + ch * 16, gv, uv);
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const int n = ch * 16 + i;
-        if (n < G.nrows) hcol[(size_t)n * p.f] = __float2bfloat16_rn(silu_f(gv[i]) * uv[i]);
+        if (in_f && n < G.nrows) hcol[(size_t)n * p.f] = __float2bfloat16_rn(silu_f(gv[i]) * uv[i]);
       }
     }
   }
-  tc_fence_before();
-  st.gemm_count++;
+  gemm_task_end(c, st);
 }
 
 __device__ void down_task(const Params& p, const Maps& maps, int task, char* smem, Ctrl* c,
@@ -1134,18 +1205,20 @@ __device__ void down_task(const Params& p, const Maps& maps, int task, char* sme
   const int dt = r / p.ks, ksplit = r - dt * p.ks;
   const Group G = load_group(p, g);
   GemmJob job;
-  if (!make_gemm_job(p, maps, task, job)) {
+  if (!make_gemm_job(p, maps, task, st.rank, job)) {
     if (threadIdx.x == 0) set_status(p, MOE_E_DEVICE, 22);
+    gemm_task_end(c, st);
     return;
   }
   const bool ok = gemm_mainloop(p, maps, job, smem, c, st);
   if (ok) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q = warp & 3, half = warp >> 2;
-    const int m = q * 32 + lane;
-    const int col0 = dt * 2 * kBM + m, col1 = col0 + kBM;
+    // this thread's two d columns: row m of this CTA's 128 rows of each
+    // accumulator's 256
+    const int col0 = dt * kDTile + st.rank * kBM + q * 32 + lane, col1 = col0 + kPair * kBM;
     const uint32_t lane_addr = c->tmem_base + ((uint32_t)(q * 32) << 16);
-    const bool has1 = col1 < p.d;
+    const bool has0 = col0 < p.d, has1 = col1 < p.d;
     for (int ch = half; ch * 16 < G.nrows; ch += 2) {
       float a[16], b[16];
       tmem_ld2x16(lane_addr + ch * 16, lane_addr + kAcc1Col + ch * 16, a, b);
@@ -1156,7 +1229,7 @@ __device__ void down_task(const Params& p, const Maps& maps, int task, char* sme
           const int n = ch * 16 + i;
           if (n < G.nrows) {
             float* yr = Y + (size_t)(G.row0 + n) * p.d;
-            yr[col0] = a[i];
+            if (has0) yr[col0] = a[i];
             if (has1) yr[col1] = b[i];
           }
         }
@@ -1167,15 +1240,14 @@ __device__ void down_task(const Params& p, const Maps& maps, int task, char* sme
           const int n = ch * 16 + i;
           if (n < G.nrows) {
             __nv_bfloat16* yr = Y + (size_t)(G.row0 + n) * p.d;
-            yr[col0] = __float2bfloat16_rn(a[i]);
+            if (has0) yr[col0] = __float2bfloat16_rn(a[i]);
             if (has1) yr[col1] = __float2bfloat16_rn(b[i]);
           }
         }
       }
     }
   }
-  tc_fence_before();
-  st.gemm_count++;
+  gemm_task_end(c, st);
 }
 
 
@@ -1379,19 +1451,26 @@ __device__ __forceinline__ void route_epilogue_k(const Params& p, Ctrl* c, int t
   else route_epilogue<16>(p, c, tile, nt, lg, ls, xch);
 }
 
-// One router task: tile `tile`, K split `split` of p.route_ks.  With a single
-// split the epilogue reads the logits from TMEM.  With several, each split
-// stores its fp32 partial logits; the split that finishes last sums all of
-// them in split order (fixed, so the result does not depend on timing) and
-// runs the epilogue.  Returns true when this call completed the tile.
-__device__ bool route_task(const Params& p, const Maps& maps, int tile, int split, char* smem,
+// One router task: router tiles 2 pt (the leader's) and 2 pt + 1 (the
+// peer's), K split `split` of p.route_ks, as one pair MMA: each CTA's 128 A
+// rows are its tile's tokens, and the experts (N, padded to 32) are split in
+// halves between the two CTAs' B operands, so each CTA's TMEM receives all
+// the logits of its own tokens.  With a single split the epilogue reads the
+// logits from TMEM.  With several, each split stores its fp32 partial logits;
+// the split that finishes last sums all of them in split order (fixed, so the
+// result does not depend on timing) and runs the epilogue.  Returns true when
+// this call completed this CTA's tile (the peer of an odd last tile has none).
+__device__ bool route_task(const Params& p, const Maps& maps, int pt, int split, char* smem,
                            Ctrl* c, CtaState& st) {
   const int rt = p.rt;  // tokens of a router tile: 128, or 64 for small layers
+  const int tile = pt * kPair + st.rank;
+  const bool mine = tile < p.n_route;
   const int t0 = tile * rt;
-  const int nt = min(rt, p.T - t0);
+  const int nt = mine ? min(rt, p.T - t0) : 0;
   const int ks = p.route_ks;
   const int nkb = p.d / kBK;
-  const int epad = ((p.E + 15) / 16) * 16;
+  const int epad = ((p.E + 15) / 16) * 16;   // logit columns read back
+  const int nmma = ((p.E + 31) / 32) * 32;   // MMA N over the pair
   for (int i = threadIdx.x; i < kMaxE * 4; i += kThreads) c->mask[i] = 0u;
   for (int e = threadIdx.x; e < kMaxE; e += kThreads)
     c->bias_s[e] = (p.bias && e < p.E) ? __ldg(p.bias + e) : 0.f;
@@ -1399,11 +1478,11 @@ __device__ bool route_task(const Params& p, const Maps& maps, int tile, int spli
   job.a0 = &maps.xr;
   job.a1 = nullptr;
   job.b = &maps.wr;
-  job.a_row0 = t0;
+  job.a_row0 = t0;  // past T (the peer of an odd last tile): zero-filled rows
   job.a1_row0 = 0;
-  job.b_row0 = 0;
-  job.b_rows = p.E;
-  job.n_mma = epad;
+  job.b_row0 = st.rank * (nmma / 2);
+  job.b_rows = nmma / 2;
+  job.n_mma = nmma;
   job.b_off = kABoxBytes;
   job.kb0 = split * nkb / ks;
   job.nkb = (split + 1) * nkb / ks - job.kb0;
@@ -1411,7 +1490,7 @@ __device__ bool route_task(const Params& p, const Maps& maps, int tile, int spli
   job.task = -1;
   const bool ok = gemm_mainloop(p, maps, job, smem, c, st);
   bool tile_done = false;
-  if (ok) {
+  if (ok && mine) {
     const int warp = threadIdx.x >> 5;
     const uint32_t lane_addr = c->tmem_base + ((uint32_t)((warp & 3) * 32) << 16);
     const int ls = route_row_stride(p.E);
@@ -1495,8 +1574,7 @@ __device__ bool route_task(const Params& p, const Maps& maps, int tile, int spli
       }
     }
   }
-  tc_fence_before();
-  st.gemm_count++;
+  gemm_task_end(c, st);
   return tile_done;
 }
 

@@ -1,8 +1,9 @@
 """Summaries of the persistent kernel's task trace (MOE_OPT_TRACE).
 
-``MoELayer.trace()`` returns one record per executed task -- the CTA, the task
-id, and the %globaltimer times at which the task was claimed, started and
-finished -- plus one record per plan phase and one exit record per CTA.
+``MoELayer.trace()`` returns one record per executed task -- the CTA (the
+leader of the CTA pair that ran it), the task id, and the %globaltimer times
+at which the task was claimed, started and finished -- plus one record per
+plan phase and one exit record per pair.
 ``summarize`` turns those records into what explains a layer's time: each
 task type's window and durations, the CTAs' utilisation over time per task
 type, the gaps between consecutive tasks on a CTA, and the plan's phases.
@@ -27,10 +28,11 @@ def summarize(tr: dict, n_bins: int = 20) -> dict:
     the result are microseconds from the first claim.  Keys:
 
     - ``span_us``: first claim to last task end;
-    - ``grid``: CTAs that wrote an exit record;
+    - ``grid``: workers (CTA pairs, whose leaders write the records) that
+      wrote an exit record;
     - ``types``: per task type, count, first start, last end and the median
       and maximum duration;
-    - ``busy_us``: the summed task time divided by the grid (the span the
+    - ``busy_us``: the summed task time divided by the workers (the span the
       tasks would take packed perfectly);
     - ``bins``: ``n_bins`` equal time windows, each with the fraction of
       CTA-time spent in each task type and in total;

@@ -40,9 +40,10 @@ def test_every_task_runs_exactly_once(case):
     assert layer.stat("tasks") == len(tasks)
     types = set((tasks >> 28).tolist())
     assert types == {1, 2, 3, 4, 5}, types
-    # every CTA recorded its exit after its last task
+    # every CTA pair (its leader) recorded its exit after its last task
     exits = tr["cta"][tr["task"] == 0x7FFFFFFF]
-    assert len(exits) == layer.stat("grid") and len(np.unique(exits)) == len(exits)
+    assert len(exits) == layer.stat("grid") // 2 and len(np.unique(exits)) == len(exits)
+    assert np.all(exits % 2 == 0), "exit records come from the pairs' leaders"
     # dependency order: per group, gate/up before down; a combine after all downs
     t_end = tr["t_end"][real]
     t_start = tr["t_start"][real]
@@ -52,7 +53,7 @@ def test_every_task_runs_exactly_once(case):
     from persistent_megakernel_sm_gb300.trace_report import summarize
     s = summarize(tr)
     assert set(s["types"]) == {"route", "gather", "gateup", "down", "combine"}
-    assert s["grid"] == layer.stat("grid") and len(s["plan_phases_us"]) == 8
+    assert s["grid"] == layer.stat("grid") // 2 and len(s["plan_phases_us"]) == 8
     assert sum(t["n"] for t in s["types"].values()) == layer.stat("tasks")
     layer.close()
 
@@ -109,22 +110,23 @@ def test_router_tile_size_keeps_routing_and_tolerance(case, rt):
 
 @pytest.mark.parametrize("grid", [None, 37])
 def test_spatial_split_matches_oracle(case, grid):
-    # the plan's split of the CTAs into movers and GEMM workers, from the
-    # routed counts, against the oracle's fp32 statement of the same cost
-    # model with the kernel's constants (40 GB/s per mover, 1925 TF/s over
-    # 152 SMs per GEMM worker, 6.79 TB/s of weight stream)
+    # the plan's split of the workers (CTA pairs) into movers and GEMM
+    # workers, from the routed counts, against the oracle's fp32 statement of
+    # the same cost model with the kernel's constants per pair (80 GB/s per
+    # mover, two SMs' share of 1925 TF/s per GEMM worker, 6.79 TB/s of weight
+    # stream)
     w, inp, dev, ref = case
     layer, out, routing = _run(w, dev, **({} if grid is None else dict(grid_ctas=grid)))
     hz.check_out(out, ref)
     counts = oracle.permute(oracle.route(inp["x"], inp["router_w"], inp["bias"], w.k)["idx"],
                             w.E)[0]
-    N = layer.stat("grid")
+    N = layer.stat("grid") // 2
     # the combine reads each expert output as stored: bf16 (2 bytes) or ks
     # fp32 partial sums (4 ks bytes), whichever layout this forward used
     ybytes = layer.stat("y_bytes")
     assert ybytes in (2, 4, 8, 16)
     want, x = oracle.movers(w.T, w.d, w.f, w.k, w.S, int(np.count_nonzero(counts)), N, ybytes,
-                            40e9, float(np.float32(1925e12) / np.float32(152)), 6.79e12)
+                            80e9, float(np.float32(1925e12) / np.float32(76)), 6.79e12)
     got = layer.stat("mover_ctas")
     if abs(x - np.floor(x) - 0.5) < 1e-3:  # fp32 contraction may tip a near tie
         assert abs(got - want) <= 1, (got, want, x)
