@@ -76,12 +76,12 @@ typedef struct moe_layer moe_layer_t;
 /* option keys for moe_layer_set_option */
 #define MOE_OPT_MODE 1         /* MOE_MODE_*                                   */
 #define MOE_OPT_TIMEOUT_NS 2   /* device wait budget in ns (default 2e9)      */
-#define MOE_OPT_MOVER_CTAS 3   /* >0: fixed number of mover workers (CTA
-                                  pairs); 0 = the cost model                  */
+#define MOE_OPT_MOVER_CTAS 3   /* >0: fixed number of mover workers (a CTA or
+                                  a CTA pair each); 0 = the cost model        */
 #define MOE_OPT_GRID_CTAS 4    /* >0: CTAs of the persistent (and static)
-                                  grid, used rounded down to pairs (at least
-                                  one pair); 0 = every SM pair the device
-                                  keeps resident                              */
+                                  grid, rounded down to whole workers (at
+                                  least one); 0 = one CTA per SM (every SM
+                                  pair the device keeps resident, for pairs) */
 #define MOE_OPT_SPLIT_K 5      /* down-projection K splits (1,2,4; 0 = auto)  */
 #define MOE_OPT_TOKENS_PER_TILE 6 /* max tokens per GEMM tile: 0 = auto, else
                                      16..256 in steps of 16, used rounded up
@@ -121,12 +121,19 @@ typedef struct moe_layer moe_layer_t;
                                   mean expert load is at most half a GEMM
                                   tile, else off; 0 = off                      */
 
+#define MOE_OPT_PAIR 16        /* CTAs per worker: 2 = GEMM tiles on CTA pairs
+                                  (clusters of two SMs sharing one tensor-core
+                                  tile, tcgen05 .cta_group::2, M = 256), 1 =
+                                  one CTA per tile (M = 128); 0 (default) =
+                                  pairs when the mean rows per expert
+                                  (T k / E) are at least 128                 */
+
 /* statistics keys for moe_layer_get_stat (values of the last forward;
  * moe_layer_status must have been called after it) */
-#define MOE_STAT_MOVER_CTAS 1  /* mover workers (CTA pairs) the cost model chose */
+#define MOE_STAT_MOVER_CTAS 1  /* mover workers the cost model chose          */
 #define MOE_STAT_TASKS 2       /* tasks executed (all types)                   */
-#define MOE_STAT_GRID 3        /* CTAs launched for the persistent kernel (two
-                                  per worker: clusters of a CTA pair)         */
+#define MOE_STAT_GRID 3        /* CTAs launched for the persistent kernel
+                                  (MOE_STAT_PAIR per worker)                  */
 #define MOE_STAT_GEMM_TASKS 4  /* expert GEMM tasks executed                   */
 #define MOE_STAT_MOVER_TASKS 5 /* gather + combine tasks executed              */
 #define MOE_STAT_STOLEN 6      /* tasks a CTA ran from the other role's queue  */
@@ -140,6 +147,7 @@ typedef struct moe_layer moe_layer_t;
                                   outputs) or 4 * split_k (fp32 partials)     */
 #define MOE_STAT_COMBINE_TOKENS 13 /* tokens per combine tile of the last
                                       forward                                  */
+#define MOE_STAT_PAIR 14       /* CTAs per worker of the last forward (1 or 2) */
 
 /* Create a layer description.  Pure host call (no CUDA call, no allocation on
  * the device).  Returns NULL on invalid dimensions (see moe_last_error),

@@ -23,10 +23,11 @@ OPTIONS = {
     "mode": 1, "timeout_ns": 2, "mover_ctas": 3, "grid_ctas": 4, "split_k": 5,
     "tokens_per_tile": 6, "fault_drop_task": 7, "route_tokens": 8, "claim_ahead": 9,
     "trace": 10, "release": 11, "prefetch": 12, "bands": 13, "route_splits": 14, "l2_prefetch": 15,
+    "pair": 16,
 }
 STATS = {"mover_ctas": 1, "tasks": 2, "grid": 3, "gemm_tasks": 4, "mover_tasks": 5, "stolen": 6,
          "ahead": 7, "trace_records": 8, "tile_tokens": 9, "split_k": 10, "bands": 11, "y_bytes": 12,
-         "combine_tokens": 13}
+         "combine_tokens": 13, "pair": 14}
 TASK_TYPES = {1: "route", 2: "gather", 3: "gateup", 4: "down", 5: "combine", 6: "plan"}
 
 _vp, _i32, _i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong

@@ -11,16 +11,14 @@
 namespace moe {
 
 constexpr int kThreads = 256;       // 8 warps per CTA
-constexpr int kPair = 2;            // CTAs per worker: a cluster of two on an SM pair
-constexpr int kBM = 128;            // weight rows per accumulator in one CTA (the pair's MMA M is 256)
-constexpr int kFTile = kPair * kBM;      // f rows of a gate/up task (per accumulator, both CTAs)
-constexpr int kDTile = 2 * kPair * kBM;  // d rows of a down task (two accumulators, both CTAs)
+constexpr int kBM = 128;            // weight rows per accumulator in one CTA (a pair's MMA M is 256)
+constexpr int kPairMinRows = 128;   // mean rows per expert from which GEMM tiles run on CTA pairs
 constexpr int kBK = 64;             // K elements per pipeline stage (128 B rows)
 constexpr int kABoxBytes = kBM * kBK * 2;   // 16 KB weight box
 constexpr int kBBoxRows = 32;       // token rows per activation box
 constexpr int kBBoxBytes = kBBoxRows * kBK * 2;  // 4 KB
-constexpr int kGatherRows = 64;     // permuted rows per gather task (32 per CTA of a pair)
-constexpr int kRouteTokens = 128;   // tokens per router tile (one CTA's half of the MMA M)
+constexpr int kGatherRowsCta = 32;  // permuted rows per gather task and CTA of the worker
+constexpr int kRouteTokens = 128;   // tokens per router tile (one CTA's 128 rows of the MMA M)
 constexpr int kRouteTokensSmall = 64;  // router tile of small layers with many experts
 constexpr int kSmallRouteT = 1024;
 constexpr int kSmallRouteMinE = 64;
@@ -38,10 +36,10 @@ constexpr int kReleaseExpert = 1;
 
 // task types (bits 28-31 of a task id)
 enum TaskType : int {
-  kTaskRoute = 1,    // router tiles (one per CTA of the pair): logits, softmax, top-k, counts
+  kTaskRoute = 1,    // router tiles (one per CTA of the worker): logits, softmax, top-k, counts
   kTaskGather = 2,   // mover: copy token rows of x into permuted rows of Xp
-  kTaskGateUp = 3,   // GEMM: H = bf16(silu(Xp Wg^T) * (Xp Wu^T)), one 256-row f tile
-  kTaskDown = 4,     // GEMM: Y = H Wd^T, one 512-row d tile, one K split
+  kTaskGateUp = 3,   // GEMM: H = bf16(silu(Xp Wg^T) * (Xp Wu^T)), one f tile (128 rows per CTA)
+  kTaskDown = 4,     // GEMM: Y = H Wd^T, one d tile (256 rows per CTA), one K split
   kTaskCombine = 5,  // mover: out = bf16(sum_j w_j Y[pos] + Y_shared)
   kTaskPlan = 6,     // (trace records only) the plan, run inline after the last router tile
 };
@@ -99,18 +97,19 @@ struct Params {
   // problem
   int T, d, f, E, k, S;
   // tiling
+  int pair;          // CTAs per worker: 1, or 2 (a cluster whose CTAs share each GEMM tile)
   int bn_max;        // max tokens per GEMM tile (multiple of 32, <= 256)
   int stages;        // pipeline stages
-  int stage_bytes;   // 2 * kABoxBytes + ceil(bn_max / 2 / 32) * kBBoxBytes
-  int n_ftiles;      // ceil(f / 256): each gate/up task covers 256 f rows
-  int n_dtiles;      // ceil(d / 512): each down task covers 512 d rows
+  int stage_bytes;   // 2 * kABoxBytes + ceil(bn_max / pair / 32) * kBBoxBytes
+  int n_ftiles;      // ceil(f / (128 pair)): each gate/up task covers 128 f rows per CTA
+  int n_dtiles;      // ceil(d / (256 pair)): each down task covers 256 d rows per CTA
   int ks;            // split of the down projection's K (= f)
   int kb_down;       // k blocks (of 64) per down split
   int rt;            // tokens per router tile (kRouteTokens or kRouteTokensSmall)
   int n_route;       // router tiles
   int route_ks;      // K splits of a router tile
-  int n_route_tasks; // ceil(n_route / 2) * route_ks (a task covers one tile per CTA of the pair)
-  int n_workers;     // CTA pairs of the persistent grid (the cost model's N)
+  int n_route_tasks; // ceil(n_route / pair) * route_ks (a task covers one tile per CTA)
+  int n_workers;     // workers of the persistent grid (the cost model's N)
   int release;       // kReleaseAll or kReleaseExpert
   int prefetch;      // producer starts the next claimed GEMM tile's loads early
   int ct;            // tokens per combine tile

@@ -31,11 +31,14 @@ __device__ __forceinline__ char* align1024(char* p) {
 }
 
 // CTA set-up shared by every kernel: barriers, TMEM, per-thread state.  The
-// kernels with tensor-core tasks (`pair`) run as clusters of two CTAs: their
-// TMEM is allocated for the pair (one warp in each CTA) and a cluster barrier
-// makes both CTAs' barriers visible before any traffic between them.
+// kernels with tensor-core tasks allocate TMEM (`tmem`); built for CTA pairs
+// (P = 2) they run as clusters of two CTAs, allocate the TMEM for the pair
+// (one warp in each CTA), and pass a cluster barrier that makes both CTAs'
+// barriers visible before any traffic between them.
+template <int P>
 __device__ __forceinline__ void cta_setup(const Params& p, const Maps& maps, char*& smem,
-                                          Ctrl*& c, CtaState& st, bool pair) {
+                                          Ctrl*& c, CtaState& st, bool tmem) {
+  constexpr bool pair = P == 2;
   extern __shared__ __align__(1024) char smem_raw[];
   smem = align1024(smem_raw);
   c = reinterpret_cast<Ctrl*>(smem + (size_t)p.stages * p.stage_bytes);
@@ -55,9 +58,9 @@ __device__ __forceinline__ void cta_setup(const Params& p, const Maps& maps, cha
     c->mb_posted = c->mb_taken = c->mb_done = c->mb_handled = c->mb_done_peer = 0;
     c->mb_late = -1;
   }
-  if (pair && warp == 1) {
-    tmem_alloc(&c->tmem_base, kTmemCols);
-    tmem_relinquish();
+  if (tmem && warp == 1) {
+    tmem_alloc<P>(&c->tmem_base, kTmemCols);
+    tmem_relinquish<P>();
   }
   if (threadIdx.x == 32 * 2) {
     prefetch_tmap(&maps.wg);
@@ -74,7 +77,7 @@ __device__ __forceinline__ void cta_setup(const Params& p, const Maps& maps, cha
   if (pair) cluster_sync();
   tc_fence_after();
   st.rank = pair ? (int)cluster_rank() : 0;
-  st.worker = pair ? (int)(blockIdx.x / kPair) : (int)blockIdx.x;
+  st.worker = (int)(blockIdx.x / P);
   st.lead_ctrl = pair ? mapa_shared(smem_u32(c), 0) : smem_u32(c);
   st.pipe_it = 0;
   st.gemm_count = 0;
@@ -94,13 +97,14 @@ __device__ __forceinline__ void cta_setup(const Params& p, const Maps& maps, cha
 // Both CTAs of a pair pass a cluster barrier before either exits or frees the
 // pair's TMEM: neither may leave while the other can still signal its
 // barriers or read its shared memory.
-__device__ __forceinline__ void cta_teardown(Ctrl* c, bool pair) {
+template <int P>
+__device__ __forceinline__ void cta_teardown(Ctrl* c, bool tmem) {
   tc_fence_before();
   __syncthreads();
-  if (pair) cluster_sync();
-  if (pair && (threadIdx.x >> 5) == 1) {
+  if (P == 2) cluster_sync();
+  if (tmem && (threadIdx.x >> 5) == 1) {
     tc_fence_after();
-    tmem_dealloc(c->tmem_base, kTmemCols);
+    tmem_dealloc<P>(c->tmem_base, kTmemCols);
   }
 }
 
@@ -131,20 +135,21 @@ __device__ __forceinline__ void trace_record(const Params& p, unsigned long long
 // Once the plan is published and until the first gate/up tiles start, HBM
 // only carries the gathers: pull the gate/up weight tiles the first GEMM wave
 // will read into L2 -- tiles (expert, f tile) in index order, the order the
-// plan keeps (Params::index_order) -- spread over the CTA pairs, up to
-// l2_pf_bytes.  One lane of each pair's leader, asynchronous.  (Issued
+// plan keeps (Params::index_order) -- spread over the workers, up to
+// l2_pf_bytes.  One lane of each worker's leader, asynchronous.  (Issued
 // earlier, while the plan runs, the prefetch traffic slows the plan's memory
 // accesses: measured 2.5 us slower on the fine and decode workloads.)
 __device__ void prefetch_first_weights(const Params& p, const CtaState& st) {
-  const size_t tile_bytes = (size_t)kFTile * p.d * 2;  // one 256-row f tile of w_gate or w_up
+  const int fr = ftile_rows(p);
+  const size_t tile_bytes = (size_t)fr * p.d * 2;  // one f tile of w_gate or w_up
   const long long n_tiles =
       min((long long)p.E * p.n_ftiles, p.l2_pf_bytes / (long long)(2 * tile_bytes));
-  const int workers = (int)gridDim.x / kPair;
+  const int workers = (int)gridDim.x / p.pair;
   constexpr uint32_t kChunk = 128u << 10;
   for (long long i = st.worker; i < n_tiles; i += workers) {
     const int e = (int)(i / p.n_ftiles), ft = (int)(i - (long long)e * p.n_ftiles);
-    const int rows = min(kFTile, p.f - ft * kFTile);
-    const size_t row0 = (size_t)e * p.f + (size_t)ft * kFTile;
+    const int rows = min(fr, p.f - ft * fr);
+    const size_t row0 = (size_t)e * p.f + (size_t)ft * fr;
     const char* g = reinterpret_cast<const char*>(p.w_gate + row0 * p.d);
     const char* u = reinterpret_cast<const char*>(p.w_up + row0 * p.d);
     const size_t bytes = (size_t)rows * p.d * 2;
@@ -156,11 +161,12 @@ __device__ void prefetch_first_weights(const Params& p, const CtaState& st) {
   }
 }
 
-// The compute warps of either CTA of a pair: take the tasks the leader's
+// The compute warps of every CTA of a worker: take the tasks the leader's
 // scheduler warp posts to this CTA's mailbox (the same tasks, in the same
-// order, in both CTAs), run this CTA's part of each, and report it finished:
-// the leader's own to its scheduler warp through its mailbox, the peer's to
-// the leader as a count of finished tasks.
+// order, in both CTAs of a pair), run this CTA's part of each, and report it
+// finished: the leader's own to its scheduler warp through its mailbox, a
+// pair's peer's to the leader as a count of finished tasks.
+template <int P>
 __device__ void compute_loop(const Params& p, const Maps& maps, char* smem, Ctrl* c,
                              CtaState& st) {
   int executed = 0, gemm_tasks = 0, mover_tasks = 0, done = 0;
@@ -196,7 +202,7 @@ __device__ void compute_loop(const Params& p, const Maps& maps, char* smem, Ctrl
     const int type = task_type(task), pl = task_payload(task);
     if (type == kTaskRoute) {
       const int pt = pl / p.route_ks, split = pl - pt * p.route_ks;
-      if (route_task(p, maps, pt, split, smem, c, st)) {
+      if (route_task<P>(p, maps, pt, split, smem, c, st)) {
         release_writes();
         if (threadIdx.x == 0) {
           const int old = atom_add_acq_rel(&p.sched->route_done, 1);
@@ -218,16 +224,16 @@ __device__ void compute_loop(const Params& p, const Maps& maps, char* smem, Ctrl
       }
     } else if (type == kTaskGather) {
       ++mover_tasks;
-      gather_task(p, pl >> 3, pl & 7, st.rank, kPair, smem, c, st);
+      gather_task(p, pl >> 3, pl & 7, st.rank, P, smem, c, st);
     } else if (type == kTaskGateUp) {
       ++gemm_tasks;
-      gateup_task(p, maps, task, smem, c, st);
+      gateup_task<P>(p, maps, task, smem, c, st);
     } else if (type == kTaskDown) {
       ++gemm_tasks;
-      down_task(p, maps, task, smem, c, st);
+      down_task<P>(p, maps, task, smem, c, st);
     } else if (type == kTaskCombine) {
       ++mover_tasks;
-      combine_task(p, pl, st.rank, kPair, smem, c, st);
+      combine_task(p, pl, st.rank, P, smem, c, st);
     } else {
       if (threadIdx.x == 0) set_status(p, MOE_E_DEVICE, 6);
       break;
@@ -267,14 +273,15 @@ __device__ void compute_loop(const Params& p, const Maps& maps, char* smem, Ctrl
   }
 }
 
-// The leader's scheduler warp (the peer's has nothing to do): claims each
-// task for the pair, posts it to both CTAs' mailboxes, and runs a finished
-// task's notifications once both CTAs have finished it.
+// The leader's scheduler warp (a pair's peer's has nothing to do): claims
+// each task for the worker, posts it to every CTA's mailbox, and runs a
+// finished task's notifications once every CTA has finished it.
+template <int P>
 __device__ void scheduler_loop(const Params& p, Ctrl* c, CtaState& st) {
   if (st.rank != 0) return;
   const int lane = threadIdx.x & 31;
   const unsigned full = 0xffffffffu;
-  const uint32_t peer = mapa_shared(smem_u32(c), 1);  // the peer's Ctrl
+  const uint32_t peer = P == 2 ? mapa_shared(smem_u32(c), 1) : 0u;  // the peer's Ctrl
   const uint32_t off_posted = (uint32_t)offsetof(Ctrl, mb_posted);
   const uint32_t off_taken = (uint32_t)offsetof(Ctrl, mb_taken);
   const uint32_t off_task = (uint32_t)offsetof(Ctrl, mb_task);
@@ -285,13 +292,13 @@ __device__ void scheduler_loop(const Params& p, Ctrl* c, CtaState& st) {
     if (lane == 0) {
       c->mb_task[posted & 1] = t;
       c->mb_tclaim[posted & 1] = globaltimer();
-      st_cluster(peer + off_task + 4u * (posted & 1), t);
+      if (P == 2) st_cluster(peer + off_task + 4u * (posted & 1), t);
     }
     ++posted;
     __syncwarp();
     if (lane == 0) {
       st_release_cta_shared(&c->mb_posted, posted);
-      st_release_cluster(peer + off_posted, posted);
+      if (P == 2) st_release_cluster(peer + off_posted, posted);
     }
   };
   while (true) {
@@ -299,8 +306,12 @@ __device__ void scheduler_loop(const Params& p, Ctrl* c, CtaState& st) {
     // notifications of the tasks both CTAs have finished
     int done = 0, taken = 0, late_seq = 0;
     if (lane == 0) {
-      done = min(ld_acquire_cta_shared(&c->mb_done), ld_acquire_cluster(smem_u32(&c->mb_done_peer)));
-      taken = min(ld_acquire_cta_shared(&c->mb_taken), ld_acquire_cluster(peer + off_taken));
+      done = ld_acquire_cta_shared(&c->mb_done);
+      taken = ld_acquire_cta_shared(&c->mb_taken);
+      if (P == 2) {
+        done = min(done, ld_acquire_cluster(smem_u32(&c->mb_done_peer)));
+        taken = min(taken, ld_acquire_cluster(peer + off_taken));
+      }
       late_seq = ld_acquire_cta_shared(&c->mb_late);
     }
     done = __shfl_sync(full, done, 0);
@@ -381,21 +392,22 @@ __device__ void scheduler_loop(const Params& p, Ctrl* c, CtaState& st) {
   }
 }
 
+template <int P>
 __global__ void __launch_bounds__(kThreads + 32, 1)
     moe_persistent_kernel(const __grid_constant__ Params p, const __grid_constant__ Maps maps) {
   char* smem;
   Ctrl* c;
   CtaState st;
-  cta_setup(p, maps, smem, c, st, true);
-  if (threadIdx.x < kThreads) compute_loop(p, maps, smem, c, st);
-  else scheduler_loop(p, c, st);
-  cta_teardown(c, true);
+  cta_setup<P>(p, maps, smem, c, st, true);
+  if (threadIdx.x < kThreads) compute_loop<P>(p, maps, smem, c, st);
+  else scheduler_loop<P>(p, c, st);
+  cta_teardown<P>(c, true);
 }
 
 // ------------------------------------------------------------------ static persistent megakernel
-// The static fused baseline: one launch, one CTA per SM (in pairs), every
-// stage's tasks assigned round-robin to the CTA pairs (task i of a stage to
-// pair i mod pairs), and a grid-wide barrier between stages -- no queue, no dependency
+// The static fused baseline: one launch, one CTA per SM, every stage's tasks
+// assigned round-robin to the workers (task i of a stage to worker i mod
+// workers), and a grid-wide barrier between stages -- no queue, no dependency
 // counters, no overlap of stages.  Same tiles as the other two modes, so its
 // gap to the persistent kernel is what the queue, the counters and the
 // cross-stage overlap buy beyond saving launches.  Launched cooperatively, so
@@ -436,17 +448,18 @@ __device__ bool grid_barrier(const Params& p, Ctrl* c, int& gen, const CtaState&
   return c->flag != 0;
 }
 
+template <int P>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_static_kernel(const __grid_constant__ Params p, const __grid_constant__ Maps maps) {
   char* smem;
   Ctrl* c;
   CtaState st;
-  cta_setup(p, maps, smem, c, st, true);
-  // tasks go round-robin to the CTA pairs; both CTAs of a pair run each one
-  const int W = (int)gridDim.x / kPair, w = st.worker;
+  cta_setup<P>(p, maps, smem, c, st, true);
+  // tasks go round-robin to the workers; every CTA of a worker runs each one
+  const int W = (int)gridDim.x / P, w = st.worker;
   int gen = 0;
   for (int i = w; i < p.n_route_tasks; i += W)
-    route_task(p, maps, i / p.route_ks, i % p.route_ks, smem, c, st);
+    route_task<P>(p, maps, i / p.route_ks, i % p.route_ks, smem, c, st);
   bool ok = grid_barrier(p, c, gen, st);
   if (ok && blockIdx.x == 0) plan_task(p, smem, c, false);
   ok = ok && grid_barrier(p, c, gen, st);
@@ -454,36 +467,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_routed = n_groups - p.n_shared_groups;
   for (int i = w; ok && i < n_routed * 8; i += W) {  // (routed group, chunk)
     const int g = p.n_shared_groups + (i >> 3), ch = i & 7;
-    if (ch * kGatherRows < load_group(p, g).nrows) gather_task(p, g, ch, st.rank, kPair, smem, c, st);
+    if (ch * gather_rows(p) < load_group(p, g).nrows) gather_task(p, g, ch, st.rank, P, smem, c, st);
   }
   ok = ok && grid_barrier(p, c, gen, st);
   for (int i = w; ok && i < n_groups * p.n_ftiles; i += W)
-    gateup_task(p, maps, task_id(kTaskGateUp, i), smem, c, st);
+    gateup_task<P>(p, maps, task_id(kTaskGateUp, i), smem, c, st);
   ok = ok && grid_barrier(p, c, gen, st);
   const int n_down = p.n_dtiles * p.ks;
   for (int i = w; ok && i < n_groups * n_down; i += W)
-    down_task(p, maps, task_id(kTaskDown, i), smem, c, st);
+    down_task<P>(p, maps, task_id(kTaskDown, i), smem, c, st);
   ok = ok && grid_barrier(p, c, gen, st);
   for (int i = w; ok && i < p.n_comb; i += W) {
-    combine_task(p, i, st.rank, kPair, smem, c, st);
+    combine_task(p, i, st.rank, P, smem, c, st);
     cta_sync();
   }
-  cta_teardown(c, true);
+  cta_teardown<P>(c, true);
 }
 
 // ------------------------------------------------------------------ ablation: one kernel per stage
-// The tensor-core stages (router, gate/up, down) launch one cluster of two
-// CTAs per task; the others one CTA per task.
+// The tensor-core stages (router, gate/up, down) launch one worker (a CTA,
+// or a cluster of two) per task; the others one CTA per task.
 
+template <int P>
 __global__ void __launch_bounds__(kThreads, 1)
     k_route(const __grid_constant__ Params p, const __grid_constant__ Maps maps) {
   char* smem;
   Ctrl* c;
   CtaState st;
-  cta_setup(p, maps, smem, c, st, true);
-  const int i = (int)blockIdx.x / kPair;
-  route_task(p, maps, i / p.route_ks, i % p.route_ks, smem, c, st);
-  cta_teardown(c, true);
+  cta_setup<P>(p, maps, smem, c, st, true);
+  const int i = (int)blockIdx.x / P;
+  route_task<P>(p, maps, i / p.route_ks, i % p.route_ks, smem, c, st);
+  cta_teardown<P>(c, true);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -491,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   char* smem;
   Ctrl* c;
   CtaState st;
-  cta_setup(p, maps, smem, c, st, false);
+  cta_setup<1>(p, maps, smem, c, st, false);
   plan_task(p, smem, c, false);
 }
 
@@ -500,39 +514,41 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int g = p.n_shared_groups + (int)(blockIdx.x >> 3), ch = blockIdx.x & 7;
   if (g >= p.sched->n_groups) return;
   const Group G = load_group(p, g);
-  if (ch * kGatherRows >= G.nrows) return;
+  if (ch * gather_rows(p) >= G.nrows) return;
   char* smem;
   Ctrl* c;
   CtaState st;
-  cta_setup(p, maps, smem, c, st, false);
+  cta_setup<1>(p, maps, smem, c, st, false);
   gather_task(p, g, ch, 0, 1, smem, c, st);
 }
 
+template <int P>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gateup(const __grid_constant__ Params p, const __grid_constant__ Maps maps) {
-  const int i = (int)blockIdx.x / kPair;  // the same for both CTAs of the cluster
+  const int i = (int)blockIdx.x / P;  // the same for both CTAs of a cluster
   const int g = i / p.n_ftiles;
   if (g >= p.sched->n_groups) return;
   char* smem;
   Ctrl* c;
   CtaState st;
-  cta_setup(p, maps, smem, c, st, true);
-  gateup_task(p, maps, task_id(kTaskGateUp, i), smem, c, st);
-  cta_teardown(c, true);
+  cta_setup<P>(p, maps, smem, c, st, true);
+  gateup_task<P>(p, maps, task_id(kTaskGateUp, i), smem, c, st);
+  cta_teardown<P>(c, true);
 }
 
+template <int P>
 __global__ void __launch_bounds__(kThreads, 1)
     k_down(const __grid_constant__ Params p, const __grid_constant__ Maps maps) {
   const int n_down = p.n_dtiles * p.ks;
-  const int i = (int)blockIdx.x / kPair;  // the same for both CTAs of the cluster
+  const int i = (int)blockIdx.x / P;  // the same for both CTAs of a cluster
   const int g = i / n_down;
   if (g >= p.sched->n_groups) return;
   char* smem;
   Ctrl* c;
   CtaState st;
-  cta_setup(p, maps, smem, c, st, true);
-  down_task(p, maps, task_id(kTaskDown, i), smem, c, st);
-  cta_teardown(c, true);
+  cta_setup<P>(p, maps, smem, c, st, true);
+  down_task<P>(p, maps, task_id(kTaskDown, i), smem, c, st);
+  cta_teardown<P>(c, true);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -540,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   char* smem;
   Ctrl* c;
   CtaState st;
-  cta_setup(p, maps, smem, c, st, false);
+  cta_setup<1>(p, maps, smem, c, st, false);
   combine_task(p, blockIdx.x, 0, 1, smem, c, st);
 }
 
@@ -632,6 +648,7 @@ struct moe_layer {
   int num_sms = 0;
   int max_pairs = 0;  // clusters of two CTAs the persistent kernel can keep resident
   // options
+  int pair_opt = 0;  // CTAs per worker: 0 = automatic, 1, 2
   int mode = MOE_MODE_PERSISTENT;
   unsigned long long timeout_ns = 2000000000ull;
   int mover_override = 0;
@@ -673,6 +690,7 @@ struct moe_layer {
   int last_bn = 0, last_ks = 0, last_bands = 0;  // tiling of the last forward
   int last_ybytes = 0;  // bytes the combine reads per expert-output value
   int last_ct = 0;      // tokens per combine tile
+  int last_pair = 0;    // CTAs per worker
   int last_T = 0;
 };
 
@@ -737,11 +755,26 @@ void layout(moe_layer* h, const Bounds& b) {
 
 // Tiling of one forward pass.
 struct Tiling {
-  int bn, stages, stage_bytes, smem, ks, rt, ct, y_f32;
+  int pair, bn, stages, stage_bytes, smem, ks, rt, ct, y_f32;
 };
+
+// CTAs per worker: a CTA pair sharing each GEMM tile (.cta_group::2) when the
+// experts' row groups are large -- a pair stages half the token rows per SM
+// and halves the shared-memory operand traffic of a 256-token tile -- and one
+// CTA when they are small, where the pair's cross-SM handshakes and the
+// halved number of independent mover workers cost more than they save
+// (same-box measurements: decode and fine layers faster with one CTA, the
+// prefill layers with pairs).
+int choose_pair(const moe_layer* h, int T) {
+  if (h->pair_opt == 1 || h->pair_opt == 2) return h->pair_opt;
+  const long long rows_per_expert = (long long)T * h->k / h->E;
+  return rows_per_expert >= kPairMinRows ? 2 : 1;
+}
 
 int choose_tiling(const moe_layer* h, int T, bool whole_rows, Tiling* t) {
   const long long Tk = (long long)T * h->k;
+  const int P = choose_pair(h, T);
+  t->pair = P;
   int bn = h->bn_opt;
   if (bn <= 0) {
     // at least 160 tokens (or twice the mean expert load): the MMA's N is the
@@ -756,12 +789,13 @@ int choose_tiling(const moe_layer* h, int T, bool whole_rows, Tiling* t) {
   }
   bn = std::max(32, std::min(256, ((bn + 31) / 32) * 32));
   t->bn = bn;
-  // a stage holds this CTA's 128 rows of each weight operand and half of the
-  // tile's token rows (the pair's other CTA holds the other half)
-  t->stage_bytes = 2 * kABoxBytes + cdiv(bn / kPair, kBBoxRows) * kBBoxBytes;
-  // the router's tile keeps x (16 KB) then half of Wr's E rows (padded to 32)
+  // a stage holds this CTA's 128 rows of each weight operand and its share of
+  // the tile's token rows (all of them, or half for a CTA pair)
+  t->stage_bytes = 2 * kABoxBytes + cdiv(bn / P, kBBoxRows) * kBBoxBytes;
+  // the router's tile keeps x (16 KB) then this CTA's share of Wr's E rows
+  const int e_mma = ((h->E + 16 * P - 1) / (16 * P)) * (16 * P);
   t->stage_bytes =
-      std::max(t->stage_bytes, kABoxBytes + cdiv(((h->E + 31) / 32) * 16, kBBoxRows) * kBBoxBytes);
+      std::max(t->stage_bytes, kABoxBytes + cdiv(e_mma / P, kBBoxRows) * kBBoxBytes);
   const int ctrl = (int)align_up(sizeof(Ctrl), 1024);
   t->stages = std::min(8, (kSmemBudget - 1024 - ctrl) / t->stage_bytes);
   if (t->stages < 2) return fail(MOE_E_INVAL, "tile too large for shared memory");
@@ -774,11 +808,13 @@ int choose_tiling(const moe_layer* h, int T, bool whole_rows, Tiling* t) {
   int ks = h->split_k;
   if (ks <= 0) {
     // the smallest split that gives about 1.5 waves of down tasks over the
-    // CTA pairs, counting one row group per expert that can be touched
+    // workers, counting one row group per expert that can be touched
+    // (decode, one CTA per worker: 2 -- 518 us against 521 us at 4 and 529 us
+    // at 1)
     const long long groups = std::min<long long>(h->E, Tk) + h->S;
-    const long long want = 3ll * std::max(h->num_sms / kPair, 1) / 2;
+    const long long want = 3ll * std::max(h->num_sms / P, 1) / 2;
     ks = 1;
-    while (ks < 4 && groups * cdiv(h->d, kDTile) * ks < want) ks <<= 1;
+    while (ks < 4 && groups * cdiv(h->d, 2 * kBM * P) * ks < want) ks <<= 1;
   }
   while (ks > 1 && (kblocks % ks != 0 || (size_t)rows * h->d * ks > h->B.y_elems)) ks >>= 1;
   if (ks < 1) ks = 1;
@@ -791,11 +827,11 @@ int choose_tiling(const moe_layer* h, int T, bool whole_rows, Tiling* t) {
   const bool small_rt = T <= kSmallRouteT && h->E >= kSmallRouteMinE;
   t->rt = h->rt_opt ? h->rt_opt : (small_rt ? kRouteTokensSmall : kRouteTokens);
   if (cdiv(T, t->rt) > kMaxE) return fail(MOE_E_INVAL, "too many router tiles: use 128-token tiles");
-  // combine tile, <= 256 (token, slot) pairs: one per CTA pair when the
+  // combine tile, <= 256 (token, slot) pairs: one per worker when the
   // combine is split in two d bands (each task then covers part of a row),
-  // two per pair with one band; the pair's CTAs split a tile's tokens
-  const bool two_bands = h->bands && cdiv(h->d, kDTile) >= 2 && !whole_rows;
-  int ct = cdiv(T, (two_bands ? 1 : 2) * std::max(h->num_sms / kPair, 1));
+  // two per worker with one band; a pair's CTAs split a tile's tokens
+  const bool two_bands = h->bands && cdiv(h->d, 2 * kBM * P) >= 2 && !whole_rows;
+  int ct = cdiv(T, (two_bands ? 1 : 2) * std::max(h->num_sms / P, 1));
   ct = std::max(1, std::min(ct, kThreads / h->k));
   t->ct = ct;
   return MOE_OK;
@@ -815,8 +851,24 @@ int set_error_from_sched(const Sched& s) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-// Launch one of the kernels: `pair` as clusters of two CTAs (the kernels with
-// tensor-core tasks), `coop` cooperatively.
+// The dynamic shared-memory limit of every kernel (both widths of worker).
+cudaError_t set_kernel_smem(int bytes) {
+  void (*kernels[])(Params, Maps) = {moe_persistent_kernel<1>, moe_persistent_kernel<2>,
+                                     moe_static_kernel<1>,     moe_static_kernel<2>,
+                                     k_route<1>,               k_route<2>,
+                                     k_gateup<1>,              k_gateup<2>,
+                                     k_down<1>,                k_down<2>,
+                                     k_plan,                   k_gather,
+                                     k_combine};
+  for (auto k : kernels) {
+    cudaError_t e = cudaFuncSetAttribute((const void*)k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+// Launch one of the kernels: `pair` as clusters of two CTAs (the tensor-core
+// kernels built for CTA pairs), `coop` cooperatively.
 cudaError_t launch_kernel(void (*kern)(Params, Maps), int grid, int threads, int smem,
                           cudaStream_t s, bool pair, bool coop, const Params& p, const Maps& m) {
   cudaLaunchConfig_t cfg = {};
@@ -828,7 +880,7 @@ cudaError_t launch_kernel(void (*kern)(Params, Maps), int grid, int threads, int
   int n = 0;
   if (pair) {
     at[n].id = cudaLaunchAttributeClusterDimension;
-    at[n].val.clusterDim.x = kPair;
+    at[n].val.clusterDim.x = 2;
     at[n].val.clusterDim.y = 1;
     at[n].val.clusterDim.z = 1;
     ++n;
@@ -847,18 +899,18 @@ cudaError_t launch_kernel(void (*kern)(Params, Maps), int grid, int threads, int
 // memory size) the device keeps resident at once; 0 if the query fails.
 int query_max_pairs(int num_sms) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)std::max(kPair, num_sms / kPair * kPair));
+  cfg.gridDim = dim3((unsigned)std::max(2, num_sms / 2 * 2));
   cfg.blockDim = dim3(kThreads + 32);
   cfg.dynamicSmemBytes = kSmemBudget;
   cudaLaunchAttribute at;
   at.id = cudaLaunchAttributeClusterDimension;
-  at.val.clusterDim.x = kPair;
+  at.val.clusterDim.x = 2;
   at.val.clusterDim.y = 1;
   at.val.clusterDim.z = 1;
   cfg.attrs = &at;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, (const void*)moe_persistent_kernel, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, (const void*)moe_persistent_kernel<2>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -950,16 +1002,7 @@ int moe_layer_reserve(moe_layer_t* h, int T_max, void* stream) {
     h->x_dev_stage = h->out_dev_stage = nullptr;
   }
   h->T_max = T_max;
-  const int kernels_smem = kSmemBudget;
-  CK(cudaFuncSetAttribute(moe_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                          kernels_smem));
-  CK(cudaFuncSetAttribute(moe_static_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kernels_smem));
-  CK(cudaFuncSetAttribute(k_route, cudaFuncAttributeMaxDynamicSharedMemorySize, kernels_smem));
-  CK(cudaFuncSetAttribute(k_plan, cudaFuncAttributeMaxDynamicSharedMemorySize, kernels_smem));
-  CK(cudaFuncSetAttribute(k_gather, cudaFuncAttributeMaxDynamicSharedMemorySize, kernels_smem));
-  CK(cudaFuncSetAttribute(k_gateup, cudaFuncAttributeMaxDynamicSharedMemorySize, kernels_smem));
-  CK(cudaFuncSetAttribute(k_down, cudaFuncAttributeMaxDynamicSharedMemorySize, kernels_smem));
-  CK(cudaFuncSetAttribute(k_combine, cudaFuncAttributeMaxDynamicSharedMemorySize, kernels_smem));
+  CK(set_kernel_smem(kSmemBudget));
   h->max_pairs = query_max_pairs(h->num_sms);
   g_err.clear();
   return MOE_OK;
@@ -1043,6 +1086,10 @@ int moe_layer_set_option(moe_layer_t* h, int key, long long v) {
       if (v < 0 || v > kMaxRouteKs) return fail(MOE_E_INVAL, "router K splits must be 0..8");
       h->route_splits = (int)v;
       break;
+    case MOE_OPT_PAIR:
+      if (v != 0 && v != 1 && v != 2) return fail(MOE_E_INVAL, "CTAs per worker must be 0 (auto), 1 or 2");
+      h->pair_opt = (int)v;
+      break;
     case MOE_OPT_ROUTE_TOKENS:
       if (v != 0 && v != kRouteTokens && v != kRouteTokensSmall)
         return fail(MOE_E_INVAL, "router tiles are 64 or 128 tokens (0: automatic)");
@@ -1091,8 +1138,10 @@ int forward_impl(moe_layer_t* h, int T, const void* x, const void* router_w, con
   p.bn_max = tl.bn;
   p.stages = tl.stages;
   p.stage_bytes = tl.stage_bytes;
-  p.n_ftiles = cdiv(h->f, kFTile);
-  p.n_dtiles = cdiv(h->d, kDTile);
+  const int P = tl.pair;
+  p.pair = P;
+  p.n_ftiles = cdiv(h->f, kBM * P);
+  p.n_dtiles = cdiv(h->d, 2 * kBM * P);
   p.ks = tl.ks;
   p.kb_down = (h->f / kBK) / tl.ks;
   p.rt = tl.rt;
@@ -1108,7 +1157,7 @@ int forward_impl(moe_layer_t* h, int T, const void* x, const void* router_w, con
     int ks = std::min(kMaxRouteKs, std::min(std::max(1, nkb / 8), cap));
     if (h->route_splits > 0) ks = std::min(std::min(h->route_splits, nkb), cap);
     p.route_ks = std::max(1, ks);
-    p.n_route_tasks = cdiv(p.n_route, kPair) * p.route_ks;
+    p.n_route_tasks = cdiv(p.n_route, P) * p.route_ks;
   }
   p.release = h->release;
   p.prefetch = h->prefetch;
@@ -1134,10 +1183,10 @@ int forward_impl(moe_layer_t* h, int T, const void* x, const void* router_w, con
   p.trace = h->trace;
   p.trace_cap = h->trace_cap;
   p.timeout_ns = h->timeout_ns;
-  // cost-model constants per worker (a CTA pair): 2 x 40 GB/s of bulk copies,
-  // two SMs' share of 1925 TF/s
-  p.beta_move = 80e9f;
-  p.phi_gemm = 1925e12f / 76.f;
+  // cost-model constants per worker (P CTAs): 40 GB/s of bulk copies and one
+  // SM's share of 1925 TF/s, per CTA
+  p.beta_move = 40e9f * (float)P;
+  p.phi_gemm = (1925e12f / 152.f) * (float)P;
   p.hbm_bw = 6.79e12f;
   p.x = static_cast<const __nv_bfloat16*>(x);
   p.wr = static_cast<const __nv_bfloat16*>(router_w);
@@ -1204,34 +1253,45 @@ int forward_impl(moe_layer_t* h, int T, const void* x, const void* router_w, con
 
   // scheduler counters and task rings are contiguous: one memset resets them
   CK(cudaMemsetAsync(w + h->o_zero, 0, h->o_ring_end - h->o_zero, s));
-  const int sms_pairs = std::max(1, h->num_sms / kPair);
-  const int cap_pairs = h->max_pairs > 0 ? std::min(h->max_pairs, sms_pairs) : sms_pairs;
-  const int pairs = h->grid_override > 0 ? std::max(1, std::min(h->grid_override / kPair, cap_pairs))
-                                         : cap_pairs;
-  p.n_workers = pairs;
+  // workers: every SM (one CTA each), or every SM pair the device keeps
+  // resident as a cluster
+  const int max_workers = P == 2 ? (h->max_pairs > 0 ? std::min(h->max_pairs, h->num_sms / 2)
+                                                     : h->num_sms / 2)
+                                 : h->num_sms;
+  const int workers = std::max(1, h->grid_override > 0
+                                      ? std::min(h->grid_override / P, std::max(max_workers, 1))
+                                      : max_workers);
+  p.n_workers = workers;
+  const bool cl = P == 2;
+  auto K = [&](void (*k1)(Params, Maps), void (*k2)(Params, Maps)) { return P == 2 ? k2 : k1; };
   if (h->mode == MOE_MODE_PERSISTENT) {
-    h->last_grid = pairs * kPair;
-    p.ahead_depth = h->ahead_opt < 0 ? pairs : h->ahead_opt;
-    CK(launch_kernel(moe_persistent_kernel, pairs * kPair, kThreads + 32, tl.smem, s, true, false, p, m));
+    h->last_grid = workers * P;
+    p.ahead_depth = h->ahead_opt < 0 ? workers : h->ahead_opt;
+    CK(launch_kernel(K(moe_persistent_kernel<1>, moe_persistent_kernel<2>), workers * P,
+                     kThreads + 32, tl.smem, s, cl, false, p, m));
   } else if (h->mode == MOE_MODE_STATIC) {
-    h->last_grid = pairs * kPair;
+    h->last_grid = workers * P;
     // cooperative, so that every CTA is resident for the grid barrier; where a
     // cooperative cluster launch is refused, a plain one (the grid is within
     // the resident-cluster count, and every barrier wait is bounded)
-    cudaError_t e = launch_kernel(moe_static_kernel, pairs * kPair, kThreads, tl.smem, s, true, true, p, m);
-    if (e != cudaSuccess) {
+    auto kern = K(moe_static_kernel<1>, moe_static_kernel<2>);
+    cudaError_t e = launch_kernel(kern, workers * P, kThreads, tl.smem, s, cl, true, p, m);
+    if (e != cudaSuccess && cl) {
       cudaGetLastError();
-      CK(launch_kernel(moe_static_kernel, pairs * kPair, kThreads, tl.smem, s, true, false, p, m));
+      e = launch_kernel(kern, workers * P, kThreads, tl.smem, s, cl, false, p, m);
     }
+    CK(e);
   } else {
     h->last_grid = 0;
-    CK(launch_kernel(k_route, p.n_route_tasks * kPair, kThreads, tl.smem, s, true, false, p, m));
+    CK(launch_kernel(K(k_route<1>, k_route<2>), p.n_route_tasks * P, kThreads, tl.smem, s, cl,
+                     false, p, m));
     CK(launch_kernel(k_plan, 1, kThreads, tl.smem, s, false, false, p, m));
     const int routed_max = p.max_groups - p.n_shared_groups;
     CK(launch_kernel(k_gather, routed_max * 8, kThreads, tl.smem, s, false, false, p, m));
-    CK(launch_kernel(k_gateup, p.max_groups * p.n_ftiles * kPair, kThreads, tl.smem, s, true, false, p, m));
-    CK(launch_kernel(k_down, p.max_groups * p.n_dtiles * p.ks * kPair, kThreads, tl.smem, s, true,
-                     false, p, m));
+    CK(launch_kernel(K(k_gateup<1>, k_gateup<2>), p.max_groups * p.n_ftiles * P, kThreads,
+                     tl.smem, s, cl, false, p, m));
+    CK(launch_kernel(K(k_down<1>, k_down<2>), p.max_groups * p.n_dtiles * p.ks * P, kThreads,
+                     tl.smem, s, cl, false, p, m));
     CK(launch_kernel(k_combine, p.n_comb, kThreads, tl.smem, s, false, false, p, m));
   }
   h->view.ws = h->ws;
@@ -1249,6 +1309,7 @@ int forward_impl(moe_layer_t* h, int T, const void* x, const void* router_w, con
   h->last_bands = p.n_bands;
   h->last_ybytes = p.y_f32 ? 4 * p.ks : 2;
   h->last_ct = p.ct;
+  h->last_pair = p.pair;
   return MOE_OK;
 }
 
@@ -1417,6 +1478,7 @@ long long moe_layer_get_stat(moe_layer_t* h, int key) {
   if (key == MOE_STAT_BANDS) return h->last_T ? h->last_bands : -1;
   if (key == MOE_STAT_Y_BYTES) return h->last_T ? h->last_ybytes : -1;
   if (key == MOE_STAT_COMBINE_TOKENS) return h->last_T ? h->last_ct : -1;
+  if (key == MOE_STAT_PAIR) return h->last_T ? h->last_pair : -1;
   if (!h->last_valid) return -1;
   switch (key) {
     case MOE_STAT_MOVER_CTAS: return h->last.n_movers;
@@ -1502,14 +1564,7 @@ int moe_layer_forward_noalloc(moe_layer_t* h, int T, const void* x, const void* 
         return fail(MOE_E_INVAL, "this library is built for sm_103a (GB300) only");
       if (!encode_fn()) return fail(MOE_E_CUDA, "cuTensorMapEncodeTiled is not available");
       CK(cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev));
-      CK(cudaFuncSetAttribute(moe_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget));
-      CK(cudaFuncSetAttribute(moe_static_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget));
-      CK(cudaFuncSetAttribute(k_route, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget));
-      CK(cudaFuncSetAttribute(k_plan, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget));
-      CK(cudaFuncSetAttribute(k_gather, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget));
-      CK(cudaFuncSetAttribute(k_gateup, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget));
-      CK(cudaFuncSetAttribute(k_down, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget));
-      CK(cudaFuncSetAttribute(k_combine, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget));
+      CK(set_kernel_smem(kSmemBudget));
       s.max_pairs = query_max_pairs(s.num_sms);
       s.scratch = scratch_now;
       s.done = true;
@@ -1553,6 +1608,7 @@ int moe_layer_forward_noalloc(moe_layer_t* h, int T, const void* x, const void* 
     h->last_bands = tmp.last_bands;
     h->last_ybytes = tmp.last_ybytes;
     h->last_ct = tmp.last_ct;
+    h->last_pair = tmp.last_pair;
   }
   return rc;
 }

@@ -135,8 +135,8 @@ __device__ __forceinline__ int atom_cas_acq_rel(int* p, int cmp, int v) {
 }
 
 // ---------------------------------------------------------------- clusters
-// Every tensor-core kernel here runs as clusters of two CTAs on a pair of
-// SMs (tcgen05 .cta_group::2): cluster rank 0 is the pair's leader.
+// The tensor-core kernels built for CTA pairs run as clusters of two CTAs on
+// a pair of SMs (tcgen05 .cta_group::2): cluster rank 0 is the pair's leader.
 
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
@@ -201,24 +201,42 @@ __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorM
       : "memory");
 }
 
-// ---------------------------------------------------------------- tcgen05 (CTA pairs)
+// ---------------------------------------------------------------- tcgen05
+// P = CTAs that share one MMA: 1 (.cta_group::1, a CTA alone) or 2
+// (.cta_group::2, a cluster's CTA pair).  One kernel uses one P throughout.
 
-// Allocate `ncols` TMEM columns in both CTAs of the pair (power of two >= 32).
-// One warp of EACH CTA executes it; the address is written to `dst` in each.
+// Allocate `ncols` TMEM columns (power of two >= 32); one warp of each CTA
+// (of both CTAs for P = 2); the address is written to `dst` in each.
+template <int P>
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                   smem_u32(dst)),
-               "r"(ncols)
-               : "memory");
+  if constexpr (P == 2)
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst)),
+                 "r"(ncols)
+                 : "memory");
+  else
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst)),
+                 "r"(ncols)
+                 : "memory");
 }
 
+template <int P>
 __device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  if constexpr (P == 2)
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  else
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
 }
 
+template <int P>
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
+  if constexpr (P == 2)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+  else
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -229,29 +247,46 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T over the CTA pair, kind::f16 (bf16 inputs,
-// fp32 accumulate), issued by the leader: M = 256 rows of A, 128 in each CTA's
-// shared memory at the descriptor's address; the N rows of B (K-major), the
-// first N/2 in the leader's shared memory and the rest in the peer's; each
-// CTA's TMEM receives its 128 rows of D for all N columns.
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (bf16 inputs, fp32 accumulate),
+// issued by one thread (of the pair's leader for P = 2).  P = 1: M = 128 rows
+// of A, the N rows of B (K-major), D in this CTA's TMEM.  P = 2: M = 256 rows
+// of A, 128 in each CTA's shared memory at the descriptor's address; the N
+// rows of B, the first N/2 in the leader's shared memory and the rest in the
+// peer's; each CTA's TMEM receives its 128 rows of D for all N columns.
+template <int P>
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                          uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
+  if constexpr (P == 2)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
 }
 
-// Arrive once on the mbarrier at CTA-local address `bar` in both CTAs of the
-// pair when every MMA this thread issued before is done.
-__device__ __forceinline__ void mma_commit_both(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
-      "[%0], %1;" ::"r"(smem_u32(bar)),
-      "h"((uint16_t)3)
-      : "memory");
+// Arrive once on the mbarrier at CTA-local address `bar` -- in both CTAs of
+// the pair for P = 2 -- when every MMA this thread issued before is done.
+template <int P>
+__device__ __forceinline__ void mma_commit_all(uint64_t* bar) {
+  if constexpr (P == 2)
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+        "[%0], %1;" ::"r"(smem_u32(bar)),
+        "h"((uint16_t)3)
+        : "memory");
+  else
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
 }
 
 // Load 16 consecutive fp32 columns of this warp's 32 TMEM lanes (one lane per

@@ -51,9 +51,9 @@ struct Ctrl {
 
 // Per-thread state that lives across tasks.
 struct CtaState {
-  int rank;             // cluster rank: 0 = the pair's leader (issues the MMAs), 1 = its peer
-  int worker;           // pair index (blockIdx.x / kPair)
-  uint32_t lead_ctrl;   // the leader's Ctrl in the cluster's shared window
+  int rank;             // cluster rank: 0 = the worker's leader (issues the MMAs), 1 = a pair's peer
+  int worker;           // worker index (blockIdx.x / CTAs per worker)
+  uint32_t lead_ctrl;   // the leader's Ctrl in the cluster's shared window (own for one CTA)
   uint32_t pipe_it;     // k blocks issued / consumed so far (producer & MMA thread)
   uint32_t gemm_count;  // GEMM tasks done (all threads)
   uint64_t deadline;    // globaltimer value after which waits give up
@@ -438,8 +438,16 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* total, Ctrl* c) 
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+// Rows of a gate/up task's f tile, a down task's d tile and a gather task,
+// over the worker's CTAs.
+__device__ __forceinline__ int ftile_rows(const Params& p) { return kBM * p.pair; }
+__device__ __forceinline__ int dtile_rows(const Params& p) { return 2 * kBM * p.pair; }
+__device__ __forceinline__ int gather_rows(const Params& p) { return kGatherRowsCta * p.pair; }
+
 // Number of gather tasks of a group.
-__device__ __forceinline__ int gather_chunks(int nrows) { return ceil_div(nrows, kGatherRows); }
+__device__ __forceinline__ int gather_chunks(const Params& p, int nrows) {
+  return ceil_div(nrows, gather_rows(p));
+}
 
 // The plan: runs once, on the CTA that finished the last router tile (or as
 // its own kernel in the ablation).  Counts and offsets per expert, the
@@ -521,7 +529,7 @@ __device__ void plan_task(const Params& p, char* scratch, Ctrl* c, bool push) {
   // gather-task prefix in group order
   int rows_per = nmt > 0 ? ((ceil_div(n_r, nmt) + 15) / 16) * 16 : 0;
   int my_chunks = 0;
-  for (int m = 0; m < nmt; ++m) my_chunks += gather_chunks(min(rows_per, n_r - m * rows_per));
+  for (int m = 0; m < nmt; ++m) my_chunks += gather_chunks(p, min(rows_per, n_r - m * rows_per));
   int n_gather = 0;
   const int chunk_base = block_exclusive_scan(my_chunks, &n_gather, c);
   const int off_e = tid < E ? offs[e_r] : 0;
@@ -543,7 +551,7 @@ __device__ void plan_task(const Params& p, char* scratch, Ctrl* c, bool push) {
     if (tid < E) {
       c->pl_cb[tid] = chunk_base;
       c->pl_sib[tid] = sib0;
-      c->pl_cpg[tid] = rows_per > 0 ? gather_chunks(rows_per) : 1;
+      c->pl_cpg[tid] = rows_per > 0 ? gather_chunks(p, rows_per) : 1;
     }
     cta_sync();
     for (int i = tid; i < n_gather; i += kThreads) {
@@ -613,22 +621,24 @@ __device__ void plan_task(const Params& p, char* scratch, Ctrl* c, bool push) {
 }
 
 // ------------------------------------------------------------------ gather (mover)
-// Xp[row, :] = x[perm[row], :] for up to 64 rows of one group, of which this
-// CTA takes part `half` of `nhalf` (the two CTAs of a pair split the rows).
+// Xp[row, :] = x[perm[row], :] for up to 32 rows per CTA of the worker of one
+// group, of which this CTA takes part `half` of `nhalf` (the CTAs of a pair
+// split the rows).
 // One thread moves whole rows with bulk copies through shared memory (global
 // -> shared on an mbarrier, then shared -> global), as many rows per round as
 // the pipeline stages hold, so hundreds of KB are in flight per SM.
 __device__ void gather_task(const Params& p, int g, int chunk, int half, int nhalf, char* smem,
                             Ctrl* c, CtaState& st) {
   const Group G = load_group(p, g);
-  if (!group_ok(p, G) || chunk * kGatherRows >= G.nrows) {
+  const int grows = gather_rows(p);
+  if (!group_ok(p, G) || chunk * grows >= G.nrows) {
     if (threadIdx.x == 0) set_status(p, MOE_E_DEVICE, 20);
     return;
   }
-  const int nr_chunk = min(kGatherRows, G.nrows - chunk * kGatherRows);
+  const int nr_chunk = min(grows, G.nrows - chunk * grows);
   const int per = ceil_div(nr_chunk, nhalf);
   const int row_lo = min(nr_chunk, half * per);
-  const int r0 = G.row0 + chunk * kGatherRows + row_lo;
+  const int r0 = G.row0 + chunk * grows + row_lo;
   const int nr = min(nr_chunk, row_lo + per) - row_lo;
   // Permuted row r of expert e is the (r - off_e)-th token of e in router-tile
   // order: the tile tau with base[tau][e] <= r - off_e < base[tau+1][e], and
@@ -753,8 +763,8 @@ __device__ void combine_direct(const Params& p, int t0, int nt, int c0, int nvec
 __device__ void combine_band(const Params& p, int ci, int part, int nparts, char* smem, Ctrl* c,
                              CtaState& st) {
   const int ctile = ci / p.n_bands, band = ci - ctile * p.n_bands;
-  const int c0 = band_dt0(p, band) * kDTile;
-  const int c1 = min(p.d, band_dt1(p, band) * kDTile);
+  const int c0 = band_dt0(p, band) * dtile_rows(p);
+  const int c1 = min(p.d, band_dt1(p, band) * dtile_rows(p));
   const int tt0 = ctile * p.ct;
   const int nt_tile = min(p.ct, p.T - tt0);
   const int per = ceil_div(nt_tile, nparts);
@@ -920,22 +930,24 @@ __device__ void combine_task(const Params& p, int ci, int half, int nhalf, char*
   norm_tile(p, ctile);
 }
 
-// ------------------------------------------------------------------ GEMM tile (tcgen05, CTA pair)
-// Swap-AB tile on a pair of SMs: the weights are the MMA's M = 256 operand
-// (128 rows in each CTA's shared memory), the tokens its N operand (the first
-// N/2 rows in the leader's shared memory, the rest in the peer's), so a
-// handful of tokens still fills the tensor core's M dimension and each CTA
-// stages only half of the token rows.
-//   gate/up (g, ft):  acc0 = Wg[e][ft*256 .. +256, :] * B^T,  acc1 = Wu[...] * B^T
-//   down (g, dt, s):  acc0 = Wd[e][dt*512 .. +256, Ks] * H^T, acc1 = rows +256 .. +512
+// ------------------------------------------------------------------ GEMM tile (tcgen05)
+// Swap-AB tile: the weights are the MMA's M operand, the tokens its N
+// operand, so a handful of tokens still fills the tensor core's M dimension.
+// A worker is one CTA (P = 1: M = 128) or a CTA pair on two SMs (P = 2,
+// .cta_group::2: M = 256, 128 weight rows in each CTA's shared memory, and
+// the first N/2 token rows in the leader's shared memory, the rest in the
+// peer's, so each CTA stages only half of the token rows).  With
+// m = 128 P rows per accumulator:
+//   gate/up (g, ft):  acc0 = Wg[e][ft*m .. +m, :] * B^T,  acc1 = Wu[...] * B^T
+//   down (g, dt, s):  acc0 = Wd[e][dt*2m .. +m, Ks] * H^T, acc1 = rows +m .. +2m
 // CTA r holds rows 128 r .. 128 r + 127 of each accumulator (its TMEM lanes)
 // for all N tokens.  B = the group's rows of Xp (or x for the shared
 // expert) / of H, K-major.
-// Pipeline: in each CTA warp 0 lane 0 issues the TMA loads of its halves into
+// Pipeline: in each CTA warp 0 lane 0 issues the TMA loads of its part into
 // a ring of `stages` stages and signals the leader's full barrier; the
-// leader's warp 1 lane 0 issues tcgen05.mma.cta_group::2 into both CTAs' TMEM
-// and commits each stage to both CTAs' empty barriers; all 8 warps of each CTA
-// run the epilogue from their own TMEM.
+// leader's warp 1 lane 0 issues tcgen05.mma into the worker's TMEM and commits
+// each stage to every CTA's empty barrier; all 8 warps of each CTA run the
+// epilogue from their own TMEM.
 
 struct GemmJob {
   const CUtensorMap* a0;
@@ -943,8 +955,8 @@ struct GemmJob {
   const CUtensorMap* b;
   int a_row0, a1_row0;    // this CTA's first A rows of the two accumulators
   int b_row0;             // this CTA's first B row
-  int b_rows;             // B rows this CTA loads (n_mma / 2, in boxes of 32 rows)
-  int n_mma;              // MMA N over the pair (multiple of 32, <= 256)
+  int b_rows;             // B rows this CTA loads (n_mma / P, in boxes of 32 rows)
+  int n_mma;              // MMA N (multiple of 16 P, <= 256)
   int b_off;              // byte offset of the B tile inside a stage (1024-aligned)
   int kb0, nkb;           // first k block and number of k blocks
   bool a_stream;          // A is read by this task only (L2 evict-first); else kept (evict-last)
@@ -962,10 +974,12 @@ __device__ __forceinline__ int mailbox_posted(Ctrl* c, const CtaState& st) {
                       : ld_acquire_cluster(smem_u32(&c->mb_posted));
 }
 
-// Producer: TMA loads of this CTA's halves of k blocks [kb_from, kb_to) of
-// `job` into the stages starting at pipeline index it0.  Both CTAs load the
-// same number of bytes per stage; the leader's full barrier expects the
-// pair's total.  Returns the number of k blocks issued (fewer on a timeout).
+// Producer: TMA loads of this CTA's part of k blocks [kb_from, kb_to) of
+// `job` into the stages starting at pipeline index it0.  The CTAs of a pair
+// load the same number of bytes per stage; the leader's full barrier expects
+// the pair's total.  Returns the number of k blocks issued (fewer on a
+// timeout).
+template <int P>
 __device__ int issue_loads(const Params& p, const GemmJob& job, char* smem, Ctrl* c,
                            const CtaState& st, uint32_t it0, int kb_from, int kb_to,
                            uint64_t pol_a, uint64_t pol_b) {
@@ -979,18 +993,27 @@ __device__ int issue_loads(const Params& p, const GemmJob& job, char* smem, Ctrl
     const uint32_t s = it % p.stages, ph = (it / p.stages) & 1u;
     if (!mbar_wait(&c->empty_bar[s], ph ^ 1u, st.deadline)) break;
     char* stage = smem + (size_t)s * p.stage_bytes;
-    if (st.rank == 0) mbar_arrive_expect_tx(&c->full_bar[s], (uint32_t)kPair * bytes);
-    const uint32_t fb = full0 + 8u * s;
+    if (st.rank == 0) mbar_arrive_expect_tx(&c->full_bar[s], (uint32_t)P * bytes);
     const int kc = (job.kb0 + kb) * kBK;
-    tma_load_2d_pair(stage, job.a0, fb, kc, job.a_row0, pol_a);
-    if (two) tma_load_2d_pair(stage + kABoxBytes, job.a1, fb, kc, job.a1_row0, pol_a);
-    for (int bx = 0; bx < nbox; ++bx)
-      tma_load_2d_pair(stage + job.b_off + bx * kBBoxBytes, job.b, fb, kc,
-                       job.b_row0 + bx * kBBoxRows, pol_b);
+    if constexpr (P == 2) {
+      const uint32_t fb = full0 + 8u * s;
+      tma_load_2d_pair(stage, job.a0, fb, kc, job.a_row0, pol_a);
+      if (two) tma_load_2d_pair(stage + kABoxBytes, job.a1, fb, kc, job.a1_row0, pol_a);
+      for (int bx = 0; bx < nbox; ++bx)
+        tma_load_2d_pair(stage + job.b_off + bx * kBBoxBytes, job.b, fb, kc,
+                         job.b_row0 + bx * kBBoxRows, pol_b);
+    } else {
+      tma_load_2d(stage, job.a0, &c->full_bar[s], kc, job.a_row0, pol_a);
+      if (two) tma_load_2d(stage + kABoxBytes, job.a1, &c->full_bar[s], kc, job.a1_row0, pol_a);
+      for (int bx = 0; bx < nbox; ++bx)
+        tma_load_2d(stage + job.b_off + bx * kBBoxBytes, job.b, &c->full_bar[s], kc,
+                    job.b_row0 + bx * kBBoxRows, pol_b);
+    }
   }
   return kb - kb_from;
 }
 
+template <int P>
 __device__ bool gemm_mainloop(const Params& p, const Maps& maps, const GemmJob& job, char* smem,
                               Ctrl* c, CtaState& st) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1007,8 +1030,8 @@ __device__ bool gemm_mainloop(const Params& p, const Maps& maps, const GemmJob& 
     const uint64_t pol_b = pol_last;
     const int kb_first = (job.task >= 0 && st.pf_task == job.task) ? st.pf_count : 0;
     st.pf_task = -1;
-    ok = issue_loads(p, job, smem, c, st, st.pipe_it + kb_first, kb_first, job.nkb, pol_a, pol_b) ==
-         job.nkb - kb_first;
+    ok = issue_loads<P>(p, job, smem, c, st, st.pipe_it + kb_first, kb_first, job.nkb, pol_a,
+                        pol_b) == job.nkb - kb_first;
     if (!ok) set_status(p, MOE_E_TIMEOUT, 10);
     // Cross-task overlap: this gate/up or down tile has issued all its loads,
     // so its late phase begins (the scheduler warp may claim the next task
@@ -1039,7 +1062,7 @@ __device__ bool gemm_mainloop(const Params& p, const Maps& maps, const GemmJob& 
         const int n = min(p.stages, nj.nkb);
         const uint64_t pa = nj.a_stream ? pol_first : pol_last;
         const uint64_t pb = pol_last;
-        const int done = issue_loads(p, nj, smem, c, st, st.pipe_it + job.nkb, 0, n, pa, pb);
+        const int done = issue_loads<P>(p, nj, smem, c, st, st.pipe_it + job.nkb, 0, n, pa, pb);
         if (done == n) {
           st.pf_task = nxt;
           st.pf_count = n;
@@ -1050,9 +1073,9 @@ __device__ bool gemm_mainloop(const Params& p, const Maps& maps, const GemmJob& 
       }
     }
   } else if (warp == 1 && lane == 0 && st.rank == 0) {
-    // the leader issues the pair's MMAs, once the peer's epilogue of the
-    // previous GEMM task has finished reading the peer's TMEM
-    if (st.gemm_count > 0) {
+    // the leader issues the worker's MMAs; a pair's leader once the peer's
+    // epilogue of the previous GEMM task has finished reading the peer's TMEM
+    if (P == 2 && st.gemm_count > 0) {
       const uint32_t par = (st.gemm_count - 1u) & 1u;
       bool got;
       while (!(got = mbar_try_wait_cluster(&c->tmem_empty, par)))
@@ -1063,7 +1086,7 @@ __device__ bool gemm_mainloop(const Params& p, const Maps& maps, const GemmJob& 
       }
     }
     if (ok) {
-      const uint32_t idesc = idesc_bf16(kPair * kBM, (uint32_t)job.n_mma);
+      const uint32_t idesc = idesc_bf16(P * kBM, (uint32_t)job.n_mma);
       const uint32_t t0 = c->tmem_base, t1 = c->tmem_base + kAcc1Col;
       uint32_t it = st.pipe_it;
       for (int kb = 0; kb < job.nkb; ++kb, ++it) {
@@ -1082,17 +1105,17 @@ __device__ bool gemm_mainloop(const Params& p, const Maps& maps, const GemmJob& 
           const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
           // advancing 16 bf16 (32 B) inside the 128-B swizzle row: +2 in the
           // 16-byte-granular start-address field
-          mma_bf16(t0, da0 + 2 * kk, db + 2 * kk, idesc, acc);
-          if (two) mma_bf16(t1, da1 + 2 * kk, db + 2 * kk, idesc, acc);
+          mma_bf16<P>(t0, da0 + 2 * kk, db + 2 * kk, idesc, acc);
+          if (two) mma_bf16<P>(t1, da1 + 2 * kk, db + 2 * kk, idesc, acc);
         }
-        mma_commit_both(&c->empty_bar[s]);
+        mma_commit_all<P>(&c->empty_bar[s]);
       }
     }
-    // (also after a failure, so that both CTAs' epilogue warps stop waiting)
-    mma_commit_both(&c->acc_bar);
+    // (also after a failure, so that the epilogue warps stop waiting)
+    mma_commit_all<P>(&c->acc_bar);
   }
   st.pipe_it += job.nkb;
-  // everyone waits for the accumulators (the leader's commit reaches both CTAs)
+  // everyone waits for the accumulators (the leader's commit reaches every CTA)
   __syncwarp();
   const int ok_all = cta_sync_and(ok ? 1 : 0);
   if (!ok_all) return false;
@@ -1103,13 +1126,14 @@ __device__ bool gemm_mainloop(const Params& p, const Maps& maps, const GemmJob& 
   return true;
 }
 
-// The end of every GEMM task (router, gate/up, down), in both CTAs, whether
-// it succeeded or not: this CTA's TMEM reads are complete; the peer tells the
-// leader, whose next MMAs overwrite the peer's accumulators.
+// The end of every GEMM task (router, gate/up, down), in every CTA, whether
+// it succeeded or not: this CTA's TMEM reads are complete; a pair's peer tells
+// the leader, whose next MMAs overwrite the peer's accumulators.
+template <int P>
 __device__ __forceinline__ void gemm_task_end(Ctrl* c, CtaState& st) {
   tc_fence_before();
   st.gemm_count++;
-  if (st.rank != 0) {
+  if (P == 2 && st.rank != 0) {
     cta_sync();
     if (threadIdx.x == 0) mbar_arrive_cluster(st.lead_ctrl + (uint32_t)offsetof(Ctrl, tmem_empty));
   }
@@ -1117,22 +1141,23 @@ __device__ __forceinline__ void gemm_task_end(Ctrl* c, CtaState& st) {
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.f + __expf(-z)); }
 
-// The GEMM job of a gate/up or down task id for the CTA of cluster rank
-// `rank` (false for other task types or an inconsistent group).
+// The GEMM job of a gate/up or down task id for the CTA of rank `rank` in
+// its worker (false for other task types or an inconsistent group).
 __device__ bool make_gemm_job(const Params& p, const Maps& maps, int task, int rank, GemmJob& job) {
   const int type = task_type(task), pl = task_payload(task);
   if (type == kTaskGateUp) {
     const int g = pl / p.n_ftiles, ft = pl - g * p.n_ftiles;
     const Group G = load_group(p, g);
     if (!group_ok(p, G) || ft < 0 || ft >= p.n_ftiles) return false;
-    job.n_mma = ((G.nrows + 31) / 32) * 32;
+    const int gran = 16 * p.pair;  // each CTA's share of N a multiple of 16 rows
+    job.n_mma = ((G.nrows + gran - 1) / gran) * gran;
     job.a0 = &maps.wg;
     job.a1 = &maps.wu;
     job.b = G.e < p.E ? &maps.xp : &maps.x;
-    job.a_row0 = G.e * p.f + ft * kFTile + rank * kBM;
+    job.a_row0 = G.e * p.f + ft * ftile_rows(p) + rank * kBM;
     job.a1_row0 = job.a_row0;
-    job.b_row0 = G.src_row0 + rank * (job.n_mma / 2);
-    job.b_rows = job.n_mma / 2;
+    job.b_row0 = G.src_row0 + rank * (job.n_mma / p.pair);
+    job.b_rows = job.n_mma / p.pair;
     job.b_off = 2 * kABoxBytes;
     job.kb0 = 0;
     job.nkb = p.d / kBK;
@@ -1146,14 +1171,15 @@ __device__ bool make_gemm_job(const Params& p, const Maps& maps, int task, int r
     const int dt = r / p.ks, ksplit = r - dt * p.ks;
     const Group G = load_group(p, g);
     if (!group_ok(p, G) || dt >= p.n_dtiles) return false;
-    job.n_mma = ((G.nrows + 31) / 32) * 32;
+    const int gran = 16 * p.pair;
+    job.n_mma = ((G.nrows + gran - 1) / gran) * gran;
     job.a0 = &maps.wd;
     job.a1 = &maps.wd;
     job.b = &maps.h;
-    job.a_row0 = G.e * p.d + dt * kDTile + rank * kBM;
-    job.a1_row0 = job.a_row0 + kPair * kBM;
-    job.b_row0 = G.row0 + rank * (job.n_mma / 2);
-    job.b_rows = job.n_mma / 2;
+    job.a_row0 = G.e * p.d + dt * dtile_rows(p) + rank * kBM;
+    job.a1_row0 = job.a_row0 + ftile_rows(p);
+    job.b_row0 = G.row0 + rank * (job.n_mma / p.pair);
+    job.b_rows = job.n_mma / p.pair;
     job.b_off = 2 * kABoxBytes;
     job.kb0 = ksplit * p.kb_down;
     job.nkb = p.kb_down;
@@ -1164,6 +1190,7 @@ __device__ bool make_gemm_job(const Params& p, const Maps& maps, int task, int r
   return false;
 }
 
+template <int P>
 __device__ void gateup_task(const Params& p, const Maps& maps, int task, char* smem, Ctrl* c,
                             CtaState& st) {
   const int pl = task_payload(task);
@@ -1172,15 +1199,15 @@ __device__ void gateup_task(const Params& p, const Maps& maps, int task, char* s
   GemmJob job;
   if (!make_gemm_job(p, maps, task, st.rank, job)) {
     if (threadIdx.x == 0) set_status(p, MOE_E_DEVICE, 21);
-    gemm_task_end(c, st);
+    gemm_task_end<P>(c, st);
     return;
   }
-  const bool ok = gemm_mainloop(p, maps, job, smem, c, st);
+  const bool ok = gemm_mainloop<P>(p, maps, job, smem, c, st);
   if (ok) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q = warp & 3, half = warp >> 2;
-    // this thread's f row: row m of this CTA's 128 rows of the 256-row tile
-    const int frow = ft * kFTile + st.rank * kBM + q * 32 + lane;
+    // this thread's f row: row m of this CTA's 128 rows of the tile
+    const int frow = ft * ftile_rows(p) + st.rank * kBM + q * 32 + lane;
     const bool in_f = frow < p.f;  // the last tile of an f that is an odd multiple of 128
     const uint32_t lane_addr = c->tmem_base + ((uint32_t)(q * 32) << 16);
     __nv_bfloat16* hcol = p.H + (size_t)G.row0 * p.f + frow;
@@ -1194,9 +1221,10 @@ __device__ void gateup_task(const Params& p, const Maps& maps, int task, char* s
       }
     }
   }
-  gemm_task_end(c, st);
+  gemm_task_end<P>(c, st);
 }
 
+template <int P>
 __device__ void down_task(const Params& p, const Maps& maps, int task, char* smem, Ctrl* c,
                           CtaState& st) {
   const int n_down = p.n_dtiles * p.ks;
@@ -1207,16 +1235,17 @@ __device__ void down_task(const Params& p, const Maps& maps, int task, char* sme
   GemmJob job;
   if (!make_gemm_job(p, maps, task, st.rank, job)) {
     if (threadIdx.x == 0) set_status(p, MOE_E_DEVICE, 22);
-    gemm_task_end(c, st);
+    gemm_task_end<P>(c, st);
     return;
   }
-  const bool ok = gemm_mainloop(p, maps, job, smem, c, st);
+  const bool ok = gemm_mainloop<P>(p, maps, job, smem, c, st);
   if (ok) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q = warp & 3, half = warp >> 2;
     // this thread's two d columns: row m of this CTA's 128 rows of each
-    // accumulator's 256
-    const int col0 = dt * kDTile + st.rank * kBM + q * 32 + lane, col1 = col0 + kPair * kBM;
+    // accumulator
+    const int col0 = dt * dtile_rows(p) + st.rank * kBM + q * 32 + lane;
+    const int col1 = col0 + ftile_rows(p);
     const uint32_t lane_addr = c->tmem_base + ((uint32_t)(q * 32) << 16);
     const bool has0 = col0 < p.d, has1 = col1 < p.d;
     for (int ch = half; ch * 16 < G.nrows; ch += 2) {
@@ -1247,7 +1276,7 @@ __device__ void down_task(const Params& p, const Maps& maps, int task, char* sme
       }
     }
   }
-  gemm_task_end(c, st);
+  gemm_task_end<P>(c, st);
 }
 
 
@@ -1451,26 +1480,27 @@ __device__ __forceinline__ void route_epilogue_k(const Params& p, Ctrl* c, int t
   else route_epilogue<16>(p, c, tile, nt, lg, ls, xch);
 }
 
-// One router task: router tiles 2 pt (the leader's) and 2 pt + 1 (the
-// peer's), K split `split` of p.route_ks, as one pair MMA: each CTA's 128 A
-// rows are its tile's tokens, and the experts (N, padded to 32) are split in
+// One router task: router tile P pt + r for the CTA of rank r, K split
+// `split` of p.route_ks, as one MMA of the worker: each CTA's 128 A rows are
+// its tile's tokens; for a pair the experts (N, padded to 32) are split in
 // halves between the two CTAs' B operands, so each CTA's TMEM receives all
 // the logits of its own tokens.  With a single split the epilogue reads the
 // logits from TMEM.  With several, each split stores its fp32 partial logits;
 // the split that finishes last sums all of them in split order (fixed, so the
 // result does not depend on timing) and runs the epilogue.  Returns true when
 // this call completed this CTA's tile (the peer of an odd last tile has none).
+template <int P>
 __device__ bool route_task(const Params& p, const Maps& maps, int pt, int split, char* smem,
                            Ctrl* c, CtaState& st) {
   const int rt = p.rt;  // tokens of a router tile: 128, or 64 for small layers
-  const int tile = pt * kPair + st.rank;
+  const int tile = pt * P + st.rank;
   const bool mine = tile < p.n_route;
   const int t0 = tile * rt;
   const int nt = mine ? min(rt, p.T - t0) : 0;
   const int ks = p.route_ks;
   const int nkb = p.d / kBK;
   const int epad = ((p.E + 15) / 16) * 16;   // logit columns read back
-  const int nmma = ((p.E + 31) / 32) * 32;   // MMA N over the pair
+  const int nmma = ((p.E + 16 * P - 1) / (16 * P)) * (16 * P);  // MMA N over the worker
   for (int i = threadIdx.x; i < kMaxE * 4; i += kThreads) c->mask[i] = 0u;
   for (int e = threadIdx.x; e < kMaxE; e += kThreads)
     c->bias_s[e] = (p.bias && e < p.E) ? __ldg(p.bias + e) : 0.f;
@@ -1480,15 +1510,15 @@ __device__ bool route_task(const Params& p, const Maps& maps, int pt, int split,
   job.b = &maps.wr;
   job.a_row0 = t0;  // past T (the peer of an odd last tile): zero-filled rows
   job.a1_row0 = 0;
-  job.b_row0 = st.rank * (nmma / 2);
-  job.b_rows = nmma / 2;
+  job.b_row0 = st.rank * (nmma / P);
+  job.b_rows = nmma / P;
   job.n_mma = nmma;
   job.b_off = kABoxBytes;
   job.kb0 = split * nkb / ks;
   job.nkb = (split + 1) * nkb / ks - job.kb0;
   job.a_stream = true;  // x rows: read by this tile only; Wr (B) is shared by all tiles
   job.task = -1;
-  const bool ok = gemm_mainloop(p, maps, job, smem, c, st);
+  const bool ok = gemm_mainloop<P>(p, maps, job, smem, c, st);
   bool tile_done = false;
   if (ok && mine) {
     const int warp = threadIdx.x >> 5;
@@ -1574,7 +1604,7 @@ __device__ bool route_task(const Params& p, const Maps& maps, int pt, int split,
       }
     }
   }
-  gemm_task_end(c, st);
+  gemm_task_end<P>(c, st);
   return tile_done;
 }
 

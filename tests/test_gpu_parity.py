@@ -1,5 +1,6 @@
 """CUDA path against the CPU oracle on small layers that span several tiles,
-ragged tails and the layer's degenerate cases, through the C ABI."""
+ragged tails and the layer's degenerate cases, through the C ABI -- with the
+GEMM tiles on one CTA (pair=1) and on CTA pairs (pair=2) alike."""
 import numpy as np
 import pytest
 
@@ -33,39 +34,55 @@ def _full_check(w, inp, mode="persistent", **opts):
     return got
 
 
+@pytest.mark.parametrize("pair", [1, 2])
 @pytest.mark.parametrize("name", list(CASES))
-def test_small_layer_parity(name):
+def test_small_layer_parity(name, pair):
     T, d, E, k, f, S, b = CASES[name]
     w, inp = hz.custom_case(T, d, E, k, f, S, b)
-    _full_check(w, inp)
+    _full_check(w, inp, pair=pair)
 
 
+@pytest.mark.parametrize("pair", [1, 2])
 @pytest.mark.parametrize("name", ["tiny", "shared_partial_dtile", "multi_mtile_skew"])
-def test_multikernel_ablation_bit_identical(name):
+def test_multikernel_ablation_bit_identical(name, pair):
     T, d, E, k, f, S, b = CASES[name]
     w, inp = hz.custom_case(T, d, E, k, f, S, b)
-    a = _full_check(w, inp, "persistent")
-    m = _full_check(w, inp, "multikernel")
+    a = _full_check(w, inp, "persistent", pair=pair)
+    m = _full_check(w, inp, "multikernel", pair=pair)
     assert np.array_equal(a, m), "ablation and megakernel outputs differ"
 
 
+@pytest.mark.parametrize("pair", [1, 2])
 @pytest.mark.parametrize("name", ["tiny", "shared_partial_dtile", "multi_mtile_skew", "top16"])
-def test_static_megakernel_bit_identical(name):
+def test_static_megakernel_bit_identical(name, pair):
     # one cooperative launch, round-robin tasks, grid barriers between stages
     T, d, E, k, f, S, b = CASES[name]
     w, inp = hz.custom_case(T, d, E, k, f, S, b)
-    a = _full_check(w, inp, "persistent")
-    s = _full_check(w, inp, "static")
+    a = _full_check(w, inp, "persistent", pair=pair)
+    s = _full_check(w, inp, "static", pair=pair)
     assert np.array_equal(a, s), "static megakernel and persistent megakernel outputs differ"
-    s7 = _full_check(w, inp, "static", grid_ctas=7)
+    s7 = _full_check(w, inp, "static", grid_ctas=7, pair=pair)
     assert np.array_equal(a, s7), "static megakernel depends on its grid size"
 
 
+@pytest.mark.parametrize("pair", [1, 2])
 @pytest.mark.parametrize("split_k", [1, 2, 4])
 @pytest.mark.parametrize("tokens_per_tile", [32, 64, 256])
-def test_tiling_options_same_result(split_k, tokens_per_tile):
+def test_tiling_options_same_result(split_k, tokens_per_tile, pair):
     w, inp = hz.custom_case(200, 256, 8, 2, 512, 0, 0.4)
-    _full_check(w, inp, split_k=split_k, tokens_per_tile=tokens_per_tile)
+    _full_check(w, inp, split_k=split_k, tokens_per_tile=tokens_per_tile, pair=pair)
+
+
+def test_pair_width_is_automatic_and_reported():
+    # pairs when the mean rows per expert reach 128, one CTA below
+    for T, E, k, want in ((64, 8, 2, 1), (512, 8, 2, 2)):
+        w, inp = hz.custom_case(T, 256, E, k, 256, 0, 0.0)
+        dev = hz.upload(inp)
+        layer = hz.make_layer(w)
+        hz.run_layer(layer, w, dev)
+        assert layer.stat("pair") == want
+        assert layer.stat("grid") % want == 0
+        layer.close()
 
 
 def test_all_tokens_one_expert():
@@ -82,10 +99,11 @@ def test_identical_experts_give_one_ffn():
         hz.check_out(got[t], oracle.f64_to_bf16(y), "identical experts")
 
 
-def test_grid_and_mover_overrides():
+@pytest.mark.parametrize("pair", [1, 2])
+def test_grid_and_mover_overrides(pair):
     w, inp = hz.custom_case(160, 256, 16, 4, 256, 1, 0.5)
-    _full_check(w, inp, grid_ctas=7, mover_ctas=3)
-    _full_check(w, inp, grid_ctas=1)
+    _full_check(w, inp, grid_ctas=7, mover_ctas=3, pair=pair)
+    _full_check(w, inp, grid_ctas=1, pair=pair)
 
 
 def test_smaller_T_than_reserved_and_repeat():

@@ -50,12 +50,15 @@ def _run(w, inp, residual, gamma, mode=0, **opts):
     return got
 
 
+@pytest.mark.parametrize("pair", [1, 2])
 @pytest.mark.parametrize("name", list(CASES))
-def test_residual_norm_parity(name):
+def test_residual_norm_parity(name, pair):
+    # GEMM tiles on one CTA and on CTA pairs (whose CTAs split each combine
+    # tile's tokens: the norm waits for both halves)
     T, d, E, k, f, S, b, opts = CASES[name]
     w, inp = hz.custom_case(T, d, E, k, f, S, b)
     residual, gamma = _extra(T, d)
-    out, norm = _run(w, inp, residual, gamma, **opts)
+    out, norm = _run(w, inp, residual, gamma, pair=pair, **opts)
     _, acc = oracle.layer(inp["x"], inp["router_w"], inp["bias"], inp["w_gate"], inp["w_up"],
                           inp["w_down"], k=w.k, S=w.S)
     ref_out, ref_norm, _ = oracle.residual_rmsnorm(acc, residual, gamma, EPS)
@@ -63,9 +66,11 @@ def test_residual_norm_parity(name):
     hz.check_out(norm, ref_norm, "RMSNorm(out) * gamma")
 
 
+@pytest.mark.parametrize("pair", [1, 2])
 @pytest.mark.parametrize("name", ["small", "shared_expert", "fp32_partials"])
-def test_residual_norm_same_bits_in_every_mode(name):
+def test_residual_norm_same_bits_in_every_mode(name, pair):
     T, d, E, k, f, S, b, opts = CASES[name]
+    opts = dict(opts, pair=pair)
     w, inp = hz.custom_case(T, d, E, k, f, S, b)
     residual, gamma = _extra(T, d)
     base = _run(w, inp, residual, gamma, mode=0, **opts)

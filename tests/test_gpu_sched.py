@@ -13,17 +13,19 @@ from persistent_megakernel_sm_gb300 import MOE_E_TIMEOUT, MOE_OK
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module")
-def case():
+@pytest.fixture(scope="module", params=[1, 2], ids=["cta", "pair"])
+def case(request):
+    # the same layer with GEMM tiles on one CTA and on CTA pairs
     w, inp = hz.custom_case(300, 256, 16, 4, 384, 1, 0.6)
     dev = hz.upload(inp)
     ref, _ = oracle.layer(inp["x"], inp["router_w"], inp["bias"], inp["w_gate"], inp["w_up"],
                           inp["w_down"], k=w.k, S=w.S)
+    dev["pair"] = request.param
     return w, inp, dev, ref
 
 
 def _run(w, dev, **opts):
-    layer = hz.make_layer(w, **opts)
+    layer = hz.make_layer(w, pair=dev["pair"], **opts)
     out, routing = hz.run_layer(layer, w, dev)
     return layer, out, routing
 
@@ -40,10 +42,11 @@ def test_every_task_runs_exactly_once(case):
     assert layer.stat("tasks") == len(tasks)
     types = set((tasks >> 28).tolist())
     assert types == {1, 2, 3, 4, 5}, types
-    # every CTA pair (its leader) recorded its exit after its last task
+    # every worker (its leader CTA) recorded its exit after its last task
+    P = layer.stat("pair")
     exits = tr["cta"][tr["task"] == 0x7FFFFFFF]
-    assert len(exits) == layer.stat("grid") // 2 and len(np.unique(exits)) == len(exits)
-    assert np.all(exits % 2 == 0), "exit records come from the pairs' leaders"
+    assert len(exits) == layer.stat("grid") // P and len(np.unique(exits)) == len(exits)
+    assert np.all(exits % P == 0), "exit records come from the workers' leaders"
     # dependency order: per group, gate/up before down; a combine after all downs
     t_end = tr["t_end"][real]
     t_start = tr["t_start"][real]
@@ -53,7 +56,7 @@ def test_every_task_runs_exactly_once(case):
     from persistent_megakernel_sm_gb300.trace_report import summarize
     s = summarize(tr)
     assert set(s["types"]) == {"route", "gather", "gateup", "down", "combine"}
-    assert s["grid"] == layer.stat("grid") // 2 and len(s["plan_phases_us"]) == 8
+    assert s["grid"] == layer.stat("grid") // P and len(s["plan_phases_us"]) == 8
     assert sum(t["n"] for t in s["types"].values()) == layer.stat("tasks")
     layer.close()
 
@@ -110,23 +113,25 @@ def test_router_tile_size_keeps_routing_and_tolerance(case, rt):
 
 @pytest.mark.parametrize("grid", [None, 37])
 def test_spatial_split_matches_oracle(case, grid):
-    # the plan's split of the workers (CTA pairs) into movers and GEMM
+    # the plan's split of the workers (P CTAs each) into movers and GEMM
     # workers, from the routed counts, against the oracle's fp32 statement of
-    # the same cost model with the kernel's constants per pair (80 GB/s per
-    # mover, two SMs' share of 1925 TF/s per GEMM worker, 6.79 TB/s of weight
+    # the same cost model with the kernel's constants per worker (40 GB/s per
+    # mover CTA, one SM's share of 1925 TF/s per GEMM CTA, 6.79 TB/s of weight
     # stream)
     w, inp, dev, ref = case
     layer, out, routing = _run(w, dev, **({} if grid is None else dict(grid_ctas=grid)))
     hz.check_out(out, ref)
     counts = oracle.permute(oracle.route(inp["x"], inp["router_w"], inp["bias"], w.k)["idx"],
                             w.E)[0]
-    N = layer.stat("grid") // 2
+    P = layer.stat("pair")
+    N = layer.stat("grid") // P
     # the combine reads each expert output as stored: bf16 (2 bytes) or ks
     # fp32 partial sums (4 ks bytes), whichever layout this forward used
     ybytes = layer.stat("y_bytes")
     assert ybytes in (2, 4, 8, 16)
     want, x = oracle.movers(w.T, w.d, w.f, w.k, w.S, int(np.count_nonzero(counts)), N, ybytes,
-                            80e9, float(np.float32(1925e12) / np.float32(76)), 6.79e12)
+                            40e9 * P, float(np.float32(1925e12) / np.float32(152) * np.float32(P)),
+                            6.79e12)
     got = layer.stat("mover_ctas")
     if abs(x - np.floor(x) - 0.5) < 1e-3:  # fp32 contraction may tip a near tie
         assert abs(got - want) <= 1, (got, want, x)
@@ -138,7 +143,7 @@ def test_spatial_split_matches_oracle(case, grid):
 def test_dropped_notification_times_out_cleanly(case):
     import torch
     w, inp, dev, ref = case
-    layer = hz.make_layer(w, timeout_ns=50_000_000, fault_drop_task=3)
+    layer = hz.make_layer(w, timeout_ns=50_000_000, fault_drop_task=3, pair=dev["pair"])
     out = torch.empty((w.T, w.d), dtype=torch.bfloat16, device="cuda")
     layer.set_router_bias(dev["bias"])
     layer.forward(dev["x"], dev["router_w"], dev["w_gate"], dev["w_up"], dev["w_down"], out)
@@ -154,7 +159,7 @@ def test_dropped_notification_times_out_cleanly(case):
 def test_cuda_graph_capture_and_replay(case):
     import torch
     w, inp, dev, ref = case
-    layer = hz.make_layer(w)
+    layer = hz.make_layer(w, pair=dev["pair"])
     layer.set_router_bias(dev["bias"])
     out = torch.empty((w.T, w.d), dtype=torch.bfloat16, device="cuda")
     eager, _ = hz.run_layer(layer, w, dev)
@@ -177,7 +182,7 @@ def test_cuda_graph_capture_and_replay(case):
 def test_forward_host_matches_device_forward(case):
     import torch
     w, inp, dev, ref = case
-    layer = hz.make_layer(w)
+    layer = hz.make_layer(w, pair=dev["pair"])
     layer.set_router_bias(dev["bias"])
     eager, _ = hz.run_layer(layer, w, dev)
     x_host = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
