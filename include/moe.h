@@ -128,6 +128,15 @@ typedef struct moe_layer moe_layer_t;
                                   pairs when the mean rows per expert
                                   (T k / E) are at least 128                 */
 
+#define MOE_OPT_FRONT_SPLIT 17 /* persistent mode, once routing is known:
+                                  1 = only the cost model's mover workers
+                                  prefer the gathers; the GEMM workers run
+                                  the GEMM tiles that are ready and take
+                                  gathers only when none is; 0 = every worker
+                                  prefers gathers while any is left; -1
+                                  (default) = 1 without a shared expert, 0
+                                  with one                                   */
+
 /* statistics keys for moe_layer_get_stat (values of the last forward;
  * moe_layer_status must have been called after it) */
 #define MOE_STAT_MOVER_CTAS 1  /* mover workers the cost model chose          */

@@ -17,7 +17,9 @@ constexpr int kBK = 64;             // K elements per pipeline stage (128 B rows
 constexpr int kABoxBytes = kBM * kBK * 2;   // 16 KB weight box
 constexpr int kBBoxRows = 32;       // token rows per activation box
 constexpr int kBBoxBytes = kBBoxRows * kBK * 2;  // 4 KB
-constexpr int kGatherRowsCta = 32;  // permuted rows per gather task and CTA of the worker
+constexpr int kGatherRowsCta = 32;  // permuted rows per gather task and CTA of the worker ...
+constexpr int kGatherRowsCtaBig = 64;  // ... and in layers of at least kGatherBigRows routed rows
+constexpr int kGatherBigRows = 16384;
 constexpr int kRouteTokens = 128;   // tokens per router tile (one CTA's 128 rows of the MMA M)
 constexpr int kRouteTokensSmall = 64;  // router tile of small layers with many experts
 constexpr int kSmallRouteT = 1024;
@@ -98,6 +100,7 @@ struct Params {
   int T, d, f, E, k, S;
   // tiling
   int pair;          // CTAs per worker: 1, or 2 (a cluster whose CTAs share each GEMM tile)
+  int gather_cta_rows;  // permuted rows per gather task and CTA
   int bn_max;        // max tokens per GEMM tile (multiple of 32, <= 256)
   int stages;        // pipeline stages
   int stage_bytes;   // 2 * kABoxBytes + ceil(bn_max / pair / 32) * kBBoxBytes
@@ -126,6 +129,7 @@ struct Params {
   int mover_override;
   int ahead_depth;   // claim the next task early when this many wait (0 = never)
   int index_order;   // the plan keeps experts in index order (not by count)
+  int front_split;   // after the plan only mover workers prefer gathers (else every worker)
   long long l2_pf_bytes;  // gate/up weight bytes prefetched into L2 at launch (0 = none)
   unsigned long long timeout_ns;
   // cost model constants

@@ -649,6 +649,7 @@ struct moe_layer {
   int max_pairs = 0;  // clusters of two CTAs the persistent kernel can keep resident
   // options
   int pair_opt = 0;  // CTAs per worker: 0 = automatic, 1, 2
+  int front_split = -1;  // the spatial split also governs the gathers: -1 = auto
   int mode = MOE_MODE_PERSISTENT;
   unsigned long long timeout_ns = 2000000000ull;
   int mover_override = 0;
@@ -1086,6 +1087,10 @@ int moe_layer_set_option(moe_layer_t* h, int key, long long v) {
       if (v < 0 || v > kMaxRouteKs) return fail(MOE_E_INVAL, "router K splits must be 0..8");
       h->route_splits = (int)v;
       break;
+    case MOE_OPT_FRONT_SPLIT:
+      if (v < -1 || v > 1) return fail(MOE_E_INVAL, "front split must be -1 (auto), 0 or 1");
+      h->front_split = (int)v;
+      break;
     case MOE_OPT_PAIR:
       if (v != 0 && v != 1 && v != 2) return fail(MOE_E_INVAL, "CTAs per worker must be 0 (auto), 1 or 2");
       h->pair_opt = (int)v;
@@ -1140,6 +1145,11 @@ int forward_impl(moe_layer_t* h, int T, const void* x, const void* router_w, con
   p.stage_bytes = tl.stage_bytes;
   const int P = tl.pair;
   p.pair = P;
+  // gather tasks of 64 rows per CTA in large layers (prefill layer, one
+  // kernel per stage: the gathers move their 1.9 GB in 273 us at 64 rows per
+  // CTA; the persistent kernel's 32-row tasks took 370 us of each worker),
+  // 32 in small ones, where the gathers are few and on the critical path
+  p.gather_cta_rows = (long long)T * h->k >= kGatherBigRows ? kGatherRowsCtaBig : kGatherRowsCta;
   p.n_ftiles = cdiv(h->f, kBM * P);
   p.n_dtiles = cdiv(h->d, 2 * kBM * P);
   p.ks = tl.ks;
@@ -1161,6 +1171,10 @@ int forward_impl(moe_layer_t* h, int T, const void* x, const void* router_w, con
   }
   p.release = h->release;
   p.prefetch = h->prefetch;
+  // the front's spatial split: on without a shared expert (skew layer 1047 ->
+  // 1039 us on one box), off with one, whose ready tiles would then run
+  // before the routed experts' (prefill layer 6468 -> 6986 us)
+  p.front_split = h->front_split < 0 ? (h->S == 0 ? 1 : 0) : h->front_split;
   p.ct = tl.ct;
   // d bands: the down tiles of the last quarter of d (at least one tile)
   // have low priority, so the other band's combines overlap them
@@ -1183,9 +1197,14 @@ int forward_impl(moe_layer_t* h, int T, const void* x, const void* router_w, con
   p.trace = h->trace;
   p.trace_cap = h->trace_cap;
   p.timeout_ns = h->timeout_ns;
-  // cost-model constants per worker (P CTAs): 40 GB/s of bulk copies and one
-  // SM's share of 1925 TF/s, per CTA
-  p.beta_move = 40e9f * (float)P;
+  // cost-model constants per worker (P CTAs): beta for the movers and one
+  // SM's share of 1925 TF/s for the GEMMs, per CTA.  beta is calibrated, not
+  // a copy rate (a gather CTA moves ~35 GB/s): GEMM workers steal gathers and
+  // combines whenever no tile is ready, so the movers only need to keep the
+  // mover work going beside the GEMMs, and sweeps of the mover count on the
+  // skew and prefill_small layers put the fastest split at about 4 of 76
+  // workers -- the split this beta gives them
+  p.beta_move = 140e9f * (float)P;
   p.phi_gemm = (1925e12f / 152.f) * (float)P;
   p.hbm_bw = 6.79e12f;
   p.x = static_cast<const __nv_bfloat16*>(x);

@@ -365,11 +365,16 @@ __device__ int claim_once(const Params& p, CtaState& st, int min_depth) {
   const int depth_l = warp_sum_i(qi == 2 ? dep : 0);
   const unsigned ball = __ballot_sync(full, mine && h < avail);
   const bool gathers_left = st.plan_seen && claimed_m < p.n_route_tasks + st.n_gather;
-  // Before the plan every CTA prefers router tiles, and afterwards every CTA
-  // prefers gathers while any is unclaimed: both gate all the GEMM work.
-  // Otherwise a mover CTA takes mover, GEMM, low-priority GEMM work in that
-  // order, a GEMM CTA GEMM, low-priority GEMM, mover work.
-  const bool mover_first = !st.plan_seen || gathers_left || st.role_mover;
+  // Before the plan every worker prefers router tiles: they gate all the
+  // GEMM work.  After it, a mover worker takes mover, GEMM, low-priority GEMM
+  // work in that order, a GEMM worker GEMM, low-priority GEMM, mover work --
+  // so with the spatial split of the front (p.front_split) the GEMM workers
+  // run the tiles that are ready (the shared expert's, then each expert's as
+  // its gathers land) while the mover workers gather, and take gathers only
+  // when no GEMM tile is ready.  Without it every worker prefers gathers
+  // while any is unclaimed.
+  const bool mover_first =
+      !st.plan_seen || (gathers_left && !p.front_split) || st.role_mover;
   const int npass = min_depth > 1 ? 1 : 3;
   const int home = st.worker & (kShards - 1);
   for (int pass = 0; pass < npass; ++pass) {
@@ -442,7 +447,7 @@ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; 
 // over the worker's CTAs.
 __device__ __forceinline__ int ftile_rows(const Params& p) { return kBM * p.pair; }
 __device__ __forceinline__ int dtile_rows(const Params& p) { return 2 * kBM * p.pair; }
-__device__ __forceinline__ int gather_rows(const Params& p) { return kGatherRowsCta * p.pair; }
+__device__ __forceinline__ int gather_rows(const Params& p) { return p.gather_cta_rows * p.pair; }
 
 // Number of gather tasks of a group.
 __device__ __forceinline__ int gather_chunks(const Params& p, int nrows) {
@@ -621,7 +626,7 @@ __device__ void plan_task(const Params& p, char* scratch, Ctrl* c, bool push) {
 }
 
 // ------------------------------------------------------------------ gather (mover)
-// Xp[row, :] = x[perm[row], :] for up to 32 rows per CTA of the worker of one
+// Xp[row, :] = x[perm[row], :] for up to 32 or 64 rows per CTA of the worker of one
 // group, of which this CTA takes part `half` of `nhalf` (the CTAs of a pair
 // split the rows).
 // One thread moves whole rows with bulk copies through shared memory (global

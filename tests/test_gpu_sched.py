@@ -115,9 +115,9 @@ def test_router_tile_size_keeps_routing_and_tolerance(case, rt):
 def test_spatial_split_matches_oracle(case, grid):
     # the plan's split of the workers (P CTAs each) into movers and GEMM
     # workers, from the routed counts, against the oracle's fp32 statement of
-    # the same cost model with the kernel's constants per worker (40 GB/s per
-    # mover CTA, one SM's share of 1925 TF/s per GEMM CTA, 6.79 TB/s of weight
-    # stream)
+    # the same cost model with the kernel's constants per worker (140 GB/s
+    # per mover CTA, one SM's share of 1925 TF/s per GEMM CTA, 6.79 TB/s of
+    # weight stream)
     w, inp, dev, ref = case
     layer, out, routing = _run(w, dev, **({} if grid is None else dict(grid_ctas=grid)))
     hz.check_out(out, ref)
@@ -130,7 +130,7 @@ def test_spatial_split_matches_oracle(case, grid):
     ybytes = layer.stat("y_bytes")
     assert ybytes in (2, 4, 8, 16)
     want, x = oracle.movers(w.T, w.d, w.f, w.k, w.S, int(np.count_nonzero(counts)), N, ybytes,
-                            40e9 * P, float(np.float32(1925e12) / np.float32(152) * np.float32(P)),
+                            140e9 * P, float(np.float32(1925e12) / np.float32(152) * np.float32(P)),
                             6.79e12)
     got = layer.stat("mover_ctas")
     if abs(x - np.floor(x) - 0.5) < 1e-3:  # fp32 contraction may tip a near tie
