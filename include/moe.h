@@ -137,6 +137,26 @@ typedef struct moe_layer moe_layer_t;
                                   (default) = 1 without a shared expert, 0
                                   with one                                   */
 
+#define MOE_OPT_FAULT_DROP_TYPE 18 /* test only: 0 off; 2, 3 or 4 = drop every
+                                      dependency notification of gather,
+                                      gate/up or down tasks, which must end
+                                      in MOE_E_TIMEOUT                        */
+#define MOE_OPT_FAULT_CORRUPT_COUNT 19 /* test only: 0 off; else the plan adds
+                                      this to the first expert's token count;
+                                      its check (counts summing to T k) must
+                                      end the pass in MOE_E_DEVICE           */
+#define MOE_OPT_FAULT_REPUSH 20 /* test only, with MOE_OPT_DEBUG_CLAIMS: -1
+                                  off; else the n-th finished gate/up task is
+                                  pushed into the queue again, which the
+                                  claimed-twice check must end in
+                                  MOE_E_DEVICE (without the check the extra
+                                  claim can end the queue's count early: the
+                                  output is then undefined)                   */
+#define MOE_OPT_DEBUG_CLAIMS 21 /* persistent mode: 1 = every task claimed
+                                  sets a bit; a task claimed twice (or an id
+                                  outside the layer's tasks) sets
+                                  MOE_E_DEVICE, never a trap; 0 (default) off */
+
 /* statistics keys for moe_layer_get_stat (values of the last forward;
  * moe_layer_status must have been called after it) */
 #define MOE_STAT_MOVER_CTAS 1  /* mover workers the cost model chose          */

@@ -84,6 +84,7 @@ struct Sched {
   int stat_mover;
   int stat_stolen;
   int fault_seen;
+  int repush_seen;
   int err_info;
   int trace_n;
   int stat_ahead;
@@ -126,6 +127,9 @@ struct Params {
   int max_groups;    // capacity of the group arrays
   int mover_seg, gemm_seg;  // ring capacity of one shard
   int fault_drop;    // -1, or the index of the GEMM completion to drop
+  int fault_drop_type;   // 0, or a task type whose every dependency notification is dropped
+  int fault_corrupt;     // 0, or a count the plan adds to the first expert's token count
+  int fault_repush;      // -1, or the index of the gate/up completion whose task is pushed again
   int mover_override;
   int ahead_depth;   // claim the next task early when this many wait (0 = never)
   int index_order;   // the plan keeps experts in index order (not by count)
@@ -173,6 +177,12 @@ struct Params {
   int* ring_gemm;    // [kShards][gemm_seg]  task id + 1, 0 = not yet pushed
   int* ring_gemm_lo; // [kShards][gemm_seg]  the low-priority GEMM queue
   Sched* sched;
+  // debug: one bit per task, set when the task is claimed (persistent mode);
+  // null when off.  Bits [0, n_route_tasks) router tasks, then
+  // claim_gather_off + g*8 + chunk, claim_gateup_off + the gate/up payload,
+  // claim_down_off + the down payload, claim_comb_off + the combine payload.
+  uint32_t* claimed;
+  int claim_gather_off, claim_gateup_off, claim_down_off, claim_comb_off, claim_bits;
   float* rpart;      // [n_route][route_ks][128][E padded to 16] partial router logits
   int* rsplit_done;  // [n_route] router K splits finished
   unsigned long long* trace;  // [trace_cap][4] task trace records (or null)

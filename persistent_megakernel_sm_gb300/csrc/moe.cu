@@ -180,6 +180,7 @@ __device__ void compute_loop(const Params& p, const Maps& maps, char* smem, Ctrl
           t = c->mb_task[st.taken & 1];
           c->t_claim = c->mb_tclaim[st.taken & 1];
           ++st.taken;
+          if (lead && t >= 0) check_claim(p, t);
           if (lead) st_release_cta_shared(&c->mb_taken, st.taken);
           else st_release_cluster(smem_u32(&c->mb_taken), st.taken);
           break;
@@ -637,6 +638,9 @@ struct Bounds {
   int n_comb;       // combine tiles at one token per tile
   int mover_cap, gemm_cap;
   size_t y_elems;   // elements of Y storage (fp32 words or 2x bf16)
+  // the debug claimed-twice bitmap: router, gather, gate/up, down and combine
+  // tasks at their largest counts (one CTA per worker, 4 K splits)
+  int claim_gather_off, claim_gateup_off, claim_down_off, claim_comb_off, claim_bits;
 };
 
 }  // namespace
@@ -657,6 +661,10 @@ struct moe_layer {
   int split_k = 0;
   int bn_opt = 0;
   int fault_drop = -1;
+  int fault_drop_type = 0;
+  int fault_corrupt = 0;
+  int fault_repush = -1;
+  int debug_claims = 0;
   int rt_opt = 0;
   int ahead_opt = -1;
   int release = kReleaseExpert;
@@ -673,7 +681,7 @@ struct moe_layer {
   Bounds B{};
   // offsets into ws
   size_t o_idx, o_wgt, o_rank, o_tile, o_counts, o_offsets, o_perm, o_pos, o_xp, o_h, o_y,
-      o_groups, o_rpart, o_rsd, o_rmask, o_zero, o_gd, o_gu, o_cd, o_nd, o_sched, o_zero_end, o_ring, o_ring_m, o_ring_g, o_ring_gl,
+      o_groups, o_rpart, o_rsd, o_rmask, o_zero, o_gd, o_gu, o_cd, o_nd, o_claimed, o_sched, o_zero_end, o_ring, o_ring_m, o_ring_g, o_ring_gl,
       o_ring_end;
   // where the last forward's routing and scheduler state live: the reserved
   // workspace, or the no-allocation entry point's scratch array
@@ -708,6 +716,11 @@ Bounds make_bounds(const moe_layer* h, int T) {
   b.mover_cap = cdiv(Tk, 32) + b.max_groups + b.n_comb + 16;
   const int n_ft = h->f / 128, n_dt = cdiv(h->d, 256);
   b.gemm_cap = b.max_groups * (n_ft + n_dt * 4) + 16;
+  b.claim_gather_off = b.n_route * kMaxRouteKs;
+  b.claim_gateup_off = b.claim_gather_off + b.max_groups * 8;
+  b.claim_down_off = b.claim_gateup_off + b.max_groups * n_ft;
+  b.claim_comb_off = b.claim_down_off + b.max_groups * n_dt * 4;
+  b.claim_bits = b.claim_comb_off + b.n_comb;
   const long long rows = Tk + (long long)T * h->S;
   // fp32 partials for up to 4 K splits when small, else bf16 (half a word each)
   const long long small = rows * h->d * 4;
@@ -745,6 +758,7 @@ void layout(moe_layer* h, const Bounds& b) {
   h->o_gu = take((size_t)b.max_groups * 4);
   h->o_cd = take((size_t)b.n_comb * 4);
   h->o_nd = take((size_t)b.n_comb * 4);
+  h->o_claimed = take((size_t)(b.claim_bits + 31) / 32 * 4);
   h->o_zero_end = o;
   h->o_ring = o;
   h->o_ring_m = take((size_t)kShards * (b.mover_cap / kShards * 2 + 64) * 4);
@@ -1047,6 +1061,21 @@ int moe_layer_set_option(moe_layer_t* h, int key, long long v) {
     case MOE_OPT_FAULT_DROP_TASK:
       h->fault_drop = v < 0 ? -1 : (int)v;
       break;
+    case MOE_OPT_FAULT_DROP_TYPE:
+      if (v != 0 && v != kTaskGather && v != kTaskGateUp && v != kTaskDown)
+        return fail(MOE_E_INVAL, "dropped task type must be 0, 2 (gather), 3 (gate/up) or 4 (down)");
+      h->fault_drop_type = (int)v;
+      break;
+    case MOE_OPT_FAULT_CORRUPT_COUNT:
+      if (v < -(1 << 20) || v > (1 << 20)) return fail(MOE_E_INVAL, "count corruption out of range");
+      h->fault_corrupt = (int)v;
+      break;
+    case MOE_OPT_FAULT_REPUSH:
+      h->fault_repush = v < 0 ? -1 : (int)std::min<long long>(v, 1 << 30);
+      break;
+    case MOE_OPT_DEBUG_CLAIMS:
+      h->debug_claims = v ? 1 : 0;
+      break;
     case MOE_OPT_CLAIM_AHEAD:
       if (v < -1) return fail(MOE_E_INVAL, "claim-ahead depth must be -1, 0 or positive");
       h->ahead_opt = (int)v;
@@ -1193,6 +1222,9 @@ int forward_impl(moe_layer_t* h, int T, const void* x, const void* router_w, con
   p.mover_seg = h->B.mover_cap / kShards * 2 + 64;
   p.gemm_seg = h->B.gemm_cap / kShards * 2 + 64;
   p.fault_drop = h->fault_drop;
+  p.fault_drop_type = h->fault_drop_type;
+  p.fault_corrupt = h->fault_corrupt;
+  p.fault_repush = h->fault_repush;
   p.mover_override = h->mover_override;
   p.trace = h->trace;
   p.trace_cap = h->trace_cap;
@@ -1255,6 +1287,12 @@ int forward_impl(moe_layer_t* h, int T, const void* x, const void* router_w, con
   p.ring_gemm = reinterpret_cast<int*>(w + h->o_ring_g);
   p.ring_gemm_lo = reinterpret_cast<int*>(w + h->o_ring_gl);
   p.sched = reinterpret_cast<Sched*>(w + h->o_sched);
+  p.claimed = h->debug_claims ? reinterpret_cast<uint32_t*>(w + h->o_claimed) : nullptr;
+  p.claim_gather_off = h->B.claim_gather_off;
+  p.claim_gateup_off = h->B.claim_gateup_off;
+  p.claim_down_off = h->B.claim_down_off;
+  p.claim_comb_off = h->B.claim_comb_off;
+  p.claim_bits = h->B.claim_bits;
   p.rpart = reinterpret_cast<float*>(w + h->o_rpart);
   p.rsplit_done = reinterpret_cast<int*>(w + h->o_rsd);
 

@@ -500,10 +500,17 @@ __device__ void plan_task(const Params& p, char* scratch, Ctrl* c, bool push) {
     const int n = ntile * E;
     for (int i = tid; i < n; i += kThreads) p.tile_cnt[i] = tb[i];
   }
+  // fault injection (host-set): a wrong count, which the check below catches
+  if (tid == 0 && p.fault_corrupt != 0) cnt[0] += p.fault_corrupt;
   cta_sync();
   if (threadIdx.x == 0) c->plan_t[1] = globaltimer();
   int total = 0;
   const int off = block_exclusive_scan(tid < E ? cnt[tid] : 0, &total, c);
+  // every token chose k experts: the counts must add up to T k
+  if (total != p.T * k) {
+    if (tid == 0) set_status(p, MOE_E_DEVICE, 9);
+    return;
+  }
   if (tid < E) {
     p.offsets[tid] = off;
     offs[tid] = off;
@@ -1613,6 +1620,26 @@ __device__ bool route_task(const Params& p, const Maps& maps, int pt, int split,
   return tile_done;
 }
 
+// ------------------------------------------------------------------ claimed-twice check
+// (debug) Mark a task claimed in the bitmap; a second claim of the same task,
+// or an id outside the layer's tasks, sets MOE_E_DEVICE.  One thread.
+__device__ __forceinline__ void check_claim(const Params& p, int task) {
+  if (!p.claimed) return;
+  const int type = task_type(task), pl = task_payload(task);
+  int bit = -1;
+  if (type == kTaskRoute) bit = pl < p.n_route_tasks ? pl : -1;
+  else if (type == kTaskGather) bit = p.claim_gather_off + pl;
+  else if (type == kTaskGateUp) bit = p.claim_gateup_off + pl;
+  else if (type == kTaskDown) bit = p.claim_down_off + pl;
+  else if (type == kTaskCombine) bit = p.claim_comb_off + pl;
+  if (bit < 0 || bit >= p.claim_bits) {
+    set_status(p, MOE_E_DEVICE, 51);
+    return;
+  }
+  const uint32_t m = 1u << (bit & 31);
+  if (atomicOr(p.claimed + (bit >> 5), m) & m) set_status(p, MOE_E_DEVICE, 50);
+}
+
 // ------------------------------------------------------------------ notifications
 // (persistent mode) Run by the scheduler warp, all 32 lanes, after the
 // compute warps handed a finished task over (their writes were released to
@@ -1736,9 +1763,18 @@ __device__ void notify_down_done(const Params& p, int task) {
 }
 
 // The notification of one finished task (any type; router tiles and combines
-// feed no counter here).
+// feed no counter here).  Host-set fault injection: every notification of
+// one task type dropped (its dependents are never released: the claims run
+// out of time), or one finished gate/up task pushed again (claimed twice).
 __device__ void sched_notify(const Params& p, int task) {
   const int type = task_type(task), pl = task_payload(task);
+  if (type == p.fault_drop_type) return;
+  if (type == kTaskGateUp && p.fault_repush >= 0) {
+    int again = 0;
+    if ((threadIdx.x & 31) == 0) again = atomicAdd(&p.sched->repush_seen, 1) == p.fault_repush;
+    if (__shfl_sync(0xffffffffu, again, 0))
+      push_gen_warp(p, gemm_queue(p), 1, [=](int) { return task; });
+  }
   if (type == kTaskGather) notify_gather_done(p, pl >> 3);
   else if (type == kTaskGateUp) notify_gateup_done(p, pl / p.n_ftiles);
   else if (type == kTaskDown) notify_down_done(p, task);

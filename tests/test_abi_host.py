@@ -90,6 +90,31 @@ def test_new_options_validate_without_device(lib):
         lib.moe_layer_destroy(h)
 
 
+def test_worker_width_split_and_fault_options_validate_without_device(lib):
+    h = lib.moe_layer_create(2048, 768, 128, 8, 0)
+    try:
+        opt = pkg.OPTIONS
+        for v in (0, 1, 2):
+            assert lib.moe_layer_set_option(h, opt["pair"], v) == 0
+        for v in (-1, 3, 4):
+            assert lib.moe_layer_set_option(h, opt["pair"], v) == pkg.MOE_E_INVAL
+        for v in (-1, 0, 1):
+            assert lib.moe_layer_set_option(h, opt["front_split"], v) == 0
+        assert lib.moe_layer_set_option(h, opt["front_split"], 2) == pkg.MOE_E_INVAL
+        for v in (0, 2, 3, 4):
+            assert lib.moe_layer_set_option(h, opt["fault_drop_type"], v) == 0
+        for v in (1, 5, -1):  # router tiles and combines feed no counter
+            assert lib.moe_layer_set_option(h, opt["fault_drop_type"], v) == pkg.MOE_E_INVAL
+        assert lib.moe_layer_set_option(h, opt["fault_corrupt_count"], 3) == 0
+        assert lib.moe_layer_set_option(h, opt["fault_corrupt_count"], 1 << 21) == pkg.MOE_E_INVAL
+        assert lib.moe_layer_set_option(h, opt["fault_repush"], 5) == 0
+        assert lib.moe_layer_set_option(h, opt["debug_claims"], 1) == 0
+        # statistics of a layer that has not run a forward
+        assert lib.moe_layer_get_stat(h, pkg.STATS["pair"]) == -1
+    finally:
+        lib.moe_layer_destroy(h)
+
+
 def test_residual_norm_entry_validates_without_device(lib):
     h = lib.moe_layer_create(2048, 768, 128, 8, 0)
     try:
