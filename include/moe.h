@@ -157,6 +157,17 @@ typedef struct moe_layer moe_layer_t;
                                   outside the layer's tasks) sets
                                   MOE_E_DEVICE, never a trap; 0 (default) off */
 
+#define MOE_OPT_FOLD_GATHER 22 /* 1: a routed gate/up tile gathers its token
+                                  rows from x itself (warps idle during its
+                                  main loop copy them into the stages through
+                                  perm, 16 bytes at a time), and the gather
+                                  tasks only write perm and pos; 0 (default):
+                                  the gather tasks copy the rows into a
+                                  permuted buffer that the tiles load by TMA.
+                                  Same bits either way; 1 is slower on this
+                                  GPU (the copies keep too few bytes in
+                                  flight)                                    */
+
 /* statistics keys for moe_layer_get_stat (values of the last forward;
  * moe_layer_status must have been called after it) */
 #define MOE_STAT_MOVER_CTAS 1  /* mover workers the cost model chose          */

@@ -24,7 +24,7 @@ OPTIONS = {
     "tokens_per_tile": 6, "fault_drop_task": 7, "route_tokens": 8, "claim_ahead": 9,
     "trace": 10, "release": 11, "prefetch": 12, "bands": 13, "route_splits": 14, "l2_prefetch": 15,
     "pair": 16, "front_split": 17, "fault_drop_type": 18, "fault_corrupt_count": 19,
-    "fault_repush": 20, "debug_claims": 21,
+    "fault_repush": 20, "debug_claims": 21, "fold_gather": 22,
 }
 STATS = {"mover_ctas": 1, "tasks": 2, "grid": 3, "gemm_tasks": 4, "mover_tasks": 5, "stolen": 6,
          "ahead": 7, "trace_records": 8, "tile_tokens": 9, "split_k": 10, "bands": 11, "y_bytes": 12,

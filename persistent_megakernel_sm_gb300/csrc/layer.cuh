@@ -134,6 +134,7 @@ struct Params {
   int ahead_depth;   // claim the next task early when this many wait (0 = never)
   int index_order;   // the plan keeps experts in index order (not by count)
   int front_split;   // after the plan only mover workers prefer gathers (else every worker)
+  int fold_gather;   // routed gate/up tiles gather their token rows from x themselves
   long long l2_pf_bytes;  // gate/up weight bytes prefetched into L2 at launch (0 = none)
   unsigned long long timeout_ns;
   // cost model constants

@@ -50,6 +50,7 @@ __device__ __forceinline__ void cta_setup(const Params& p, const Maps& maps, cha
     }
     mbar_init(&c->acc_bar, 1);
     mbar_init(&c->tmem_empty, 1);
+    for (int s = 0; s < p.stages; ++s) mbar_init(&c->bfull_bar[s], P);
     mbar_init(&c->gbar, 1);
     mbar_init(&c->cbar[0], 1);
     mbar_init(&c->cbar[1], 1);
@@ -80,6 +81,7 @@ __device__ __forceinline__ void cta_setup(const Params& p, const Maps& maps, cha
   st.worker = (int)(blockIdx.x / P);
   st.lead_ctrl = pair ? mapa_shared(smem_u32(c), 0) : smem_u32(c);
   st.pipe_it = 0;
+  st.bphase = 0;
   st.gemm_count = 0;
   st.deadline = c->deadline;
   st.role_mover = 0;
@@ -654,6 +656,11 @@ struct moe_layer {
   // options
   int pair_opt = 0;  // CTAs per worker: 0 = automatic, 1, 2
   int front_split = -1;  // the spatial split also governs the gathers: -1 = auto
+  // routed gate/up tiles gather their token rows themselves: off by default
+  // -- bit-identical, but the 16-byte copies keep too few bytes in flight
+  // beside the weight stream (gate/up tiles 49 -> 99 us on decode, 50 -> 107
+  // us on skew; decode 522 -> 800 us, prefill 6260 -> 10340 us on one box)
+  int fold_gather = 0;
   int mode = MOE_MODE_PERSISTENT;
   unsigned long long timeout_ns = 2000000000ull;
   int mover_override = 0;
@@ -1116,6 +1123,9 @@ int moe_layer_set_option(moe_layer_t* h, int key, long long v) {
       if (v < 0 || v > kMaxRouteKs) return fail(MOE_E_INVAL, "router K splits must be 0..8");
       h->route_splits = (int)v;
       break;
+    case MOE_OPT_FOLD_GATHER:
+      h->fold_gather = v ? 1 : 0;
+      break;
     case MOE_OPT_FRONT_SPLIT:
       if (v < -1 || v > 1) return fail(MOE_E_INVAL, "front split must be -1 (auto), 0 or 1");
       h->front_split = (int)v;
@@ -1204,6 +1214,7 @@ int forward_impl(moe_layer_t* h, int T, const void* x, const void* router_w, con
   // 1039 us on one box), off with one, whose ready tiles would then run
   // before the routed experts' (prefill layer 6468 -> 6986 us)
   p.front_split = h->front_split < 0 ? (h->S == 0 ? 1 : 0) : h->front_split;
+  p.fold_gather = h->fold_gather;
   p.ct = tl.ct;
   // d bands: the down tiles of the last quarter of d (at least one tile)
   // have low priority, so the other band's combines overlap them

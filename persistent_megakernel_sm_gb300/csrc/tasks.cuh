@@ -18,6 +18,7 @@ struct Ctrl {
   uint64_t empty_bar[8];  // stage s free again (the leader's MMAs commit to both CTAs')
   uint64_t acc_bar;       // the tile's accumulators are complete (committed to both CTAs')
   uint64_t tmem_empty;    // (leader's is used) the peer finished reading its TMEM, once per GEMM task
+  uint64_t bfull_bar[8];  // (leader's are used) gathered token rows of stage s in every CTA
   unsigned long long deadline;
   unsigned long long t_claim, t_start;
   uint32_t tmem_base;
@@ -52,6 +53,7 @@ struct Ctrl {
 // Per-thread state that lives across tasks.
 struct CtaState {
   int rank;             // cluster rank: 0 = the worker's leader (issues the MMAs), 1 = a pair's peer
+  uint32_t bphase;      // MMA thread: parity bit per stage of the gathered-row barriers
   int worker;           // worker index (blockIdx.x / CTAs per worker)
   uint32_t lead_ctrl;   // the leader's Ctrl in the cluster's shared window (own for one CTA)
   uint32_t pipe_it;     // k blocks issued / consumed so far (producer & MMA thread)
@@ -690,8 +692,9 @@ __device__ void gather_task(const Params& p, int g, int chunk, int half, int nha
       if (__ldcg(p.idx + (size_t)t * p.k + j) == G.e) p.pos[(size_t)t * p.k + j] = r;
   }
   cta_sync();
-  if (threadIdx.x == 0 && nr <= 0) st_release_cta_shared(&c->mb_late, st.taken);
-  if (threadIdx.x == 0 && nr > 0) {
+  // folded gathers: the gate/up tiles read the token rows of x through perm
+  if (threadIdx.x == 0 && (nr <= 0 || p.fold_gather)) st_release_cta_shared(&c->mb_late, st.taken);
+  if (threadIdx.x == 0 && nr > 0 && !p.fold_gather) {
     const uint32_t row_bytes = (uint32_t)p.d * 2;
     const int cap = max(1, (int)(((size_t)p.stages * p.stage_bytes) / row_bytes));
     fence_proxy_async_shared();
@@ -970,6 +973,8 @@ struct GemmJob {
   int b_rows;             // B rows this CTA loads (n_mma / P, in boxes of 32 rows)
   int n_mma;              // MMA N (multiple of 16 P, <= 256)
   int b_off;              // byte offset of the B tile inside a stage (1024-aligned)
+  const int* gperm;       // non-null: B rows gathered from x, row r = token gperm[r] ...
+  int b_valid;            // ... for r < b_valid (the others are left unwritten)
   int kb0, nkb;           // first k block and number of k blocks
   bool a_stream;          // A is read by this task only (L2 evict-first); else kept (evict-last)
   int task;               // task id (-1: not a queue task)
@@ -995,7 +1000,7 @@ template <int P>
 __device__ int issue_loads(const Params& p, const GemmJob& job, char* smem, Ctrl* c,
                            const CtaState& st, uint32_t it0, int kb_from, int kb_to,
                            uint64_t pol_a, uint64_t pol_b) {
-  const int nbox = ceil_div(job.b_rows, kBBoxRows);
+  const int nbox = job.gperm ? 0 : ceil_div(job.b_rows, kBBoxRows);  // gathered B: not by TMA
   const bool two = job.a1 != nullptr;
   const uint32_t bytes = (two ? 2u : 1u) * kABoxBytes + (uint32_t)nbox * kBBoxBytes;
   const uint32_t full0 = st.lead_ctrl + (uint32_t)offsetof(Ctrl, full_bar);
@@ -1023,6 +1028,85 @@ __device__ int issue_loads(const Params& p, const GemmJob& job, char* smem, Ctrl
     }
   }
   return kb - kb_from;
+}
+
+// Barrier of the 128 B-gathering threads (warps 2-5): true on every thread
+// when any of them passes true.
+__device__ __forceinline__ bool bthreads_any(bool pred) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.s32 p, %1, 0;\n\t"
+      "bar.red.or.pred p, 2, 128, p;\n\t"
+      "selp.s32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(pred ? 1 : 0)
+      : "memory");
+  return r != 0;
+}
+
+// The gathered B operand of a routed gate/up tile (the folded gather, a5 into
+// a6): warps 2-5 -- idle during the main loop -- copy each of this CTA's token
+// rows' eight 16-byte chunks of every k block from x straight into the stage,
+// at the offsets the 128-byte swizzle gives a TMA box (row r at
+// (r / 8) * 1024 + (r % 8) * 128, chunk c at ((c ^ (r % 8)) * 16)).  Thread t
+// takes chunk t % 8 of rows t / 8 + 16 j (j < 16: up to 256 rows).  A stage is signalled on the
+// leader's barrier bfull[s] (one arrival per CTA) once its copies are
+// complete and fenced to the async proxy, up to three stages behind the
+// copies in flight.  Returns false on a timeout (status set); the outcome is the same
+// on all 128 threads.
+template <int P>
+__device__ bool gather_b_loads(const Params& p, const GemmJob& job, char* smem, Ctrl* c,
+                               const CtaState& st) {
+  const int lag = min(3, p.stages - 1);  // stages of copies in flight per thread
+  const int bt = (int)threadIdx.x - 64;
+  const int chunk = bt & 7, r0 = bt >> 3;
+  // rows r0 + 16 j, up to the 256 rows a one-CTA tile holds (128 for a pair)
+  int tok[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int r = r0 + 16 * j;
+    tok[j] = r < job.b_valid ? __ldcg(job.gperm + r) : -1;
+    if (tok[j] >= p.T) tok[j] = -1;  // (never: perm holds token ids)
+  }
+  const uint32_t bfull0 = st.lead_ctrl + (uint32_t)offsetof(Ctrl, bfull_bar);
+  auto signal = [&](uint32_t it) {  // every B thread: its copies of stage `it` landed
+    fence_proxy_async_shared();
+    bthreads_any(false);
+    if (bt == 0) mbar_arrive_cluster(bfull0 + 8u * (it % p.stages));
+  };
+  uint32_t it = st.pipe_it, sig = st.pipe_it;
+  bool ok = true;
+  for (int kb = 0; kb < job.nkb; ++kb, ++it) {
+    const uint32_t s = it % p.stages, ph = (it / p.stages) & 1u;
+    const bool fail = bt == 0 && !mbar_wait(&c->empty_bar[s], ph ^ 1u, st.deadline);
+    if (bthreads_any(fail)) {
+      ok = false;
+      break;
+    }
+    char* dst0 = smem + (size_t)s * p.stage_bytes + job.b_off;
+    const __nv_bfloat16* src0 = p.x + (size_t)(job.kb0 + kb) * kBK + chunk * 8;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int r = r0 + 16 * j;
+      if (tok[j] >= 0)
+        cp_async16(dst0 + (r >> 3) * 1024 + (r & 7) * 128 + (chunk ^ (r & 7)) * 16,
+                   src0 + (size_t)tok[j] * p.d);
+    }
+    cp_async_commit();
+    // signal the oldest stage once `lag` are in flight; lag < stages, so the
+    // copies of stage it never wait on a stage that is not yet signalled
+    if (it + 1 - sig >= (uint32_t)lag) {
+      if (lag >= 3) cp_async_wait<2>();
+      else if (lag == 2) cp_async_wait<1>();
+      else cp_async_wait<0>();
+      signal(sig++);
+    }
+  }
+  cp_async_wait<0>();
+  if (!ok) return false;
+  while (sig < it) signal(sig++);
+  return true;
 }
 
 template <int P>
@@ -1108,6 +1192,18 @@ __device__ bool gemm_mainloop(const Params& p, const Maps& maps, const GemmJob& 
           ok = false;
           break;
         }
+        if (job.gperm) {  // the gathered token rows of this stage, in every CTA
+          bool got;
+          const uint32_t bpar = (st.bphase >> s) & 1u;
+          while (!(got = mbar_try_wait_cluster(&c->bfull_bar[s], bpar)))
+            if (globaltimer() > st.deadline) break;
+          if (!got) {
+            set_status(p, MOE_E_TIMEOUT, 15);
+            ok = false;
+            break;
+          }
+          st.bphase ^= 1u << s;
+        }
         tc_fence_after();
         const uint32_t base = smem_u32(smem + (size_t)s * p.stage_bytes);
         const uint64_t da0 = sw128_desc(base), da1 = sw128_desc(base + kABoxBytes);
@@ -1125,6 +1221,9 @@ __device__ bool gemm_mainloop(const Params& p, const Maps& maps, const GemmJob& 
     }
     // (also after a failure, so that the epilogue warps stop waiting)
     mma_commit_all<P>(&c->acc_bar);
+  } else if (job.gperm && warp >= 2 && warp < 6) {
+    ok = gather_b_loads<P>(p, job, smem, c, st);
+    if (!ok && threadIdx.x == 64) set_status(p, MOE_E_TIMEOUT, 16);
   }
   st.pipe_it += job.nkb;
   // everyone waits for the accumulators (the leader's commit reaches every CTA)
@@ -1171,6 +1270,10 @@ __device__ bool make_gemm_job(const Params& p, const Maps& maps, int task, int r
     job.b_row0 = G.src_row0 + rank * (job.n_mma / p.pair);
     job.b_rows = job.n_mma / p.pair;
     job.b_off = 2 * kABoxBytes;
+    // a routed group's token rows, gathered from x through perm (folded
+    // gathers); the shared expert's are consecutive rows of x (TMA)
+    job.gperm = (p.fold_gather && G.e < p.E) ? p.perm + job.b_row0 : nullptr;
+    job.b_valid = max(0, min(job.b_rows, G.nrows - rank * job.b_rows));
     job.kb0 = 0;
     job.nkb = p.d / kBK;
     job.a_stream = G.nsib == 1;
@@ -1193,6 +1296,8 @@ __device__ bool make_gemm_job(const Params& p, const Maps& maps, int task, int r
     job.b_row0 = G.row0 + rank * (job.n_mma / p.pair);
     job.b_rows = job.n_mma / p.pair;
     job.b_off = 2 * kABoxBytes;
+    job.gperm = nullptr;
+    job.b_valid = job.b_rows;
     job.kb0 = ksplit * p.kb_down;
     job.nkb = p.kb_down;
     job.a_stream = G.nsib == 1;
@@ -1526,6 +1631,8 @@ __device__ bool route_task(const Params& p, const Maps& maps, int pt, int split,
   job.b_rows = nmma / P;
   job.n_mma = nmma;
   job.b_off = kABoxBytes;
+  job.gperm = nullptr;
+  job.b_valid = job.b_rows;
   job.kb0 = split * nkb / ks;
   job.nkb = (split + 1) * nkb / ks - job.kb0;
   job.a_stream = true;  // x rows: read by this tile only; Wr (B) is shared by all tiles

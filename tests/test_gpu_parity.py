@@ -121,3 +121,18 @@ def test_smaller_T_than_reserved_and_repeat():
     layer.forward(dev["x"][:0], dev["router_w"], dev["w_gate"], dev["w_up"], dev["w_down"], out)
     layer.check()
     layer.close()
+
+
+@pytest.mark.parametrize("pair", [1, 2])
+@pytest.mark.parametrize("name", ["tiny", "shared_partial_dtile", "multi_mtile_skew", "wide_E"])
+def test_folded_gather_bit_identical(name, pair):
+    # gate/up tiles gathering their token rows from x themselves, against the
+    # gather tasks copying them into the permuted buffer: the same bits
+    T, d, E, k, f, S, b = CASES[name]
+    w, inp = hz.custom_case(T, d, E, k, f, S, b)
+    folded = _full_check(w, inp, pair=pair, fold_gather=1)
+    copied = _full_check(w, inp, pair=pair, fold_gather=0)
+    assert np.array_equal(folded, copied), "folded and copied gathers differ"
+    for mode in ("multikernel", "static"):
+        other = _full_check(w, inp, mode, pair=pair, fold_gather=1)
+        assert np.array_equal(folded, other), mode
