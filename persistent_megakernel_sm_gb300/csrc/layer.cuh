@@ -31,6 +31,7 @@ constexpr int kMaxK = 16;
 constexpr int kMaxD = 32768;        // model dim limit: one bf16 row (64 KB) fits a gather round
 constexpr int kTmemCols = 512;
 constexpr int kAcc1Col = 256;       // second accumulator's first TMEM column
+constexpr int kEpiBytes = 1024;     // GEMM epilogue staging per compute warp (16 x 32 bf16)
 
 // release policies of the gate/up tiles
 constexpr int kReleaseAll = 0;

@@ -39,15 +39,23 @@ struct Ctrl {
   int qbase[kShards];
   unsigned long long plan_t[8];  // plan phase timestamps (trace only)
   int pl_cb[kMaxE], pl_sib[kMaxE], pl_cpg[kMaxE];  // plan: per expert slot
-  int tok[kThreads];      // scratch: token ids / combine tiles per row
-  int cnt[kMaxE];         // scratch: per-expert counts
-  int aux[kMaxE];
-  int aux2[kMaxE];
-  float wsum[kThreads];
   uint64_t gbar;                 // bulk-copy barrier of the gather
   uint64_t cbar[2];              // bulk-copy barriers of the combine (two buffers)
-  uint32_t mask[kMaxE * 4];      // router: 128-bit token mask per expert
   alignas(16) float bias_s[kMaxE];
+  // Scratch of one task at a time.  The router, plan, gather and combine
+  // tasks use the named arrays; a GEMM task's epilogue (which never runs
+  // beside them in one CTA) reuses the same bytes to stage its stores.
+  union {
+    struct {
+      int tok[kThreads];      // token ids / combine tiles per row
+      int cnt[kMaxE];         // per-expert counts
+      int aux[kMaxE];
+      int aux2[kMaxE];
+      float wsum[kThreads];
+      uint32_t mask[kMaxE * 4];  // router: 128-bit token mask per expert
+    };
+    alignas(16) char epi[kThreads / 32][kEpiBytes];  // one staging block per compute warp
+  };
 };
 
 // Per-thread state that lives across tasks.
@@ -1250,7 +1258,54 @@ __device__ __forceinline__ void gemm_task_end(Ctrl* c, CtaState& st) {
   }
 }
 
-__device__ __forceinline__ float silu_f(float z) { return z / (1.f + __expf(-z)); }
+// SiLU with the approximate divide: an IEEE division here cost the gate/up
+// epilogue two thirds of its time.  For z < -88 the denominator overflows
+// and the result is -0 (the exact value is below 1e-36 in magnitude).
+__device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.f + __expf(-z)); }
+
+// A warp's epilogue writes a block of 16 rows x 32 consecutive columns of a
+// row-major output (row stride `ld` elements), lane j holding column j of
+// every row.  Element-wise stores would put 64 bytes in each warp store; the
+// block goes through the warp's 1 KB staging area instead and leaves as
+// 16-byte vectors, 4 lanes per 64-byte row segment.  Rows >= nrows are not
+// written; `col_ok` false skips the whole block.
+__device__ __forceinline__ void warp_store_bf16_16x32(char* stg, const float (&v)[16], int lane,
+                                                      __nv_bfloat16* dst, size_t ld, int nrows,
+                                                      bool col_ok) {
+  __nv_bfloat16* s16 = reinterpret_cast<__nv_bfloat16*>(stg);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) s16[i * 32 + lane] = __float2bfloat16_rn(v[i]);
+  __syncwarp();
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const int e = lane + 32 * j, i = e >> 2, cc = e & 3;
+    if (col_ok && i < nrows)
+      *reinterpret_cast<uint4*>(dst + i * ld + cc * 8) =
+          *reinterpret_cast<const uint4*>(stg + i * 64 + cc * 16);
+  }
+  __syncwarp();
+}
+
+// The same for fp32 values, eight rows (1 KB) at a time.
+__device__ __forceinline__ void warp_store_f32_16x32(char* stg, const float (&v)[16], int lane,
+                                                     float* dst, size_t ld, int nrows,
+                                                     bool col_ok) {
+  float* sf = reinterpret_cast<float*>(stg);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sf[i * 32 + lane] = v[h * 8 + i];
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int e = lane + 32 * j, i = e >> 3, cc = e & 7, r = h * 8 + i;
+      if (col_ok && r < nrows)
+        *reinterpret_cast<float4*>(dst + r * ld + cc * 4) =
+            *reinterpret_cast<const float4*>(stg + i * 128 + cc * 16);
+    }
+    __syncwarp();
+  }
+}
 
 // The GEMM job of a gate/up or down task id for the CTA of rank `rank` in
 // its worker (false for other task types or an inconsistent group).
@@ -1323,19 +1378,19 @@ __device__ void gateup_task(const Params& p, const Maps& maps, int task, char* s
   if (ok) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q = warp & 3, half = warp >> 2;
-    // this thread's f row: row m of this CTA's 128 rows of the tile
-    const int frow = ft * ftile_rows(p) + st.rank * kBM + q * 32 + lane;
-    const bool in_f = frow < p.f;  // the last tile of an f that is an odd multiple of 128
+    // this warp's 32 f rows: rows q*32.. of this CTA's 128 rows of the tile
+    // (the TMEM lanes it may read); lane j holds f row f0 + j
+    const int f0 = ft * ftile_rows(p) + st.rank * kBM + q * 32;
+    const bool in_f = f0 < p.f;  // the last tile of an f that is an odd multiple of 128
     const uint32_t lane_addr = c->tmem_base + ((uint32_t)(q * 32) << 16);
-    __nv_bfloat16* hcol = p.H + (size_t)G.row0 * p.f + frow;
+    __nv_bfloat16* hblk = p.H + (size_t)G.row0 * p.f + f0;
     for (int ch = half; ch * 16 < G.nrows; ch += 2) {
       float gv[16], uv[16];
       tmem_ld2x16(lane_addr + ch * 16, lane_addr + kAcc1Col + ch * 16, gv, uv);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int n = ch * 16 + i;
-        if (in_f && n < G.nrows) hcol[(size_t)n * p.f] = __float2bfloat16_rn(silu_f(gv[i]) * uv[i]);
-      }
+      for (int i = 0; i < 16; ++i) gv[i] = silu_f(gv[i]) * uv[i];
+      warp_store_bf16_16x32(c->epi[warp], gv, lane, hblk + (size_t)ch * 16 * p.f, p.f,
+                            G.nrows - ch * 16, in_f);
     }
   }
   gemm_task_end<P>(c, st);
@@ -1359,37 +1414,25 @@ __device__ void down_task(const Params& p, const Maps& maps, int task, char* sme
   if (ok) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q = warp & 3, half = warp >> 2;
-    // this thread's two d columns: row m of this CTA's 128 rows of each
-    // accumulator
-    const int col0 = dt * dtile_rows(p) + st.rank * kBM + q * 32 + lane;
-    const int col1 = col0 + ftile_rows(p);
+    // this warp's two blocks of 32 d columns: rows q*32.. of this CTA's 128
+    // rows of each accumulator; lane j holds columns d0 + j and d1 + j
+    const int d0 = dt * dtile_rows(p) + st.rank * kBM + q * 32;
+    const int d1 = d0 + ftile_rows(p);
     const uint32_t lane_addr = c->tmem_base + ((uint32_t)(q * 32) << 16);
-    const bool has0 = col0 < p.d, has1 = col1 < p.d;
+    const bool has0 = d0 < p.d, has1 = d1 < p.d;
     for (int ch = half; ch * 16 < G.nrows; ch += 2) {
       float a[16], b[16];
       tmem_ld2x16(lane_addr + ch * 16, lane_addr + kAcc1Col + ch * 16, a, b);
+      const size_t row = (size_t)G.row0 + ch * 16;
+      const int nr = G.nrows - ch * 16;
       if (p.y_f32) {
-        float* Y = reinterpret_cast<float*>(p.Y) + (size_t)ksplit * p.rows_y * p.d;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int n = ch * 16 + i;
-          if (n < G.nrows) {
-            float* yr = Y + (size_t)(G.row0 + n) * p.d;
-            if (has0) yr[col0] = a[i];
-            if (has1) yr[col1] = b[i];
-          }
-        }
+        float* Y = reinterpret_cast<float*>(p.Y) + (size_t)ksplit * p.rows_y * p.d + row * p.d;
+        warp_store_f32_16x32(c->epi[warp], a, lane, Y + d0, p.d, nr, has0);
+        warp_store_f32_16x32(c->epi[warp], b, lane, Y + d1, p.d, nr, has1);
       } else {
-        __nv_bfloat16* Y = reinterpret_cast<__nv_bfloat16*>(p.Y);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int n = ch * 16 + i;
-          if (n < G.nrows) {
-            __nv_bfloat16* yr = Y + (size_t)(G.row0 + n) * p.d;
-            if (has0) yr[col0] = __float2bfloat16_rn(a[i]);
-            if (has1) yr[col1] = __float2bfloat16_rn(b[i]);
-          }
-        }
+        __nv_bfloat16* Y = reinterpret_cast<__nv_bfloat16*>(p.Y) + row * p.d;
+        warp_store_bf16_16x32(c->epi[warp], a, lane, Y + d0, p.d, nr, has0);
+        warp_store_bf16_16x32(c->epi[warp], b, lane, Y + d1, p.d, nr, has1);
       }
     }
   }
