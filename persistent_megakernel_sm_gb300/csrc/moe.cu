@@ -89,6 +89,7 @@ __device__ __forceinline__ void cta_setup(const Params& p, const Maps& maps, cha
   st.comb_phase = 0;
   st.exit_reason = 0;
   st.polls = 0;
+  st.claims = 0;
   st.plan_seen = false;
   st.n_gather = st.mover_total = st.gemm_total = 0;
   st.pf_task = -1;

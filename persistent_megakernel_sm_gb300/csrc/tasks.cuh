@@ -72,6 +72,7 @@ struct CtaState {
   uint32_t comb_phase;    // parities of the two combine barriers (bits 0, 1; all threads)
   int exit_reason;        // why the scheduler warp stopped (trace only): 1 done, 2 abort, 3 deadline
   unsigned polls;         // scheduler warp: claims that found nothing while idle (trace only)
+  unsigned claims;        // scheduler warp: tasks claimed so far (rotates the home shard)
   bool plan_seen;         // scheduler warp: the plan's totals below are cached
   int n_gather, mover_total, gemm_total, gemm_lo_total;
   int pf_task, pf_count;  // producer: task whose first k blocks are already loading
@@ -386,7 +387,15 @@ __device__ int claim_once(const Params& p, CtaState& st, int min_depth) {
   const bool mover_first =
       !st.plan_seen || (gathers_left && !p.front_split) || st.role_mover;
   const int npass = min_depth > 1 ? 1 : 3;
-  const int home = st.worker & (kShards - 1);
+  // Home shard: fixed for the first multiple of kShards workers; the rest
+  // (4 of the 76 CTA pairs of a pair layer) move to the next shard after
+  // every claim.  Fixed homes alone drained the shards unevenly (10 home
+  // workers on some shards, 9 on others), and tasks pushed together -- an
+  // expert's sibling row groups, which read the same weight tiles -- drifted
+  // apart by far more than a weight tile stays in L2; moving every worker's
+  // home scattered each worker's consecutive claims instead.
+  const int fixed = p.n_workers & ~(kShards - 1);
+  const int home = (st.worker < fixed ? st.worker : st.worker + (int)st.claims) & (kShards - 1);
   for (int pass = 0; pass < npass; ++pass) {
     const int qq = mover_first ? pass : (pass == 2 ? 0 : pass + 1);
     const int depth = qq == 0 ? depth_m : qq == 1 ? depth_g : depth_l;
@@ -413,6 +422,7 @@ __device__ int claim_once(const Params& p, CtaState& st, int min_depth) {
       }
     }
     r = __shfl_sync(full, r, plane);
+    if (r >= 0) ++st.claims;
     if (r >= 0 && pass > 0 && st.plan_seen && lane == 0) atomicAdd(&s->stat_stolen, 1);
     return r;  // a task, -3, or -4 (the shard drained under us: retry)
   }
