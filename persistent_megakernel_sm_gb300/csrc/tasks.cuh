@@ -1466,9 +1466,9 @@ __device__ __forceinline__ int route_row_stride(int E) { return ((E + 15) / 16) 
 // Shared-memory bytes the router epilogue needs (logits + exchange area), for
 // either tile size (128 tokens, two threads per token; 64 tokens, four).
 __host__ __device__ __forceinline__ size_t route_smem_bytes(int E) {
-  // max [rt] + part sums [parts][rt] + (parts - 1) lists of 2 KL words per token
-  const size_t xch128 = (size_t)(1 + 2 + 1 * 2 * kMaxK) * 128;
-  const size_t xch64 = (size_t)(1 + 4 + 3 * 2 * kMaxK) * 64;
+  // (parts - 1) lists of 2 KL words per token
+  const size_t xch128 = (size_t)(1 * 2 * kMaxK) * 128;
+  const size_t xch64 = (size_t)(3 * 2 * kMaxK) * 64;
   return (size_t)kRouteTokens * (((E + 15) / 16) * 16 + 4) * 4 +
          (xch128 > xch64 ? xch128 : xch64) * 4;
 }
@@ -1504,6 +1504,32 @@ __device__ __forceinline__ void topk_merge(float (&tv)[KL], int (&te)[KL], float
   }
 }
 
+// Store a token's k per-slot values (k consecutive 32-bit words at dst):
+// 16-byte vectors when k is a multiple of 4 (dst is then 16-byte aligned),
+// 8-byte ones when k is even, else one word at a time.  A warp's stores then
+// cover its 32 tokens' rows in few wide transactions instead of k scattered
+// 4-byte stores per lane.
+template <int KL>
+__device__ __forceinline__ void store_slots(uint32_t* dst, const uint32_t (&v)[KL], int k) {
+  if constexpr (KL >= 4) {
+    if ((k & 3) == 0) {
+#pragma unroll
+      for (int s = 0; s < KL; s += 4)
+        if (s < k) *reinterpret_cast<uint4*>(dst + s) = make_uint4(v[s], v[s + 1], v[s + 2], v[s + 3]);
+      return;
+    }
+  }
+  if ((k & 1) == 0) {
+#pragma unroll
+    for (int s = 0; s < KL; s += 2)
+      if (s < k) *reinterpret_cast<uint2*>(dst + s) = make_uint2(v[s], v[s + 1]);
+    return;
+  }
+#pragma unroll
+  for (int s = 0; s < KL; ++s)
+    if (s < k) dst[s] = v[s];
+}
+
 // Epilogue of one router tile of rt tokens (p.rt: 128 or 64) whose logits
 // (without bias) sit in shared memory, token m's row at lg + m * ls.  The
 // CTA's threads split each token's experts: thread t takes token t % rt and
@@ -1511,9 +1537,9 @@ __device__ __forceinline__ void topk_merge(float (&tv)[KL], int (&te)[KL], float
 // Pass 1 keeps each range's top-KL list, four logits at a time (sorted by a
 // 4-input network, then merged); the other parts hand their lists to part 0,
 // which merges them in part order, so its list starts with the row maximum.
-// Pass 2 sums exp(L - max) over each range; part 0 adds the parts' sums in
-// part order.  Then p_j = exp(L_j - max) / sum and w_j = p_j / sum of the
-// kept p.
+// The weights follow from the kept logits alone: w_j = exp(L_j - max) over
+// the sum of exp(L_s - max) for the kept s (the softmax's denominator over
+// all E cancels in the renormalisation).
 template <int KL>
 __device__ __noinline__ void route_epilogue(const Params& p, Ctrl* c, int tile, int nt,
                                             const float* lg, int ls, float* xch) {
@@ -1555,11 +1581,9 @@ __device__ __noinline__ void route_epilogue(const Params& p, Ctrl* c, int tile, 
     topk_cx(nv[1], ne[1], nv[2], ne[2]);
     topk_merge<KL, 4>(tv, te, nv, ne);
   }
-  // exchange area, token-minor (conflict-free): max [rt], sums [parts][rt],
-  // then the lists of parts 1.. : values [KL][rt] and experts [KL][rt] each
-  float* x_max = xch;
-  float* x_sum = xch + rt;
-  float* x_list = xch + (size_t)(1 + parts) * rt;
+  // exchange area, token-minor (conflict-free): the lists of parts 1.. :
+  // values [KL][rt] and experts [KL][rt] each
+  float* x_list = xch;
   const size_t list_words = (size_t)2 * KL * rt;
   if (part > 0) {
     float* v = x_list + (size_t)(part - 1) * list_words;
@@ -1584,39 +1608,43 @@ __device__ __noinline__ void route_epilogue(const Params& p, Ctrl* c, int tile, 
       }
       topk_merge<KL, KL>(tv, te, bv, be);
     }
-    x_max[m] = tv[0];
   }
-  cta_sync();
-  const float mx = x_max[m];
-  float sum = 0.f;
-#pragma unroll 1
-  for (int e4 = e0; e4 < e1; e4 += 4) {
-    const float4 v4 = row[e4 >> 2], b4 = brow[e4 >> 2];
-    const float nv[4] = {v4.x + b4.x, v4.y + b4.y, v4.z + b4.z, v4.w + b4.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      if (e4 + j < e1) sum += __expf(nv[j] - mx);
-  }
-  x_sum[part * rt + m] = sum;
-  cta_sync();
+  // The renormalised weights need no softmax denominator: p_j = e_j / S over
+  // all experts and w_j = p_j / (sum of the kept p) = e_j / (sum of the kept
+  // e), with e_j = exp(L_j - max).  tv[0] is the row maximum.
   const bool valid = part == 0 && m < nt;
-  if (part == 0)
-    for (int q = 1; q < parts; ++q) sum += x_sum[q * rt + m];
-  float pk[KL];
+  float ek[KL];
   float kept = 0.f;
 #pragma unroll
   for (int s = 0; s < KL; ++s) {
-    pk[s] = s < k ? __expf(tv[s] - mx) / sum : 0.f;
-    kept += pk[s];
+    ek[s] = s < k ? __expf(tv[s] - tv[0]) : 0.f;
+    kept += ek[s];
   }
+  const float inv_kept = 1.f / kept;
   if (valid) {
     const size_t o = (size_t)(t0 + m) * k;
+    uint32_t iv[KL], wv[KL];
+#pragma unroll
+    for (int s = 0; s < KL; ++s) {
+      iv[s] = (uint32_t)te[s];
+      wv[s] = __float_as_uint(ek[s] * inv_kept);
+    }
+    store_slots<KL>(reinterpret_cast<uint32_t*>(p.idx + o), iv, k);
+    store_slots<KL>(reinterpret_cast<uint32_t*>(p.wgt + o), wv, k);
+  }
+  // the tile's token mask per expert: word m / 32 of every expert is written
+  // by the warp of tokens m / 32 * 32 .., and only by it (rt is a multiple of
+  // 32, so lane j holds token 32 (m / 32) + j); the lanes that chose the same
+  // expert in slot s merge their bits first, so each distinct expert takes
+  // one OR instead of one atomic per lane (the lanes of a warp that picked a
+  // popular expert all hit the same word)
+  if (part == 0 && (m >> 5) * 32 < nt) {
 #pragma unroll
     for (int s = 0; s < KL; ++s) {
       if (s < k) {
-        p.idx[o + s] = te[s];
-        p.wgt[o + s] = pk[s] / kept;
-        atomicOr(&c->mask[te[s] * 4 + (m >> 5)], 1u << (m & 31));
+        const int e = valid ? te[s] : -1;
+        const unsigned same = __match_any_sync(0xffffffffu, e);
+        if (valid && (threadIdx.x & 31) == __ffs(same) - 1) c->mask[e * 4 + (m >> 5)] |= same;
       }
     }
   }
@@ -1625,15 +1653,18 @@ __device__ __noinline__ void route_epilogue(const Params& p, Ctrl* c, int tile, 
     const size_t o = (size_t)(t0 + m) * k;
     const int wd = m >> 5;
     const uint32_t below = (1u << (m & 31)) - 1u;
+    uint32_t rv[KL];
 #pragma unroll
     for (int s = 0; s < KL; ++s) {
+      rv[s] = 0u;
       if (s < k) {
         const uint32_t* mk = c->mask + te[s] * 4;
         int r = __popc(mk[wd] & below);
         for (int q = 0; q < wd; ++q) r += __popc(mk[q]);
-        p.rank[o + s] = r;
+        rv[s] = (uint32_t)r;
       }
     }
+    store_slots<KL>(reinterpret_cast<uint32_t*>(p.rank + o), rv, k);
   }
   for (int e = threadIdx.x; e < E; e += kThreads) {
     const uint32_t* mk = c->mask + e * 4;
