@@ -19,6 +19,9 @@ CASES = {
     "multi_mtile_skew": (300, 256, 4, 2, 256, 0, 2.0),
     "wide_E": (96, 256, 64, 8, 256, 0, 1.0),
     "top16": (40, 128, 32, 16, 128, 1, 0.0),
+    # odd k above 1: the router stores each token's slots one word at a time
+    "odd_k3": (70, 256, 12, 3, 256, 0, 0.4),
+    "odd_k5_shared": (50, 256, 16, 5, 256, 1, 0.2),
 }
 
 
