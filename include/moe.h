@@ -14,7 +14,7 @@
  *   m.xxqk.cn/news/657744 section 2.1 (scheduling units: an expert's up
  *     projection, then its down projection, large GEMMs split along K) and
  *     section 5.1 (scheduling state lives in device memory passed to the
- *     kernel, so the launch can be captured in a CUDA graph).
+ *     kernel).
  *
  * Per token t (T tokens, model dim d, E routed experts, top-k, expert FFN
  * dim f, S in {0,1} always-on shared experts):
