@@ -1063,8 +1063,8 @@ __device__ __forceinline__ bool bthreads_any(bool pred) {
   return r != 0;
 }
 
-// The gathered B operand of a routed gate/up tile (the folded gather, a5 into
-// a6): warps 2-5 -- idle during the main loop -- copy each of this CTA's token
+// The gathered B operand of a routed gate/up tile (the gather folded into the
+// tile): warps 2-5 -- idle during the main loop -- copy each of this CTA's token
 // rows' eight 16-byte chunks of every k block from x straight into the stage,
 // at the offsets the 128-byte swizzle gives a TMA box (row r at
 // (r / 8) * 1024 + (r % 8) * 128, chunk c at ((c ^ (r % 8)) * 16)).  Thread t
