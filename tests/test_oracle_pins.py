@@ -153,6 +153,21 @@ def test_topk_with_k_equal_E_is_full_softmax():
     assert np.allclose(full, ex / ex.sum(axis=1, keepdims=True), rtol=1e-13)
 
 
+@pytest.mark.parametrize("E,k", [(8, 2), (64, 6), (128, 8), (256, 8), (32, 16)])
+def test_renormalised_weights_need_no_softmax_denominator(E, k):
+    # w_j = p_j / sum_kept p = exp(L_j - max) / sum_kept exp(L_s - max): the
+    # softmax denominator over all E cancels (the kernel computes this form,
+    # the oracle the softmax-then-renormalise one)
+    rng = np.random.default_rng(E * 31 + k)
+    L = rng.standard_normal((40, E)) * 2.5
+    idx, w, _, _ = oracle.topk(L, k)
+    for t in range(L.shape[0]):
+        kept = L[t, idx[t]]
+        e = np.exp(kept - kept.max())
+        assert kept.max() == L[t].max()
+        assert np.allclose(w[t], e / e.sum(), rtol=1e-12, atol=0)
+
+
 def test_topk_hand_example_renormalisation():
     # logits 0, ln 2, ln 3: softmax is (1, 2, 3)/6; the top two are experts 2
     # and 1, renormalised to 3/5 and 2/5.
