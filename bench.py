@@ -179,6 +179,7 @@ class ClockSampler:
         inside = [r for r in rows if self.t0 - 0.2 <= r[0] <= self.t1 + 0.2] or rows[-2:]
         sm = [float(p[1]) for _, p in inside if p[1].replace(".", "").isdigit()]
         mx = [float(p[2]) for _, p in inside if p[2].replace(".", "").isdigit()]
+        pw = [float(p[3]) for _, p in inside if p[3].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = set()
         for _, p in inside:
@@ -187,6 +188,7 @@ class ClockSampler:
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None,
+                "power_w": statistics.median(pw) if pw else None,
                 "reasons": sorted(reasons), "samples": len(inside)}
 
 
